@@ -1,0 +1,181 @@
+"""CPU fp64 oracle for the fused attention forward -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the package's smoke check and the CPU-baseline leg of the
+benchmark may import this module.  The CUDA library never calls it and has no
+fallback to it.  It shares no code with the CUDA path: the arithmetic lives in
+``attn_oracle.c`` (plain C, fp64, one explicit score row per query), which this
+wrapper compiles with gcc on first use and calls through ctypes.
+
+Definitions followed (see the header of ``attn_oracle.c`` for the steps):
+
+* ``attention``: "Skill: Write a Triton Attention Kernel", Required reasoning
+  process steps 1-8 -- O = softmax(scale * Q K^T + causal mask) V with the KV
+  head h // (H_q / H_kv), and LSE = m + ln(l) in natural log.
+* ``decode``: "Triton-FlashAttention", Phase 2 -- one query token over a cache
+  whose first ``cache_len`` positions are all valid (no causal mask).
+* ``kv_cache_write``: "Triton-FlashAttention", Phase 2 (the preallocated-cache
+  write helper kept apart from the attention math) -- a plain copy of the new
+  tokens into positions [pos, pos + n) of the cache.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(hand-derived fixtures, closed forms, invariants and planted-mistake checks).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+
+_c_double_p = ctypes.POINTER(ctypes.c_double)
+_c_int64_p = ctypes.POINTER(ctypes.c_int64)
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile a C oracle source into a shared library (gcc, -O2, IEEE arithmetic)."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+           "-o", tmp, src, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into liboracle.so next to it (if stale or missing)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(SOURCE):
+        compile_source(SOURCE, _LIB)
+    return _LIB
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_c_double_p)
+
+
+class Oracle:
+    """ctypes front end of one compiled oracle library."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        i64 = ctypes.c_int64
+        lib.oracle_attention_fwd.restype = ctypes.c_int
+        lib.oracle_attention_fwd.argtypes = [
+            _c_double_p, _c_double_p, _c_double_p, _c_double_p, _c_double_p,
+            i64, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_double, ctypes.c_int]
+        lib.oracle_attention_rows.restype = ctypes.c_int
+        lib.oracle_attention_rows.argtypes = [
+            _c_double_p, _c_double_p, _c_double_p,
+            i64, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_double,
+            _c_int64_p, i64, _c_double_p, _c_double_p, ctypes.c_int]
+        self._lib = lib
+
+    def attention(self, q, k, v, causal: bool, scale: float, nthreads: int | None = None):
+        """Full attention forward.
+
+        q: (B, H_q, N_q, D); k, v: (B, H_kv, N_kv, D) -- any real dtype, converted
+        exactly to fp64.  Returns (O (B,H_q,N_q,D) fp64, LSE (B,H_q,N_q) fp64).
+        """
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Nq, D = q.shape
+        Bk, Hkv, Nkv, Dk = k.shape
+        if v.shape != k.shape or Bk != B or Dk != D:
+            raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
+        o = np.empty((B, Hq, Nq, D), dtype=np.float64)
+        lse = np.empty((B, Hq, Nq), dtype=np.float64)
+        rc = self._lib.oracle_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                            B, Hq, Hkv, Nq, Nkv, D, 1 if causal else 0, float(scale),
+                                            nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_attention_fwd rejected the arguments (code {rc})")
+        return o, lse
+
+    def attention_rows(self, q, k, v, causal: bool, scale: float, rows, nthreads: int | None = None):
+        """Attention for selected query rows only.
+
+        rows: integer array (n, 3) of (b, h, i).  Returns (O (n, D), LSE (n,)).
+        """
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Nq, D = q.shape
+        _, Hkv, Nkv, _ = k.shape
+        sel = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+        n = sel.shape[0]
+        o = np.empty((n, D), dtype=np.float64)
+        lse = np.empty((n,), dtype=np.float64)
+        rc = self._lib.oracle_attention_rows(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, D,
+                                             1 if causal else 0, float(scale),
+                                             sel.ctypes.data_as(_c_int64_p), n, _ptr(o), _ptr(lse),
+                                             nthreads or default_threads())
+        if rc != 0:
+            raise ValueError(f"oracle_attention_rows rejected the arguments (code {rc})")
+        return o, lse
+
+    def decode(self, q, k_cache, v_cache, cache_len: int, scale: float, nthreads: int | None = None):
+        """One query token per (batch, q-head) over the first cache_len cache rows.
+
+        q: (B, H_q, D) or (B, H_q, 1, D); caches: (B, H_kv, max_len, D).
+        Returns (O (B, H_q, D), LSE (B, H_q)).
+        """
+        q = _f64(q)
+        if q.ndim == 3:
+            q = q[:, :, None, :]
+        if cache_len < 1:
+            raise ValueError("cache_len must be >= 1")
+        kc = np.asarray(k_cache)[:, :, :cache_len, :]
+        vc = np.asarray(v_cache)[:, :, :cache_len, :]
+        o, lse = self.attention(q, kc, vc, causal=False, scale=scale, nthreads=nthreads)
+        return o[:, :, 0, :], lse[:, :, 0]
+
+
+_default = None
+
+
+def _oracle() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def attention(q, k, v, causal: bool, scale: float, nthreads: int | None = None):
+    return _oracle().attention(q, k, v, causal, scale, nthreads)
+
+
+def attention_rows(q, k, v, causal: bool, scale: float, rows, nthreads: int | None = None):
+    return _oracle().attention_rows(q, k, v, causal, scale, rows, nthreads)
+
+
+def decode(q, k_cache, v_cache, cache_len: int, scale: float, nthreads: int | None = None):
+    return _oracle().decode(q, k_cache, v_cache, cache_len, scale, nthreads)
+
+
+attention.__doc__ = Oracle.attention.__doc__
+attention_rows.__doc__ = Oracle.attention_rows.__doc__
+decode.__doc__ = Oracle.decode.__doc__
+
+
+def kv_cache_write(k_cache, v_cache, k_new, v_new, pos: int):
+    """Copies of the caches with k_new/v_new (B, H_kv, n, D) placed at [pos, pos+n)."""
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    n = np.asarray(k_new).shape[2]
+    if pos < 0 or pos + n > kc.shape[2]:
+        raise ValueError("write outside the cache")
+    kc[:, :, pos:pos + n, :] = k_new
+    vc[:, :, pos:pos + n, :] = v_new
+    return kc, vc
