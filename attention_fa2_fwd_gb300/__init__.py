@@ -1,0 +1,228 @@
+"""Python binding of libattn_gb300.so -- the GB300 (sm_103a) fused attention forward.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of the shared library, reached through its C ABI (``include/attn.h``).
+PyTorch supplies device memory and streams.  If the library has not been
+built, every call raises ``AttnLibraryMissing``; there is no fallback.
+
+Low-level functions carry the C names (``attn_fwd_prefill``, ``attn_fwd_decode``,
+``kv_cache_write``, ``attn_decode_workspace_size``, ``attn_get_device_error``,
+``attn_status_string``) and take raw pointers, sizes and strides.  The
+tensor-level helpers ``prefill``, ``decode`` and ``write_kv_cache`` fill those
+arguments from PyTorch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn_gb300.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_ALIGNMENT = 3
+ATTN_ERR_WORKSPACE = 4
+ATTN_ERR_CUDA = 5
+ATTN_ERR_DEVICE_TIMEOUT = 6
+
+ATTN_F16 = 0
+ATTN_BF16 = 1
+
+# Every function that include/attn.h declares.
+EXPORTS = ("attn_fwd_prefill", "attn_decode_workspace_size", "attn_fwd_decode", "kv_cache_write",
+           "attn_get_device_error", "attn_status_string", "attn_version")
+
+
+class AttnLibraryMissing(RuntimeError):
+    pass
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+_I64x4 = ctypes.c_int64 * 4
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (built in-tree by ``attention_fa2_fwd_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise AttnLibraryMissing(
+                    f"{LIB_PATH} is missing: build it with `python -m attention_fa2_fwd_gb300.build` "
+                    "(or __graft_entry__.build()); there is no CPU fallback")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            L.attn_fwd_prefill.restype = i32
+            L.attn_fwd_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                           i64p, i64p, i64p, i64p, i32, f32, vp]
+            L.attn_decode_workspace_size.restype = ctypes.c_size_t
+            L.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+            L.attn_fwd_decode.restype = i32
+            L.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                          i64p, i64p, i64p, i64p, f32, vp, ctypes.c_size_t, vp]
+            L.kv_cache_write.restype = i32
+            L.kv_cache_write.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                         i64p, i64p, i64p, i64p, vp]
+            L.attn_get_device_error.restype = i32
+            L.attn_get_device_error.argtypes = [vp]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_status_string.argtypes = [i32]
+            L.attn_version.restype = i32
+            L.attn_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _strides(s):
+    return _I64x4(*[int(x) for x in s])
+
+
+# ------------------------------------------------------------------ C names
+
+def attn_fwd_prefill(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, k_str, v_str, o_str,
+                     causal, scale, stream) -> int:
+    return lib().attn_fwd_prefill(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, _strides(q_str),
+                                  _strides(k_str), _strides(v_str), _strides(o_str), int(causal), float(scale),
+                                  stream)
+
+
+def attn_decode_workspace_size(B, H_q, H_kv, D) -> int:
+    return int(lib().attn_decode_workspace_size(B, H_q, H_kv, D))
+
+
+def attn_fwd_decode(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, q_str, kc_str, vc_str, o_str,
+                    scale, workspace, workspace_bytes, stream) -> int:
+    return lib().attn_fwd_decode(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, _strides(q_str),
+                                 _strides(kc_str), _strides(vc_str), _strides(o_str), float(scale), workspace,
+                                 workspace_bytes, stream)
+
+
+def kv_cache_write(k_cache, v_cache, k_new, v_new, dtype, B, H_kv, n_new, D, pos, max_len, kc_str, vc_str, kn_str,
+                   vn_str, stream) -> int:
+    return lib().kv_cache_write(k_cache, v_cache, k_new, v_new, dtype, B, H_kv, n_new, D, pos, max_len,
+                                _strides(kc_str), _strides(vc_str), _strides(kn_str), _strides(vn_str), stream)
+
+
+def attn_get_device_error(stream=None) -> int:
+    return lib().attn_get_device_error(stream)
+
+
+def attn_status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def attn_version() -> int:
+    return lib().attn_version()
+
+
+# ------------------------------------------------------------------ tensor helpers
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    raise TypeError(f"unsupported dtype {t.dtype}: fp16 or bf16 only")
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_lse: bool = True, out=None,
+            lse_out=None, stream=None):
+    """Fused attention forward.  q (B,H_q,N_q,D); k, v (B,H_kv,N_kv,D) CUDA tensors.
+
+    Any (b, h, n) strides are accepted (16-byte multiples, d stride 1), so a
+    (B,N,H,D) tensor passed as its permuted (B,H,N,D) view works directly.
+    Returns (O, LSE) with O shaped like q (contiguous unless ``out`` is given)
+    and LSE (B,H_q,N_q) fp32, or None when ``return_lse`` is False.
+    """
+    import torch
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = out if out is not None else torch.empty((B, Hq, Nq, D), dtype=q.dtype, device=q.device)
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    st = attn_fwd_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D,
+                          q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
+                          _stream_handle(stream))
+    _check(st, "attn_fwd_prefill")
+    return o, lse
+
+
+def decode_workspace(B, H_q, H_kv, D, device=None):
+    """A workspace tensor of attn_decode_workspace_size bytes (None when 0 bytes)."""
+    import torch
+    n = attn_decode_workspace_size(B, H_q, H_kv, D)
+    if n == 0:
+        return None
+    return torch.empty((n + 15) // 16 * 4, dtype=torch.float32, device=device or "cuda")
+
+
+def decode(q, k_cache, v_cache, cache_len: int, scale: float | None = None, return_lse: bool = True, out=None,
+           lse_out=None, workspace=None, stream=None):
+    """One query token per (batch, q-head) over the first cache_len cache rows.
+
+    q (B,H_q,D) or (B,H_q,1,D); caches (B,H_kv,max_len,D).  Returns (O (B,H_q,D), LSE (B,H_q)).
+    """
+    import torch
+    q4 = q if q.dim() == 4 else q.unsqueeze(2)
+    B, Hq, _, D = q4.shape
+    _, Hkv, max_len, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = out if out is not None else torch.empty((B, Hq, D), dtype=q.dtype, device=q.device)
+    o4 = o.unsqueeze(2) if o.dim() == 3 else o
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, D, q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = attn_fwd_decode(q4.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o4.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, int(cache_len), D,
+                         q4.stride(), k_cache.stride(), v_cache.stride(), o4.stride(), scale, ws_ptr, ws_bytes,
+                         _stream_handle(stream))
+    _check(st, "attn_fwd_decode")
+    return o, lse
+
+
+def write_kv_cache(k_cache, v_cache, k_new, v_new, pos: int, stream=None):
+    """Copy k_new/v_new (B,H_kv,n,D) into cache rows [pos, pos+n) in place."""
+    B, Hkv, max_len, D = k_cache.shape
+    n = k_new.shape[2]
+    st = kv_cache_write(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                        _dtype_code(k_cache), B, Hkv, n, D, int(pos), max_len, k_cache.stride(), v_cache.stride(),
+                        k_new.stride(), v_new.stride(), _stream_handle(stream))
+    _check(st, "kv_cache_write")
+
+
+def check_device_error(stream=None):
+    """Synchronise and raise if a kernel recorded a failure (clears the record)."""
+    _check(attn_get_device_error(_stream_handle(stream)), "device")

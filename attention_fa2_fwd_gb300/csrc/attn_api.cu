@@ -1,0 +1,347 @@
+// attn_api.cu -- the extern "C" boundary of libattn_gb300.so.
+//
+// Host-side work only: argument validation (before anything is launched),
+// TMA tensor-map encoding, split-count selection for decode, the device error
+// word, and dispatch to the kernels in prefill.cu and decode.cu.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+__device__ unsigned g_device_error = 0;
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  unsigned *err = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_state[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device setup with the device current: SM count, architecture check and
+// the address of the device error word.
+attn_status_t device_state(const DeviceState **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState &s = g_state[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    s.supported = (major == 10 && minor == 3);
+    s.sm_count = sms;
+    if (s.supported) {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return ATTN_ERR_CUDA;
+      s.err = static_cast<unsigned *>(p);
+      if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+          return ATTN_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+    }
+    s.ready = true;
+  }
+  if (!s.supported) return ATTN_ERR_UNSUPPORTED;
+  *out = &s;
+  return ATTN_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// (b, h, n, d) element strides of a tensor with sizes sz: d stride 1, every
+// stride of an extent > 1 positive and a multiple of 8 elements (16 bytes).
+attn_status_t check_strides(const int64_t s[4], const int64_t sz[4]) {
+  if (s == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (sz[3] > 1 && s[3] != 1) return ATTN_ERR_ALIGNMENT;
+  for (int i = 0; i < 3; ++i) {
+    if (sz[i] <= 1) continue;
+    if (s[i] <= 0) return ATTN_ERR_INVALID_ARG;
+    if (s[i] % 8 != 0) return ATTN_ERR_ALIGNMENT;
+  }
+  return ATTN_OK;
+}
+
+// Encodes a 4-D tensor map over (d, n, h, b) with a box of 64 x box_n x 1 x 1
+// and 128-byte swizzling.  The three outer dimensions are ordered by stride
+// (smallest first) as the encoder expects; `slots` records where n, h and b
+// went.  Extent-1 dimensions get a harmless stride.
+attn_status_t make_map(CUtensorMap *map, const void *base, bool bf16, const int64_t sz[4], const int64_t st[4],
+                       int box_n, uint32_t *slots) {
+  struct Dim {
+    int which;  // 0 = b, 1 = h, 2 = n
+    uint64_t size, stride_bytes;
+  } dims[3];
+  uint64_t span = static_cast<uint64_t>(sz[3]) * 2;
+  for (int i = 0; i < 3; ++i) span = std::max<uint64_t>(span, static_cast<uint64_t>(sz[i]) * st[i] * 2);
+  span = (span + 15) & ~uint64_t(15);
+  const int order[3] = {2, 1, 0};  // n, h, b (indices into the (b, h, n, d) arrays)
+  for (int k = 0; k < 3; ++k) {
+    const int i = order[k];
+    dims[k].which = i;
+    dims[k].size = static_cast<uint64_t>(sz[i]);
+    dims[k].stride_bytes = sz[i] > 1 ? static_cast<uint64_t>(st[i]) * 2 : span;
+  }
+  std::stable_sort(dims, dims + 3, [](const Dim &a, const Dim &b) { return a.stride_bytes < b.stride_bytes; });
+  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(sz[3]), dims[0].size, dims[1].size, dims[2].size};
+  cuuint64_t gstride[3] = {dims[0].stride_bytes, dims[1].stride_bytes, dims[2].stride_bytes};
+  cuuint32_t box[4] = {64, 1, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  uint32_t sn = 0, sh = 0, sb = 0;
+  for (int k = 0; k < 3; ++k) {
+    if (dims[k].which == 2) {
+      sn = k + 1;
+      box[k + 1] = static_cast<cuuint32_t>(box_n);
+    } else if (dims[k].which == 1) {
+      sh = k + 1;
+    } else {
+      sb = k + 1;
+    }
+  }
+  for (int k = 0; k < 3; ++k)
+    if (gstride[k] % 16 != 0 || gstride[k] >= (1ull << 40)) return ATTN_ERR_ALIGNMENT;
+  *slots = sn | (sh << 2) | (sb << 4);
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                        const_cast<void *>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Largest number of KV splits decode may use for these sizes on this device.
+int decode_max_splits(int B, int H_q, int H_kv, int sm_count) {
+  const int group = H_q / H_kv;
+  const int gh = decode_heads_per_cta(group);
+  const int nhc = (group + gh - 1) / gh;
+  const int64_t ctas = static_cast<int64_t>(B) * H_kv * nhc;
+  const int64_t target = 4LL * sm_count;
+  int64_t s = (target + ctas - 1) / ctas;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, 64)));
+}
+
+size_t decode_ws_bytes(int B, int H_q, int D, int splits) {
+  if (splits <= 1) return 0;
+  return static_cast<size_t>(B) * H_q * splits * (D + 1) * sizeof(float);
+}
+
+bool valid_dtype(attn_dtype_t dt) { return dt == ATTN_F16 || dt == ATTN_BF16; }
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void *o, float *lse, attn_dtype_t dtype,
+                               int B, int H_q, int H_kv, int N_q, int N_kv, int D, const int64_t q_str[4],
+                               const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4], int causal,
+                               float scale, void *stream) {
+  if (!q || !k || !v || !o || !q_str || !k_str || !v_str || !o_str) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H_q < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || H_q > 65535) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3)))
+    return ATTN_ERR_ALIGNMENT;
+  const int64_t qsz[4] = {B, H_q, N_q, D}, kvsz[4] = {B, H_kv, N_kv, D};
+  attn_status_t st;
+  if ((st = check_strides(q_str, qsz)) || (st = check_strides(k_str, kvsz)) || (st = check_strides(v_str, kvsz)) ||
+      (st = check_strides(o_str, qsz)))
+    return st;
+
+  const DeviceState *dev = nullptr;
+  if ((st = device_state(&dev)) != ATTN_OK) return st;
+  const bool bf16 = dtype == ATTN_BF16;
+  CUtensorMap tq, tk, tv;
+  PrefillParams p{};
+  if ((st = make_map(&tq, q, bf16, qsz, q_str, kPrefillBM, &p.slots_q)) ||
+      (st = make_map(&tk, k, bf16, kvsz, k_str, kPrefillBN, &p.slots_k)) ||
+      (st = make_map(&tv, v, bf16, kvsz, v_str, kPrefillBN, &p.slots_v)))
+    return st;
+  p.o = o;
+  p.lse = lse;
+  p.err = dev->err;
+  p.o_sb = o_str[0];
+  p.o_sh = o_str[1];
+  p.o_sn = o_str[2];
+  p.Nq = N_q;
+  p.Nkv = N_kv;
+  p.Hq = H_q;
+  p.group = H_q / H_kv;
+  p.n_qtiles = (N_q + kPrefillBM - 1) / kPrefillBM;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  cudaError_t e = launch_prefill(D, causal != 0, bf16, tq, tk, tv, p, B, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_decode_workspace_size(int B, int H_q, int H_kv, int D) {
+  if (B < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || (D != 64 && D != 128)) return 0;
+  const DeviceState *dev = nullptr;
+  if (device_state(&dev) != ATTN_OK) return 0;
+  return decode_ws_bytes(B, H_q, D, decode_max_splits(B, H_q, H_kv, dev->sm_count));
+}
+
+attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                              attn_dtype_t dtype, int B, int H_q, int H_kv, int cache_len, int D,
+                              const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
+                              const int64_t o_str[4], float scale, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+  if (!q || !k_cache || !v_cache || !o || !q_str || !kc_str || !vc_str || !o_str) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H_q < 1 || H_kv < 1 || cache_len < 1 || D < 1 || H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f) || B > 65535) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3)))
+    return ATTN_ERR_ALIGNMENT;
+  const int64_t qsz[4] = {B, H_q, 1, D}, csz[4] = {B, H_kv, cache_len, D};
+  attn_status_t st;
+  if ((st = check_strides(q_str, qsz)) || (st = check_strides(kc_str, csz)) || (st = check_strides(vc_str, csz)) ||
+      (st = check_strides(o_str, qsz)))
+    return st;
+  const DeviceState *dev = nullptr;
+  if ((st = device_state(&dev)) != ATTN_OK) return st;
+
+  const int group = H_q / H_kv;
+  const int gh = decode_heads_per_cta(group);
+  const int nhc = (group + gh - 1) / gh;
+  const int max_splits = decode_max_splits(B, H_q, H_kv, dev->sm_count);
+  const int step = decode_tokens_per_step(D);
+  constexpr int kMinChunk = 256;  // keys per split at least
+  int nsplit = std::min<int>(max_splits, (cache_len + kMinChunk - 1) / kMinChunk);
+  nsplit = std::max(nsplit, 1);
+  int chunk = (cache_len + nsplit - 1) / nsplit;
+  chunk = (chunk + step - 1) / step * step;
+  nsplit = (cache_len + chunk - 1) / chunk;  // every split non-empty
+  if (nsplit > 1) {
+    const size_t need = decode_ws_bytes(B, H_q, D, nsplit);
+    if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15) != 0) return ATTN_ERR_ALIGNMENT;
+  }
+  DecodeParams p{};
+  p.q = q;
+  p.kc = k_cache;
+  p.vc = v_cache;
+  p.o = o;
+  p.lse = lse;
+  p.ws_o = static_cast<float *>(workspace);
+  p.ws_lse = nsplit > 1 ? static_cast<float *>(workspace) + static_cast<size_t>(B) * H_q * nsplit * D : nullptr;
+  p.err = dev->err;
+  p.q_sb = q_str[0];
+  p.q_sh = q_str[1];
+  p.kc_sb = kc_str[0];
+  p.kc_sh = kc_str[1];
+  p.kc_sn = kc_str[2];
+  p.vc_sb = vc_str[0];
+  p.vc_sh = vc_str[1];
+  p.vc_sn = vc_str[2];
+  p.o_sb = o_str[0];
+  p.o_sh = o_str[1];
+  p.Hq = H_q;
+  p.group = group;
+  p.nhc = nhc;
+  p.cache_len = cache_len;
+  p.chunk = chunk;
+  p.nsplit = nsplit;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  if (static_cast<int64_t>(H_kv) * nhc > 65535) return ATTN_ERR_INVALID_ARG;
+  cudaError_t e = launch_decode(D, dtype == ATTN_BF16, gh, p, B, H_kv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t kv_cache_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new, attn_dtype_t dtype,
+                             int B, int H_kv, int n_new, int D, int pos, int max_len, const int64_t kc_str[4],
+                             const int64_t vc_str[4], const int64_t kn_str[4], const int64_t vn_str[4],
+                             void *stream) {
+  if (!k_cache || !v_cache || !k_new || !v_new || !kc_str || !vc_str || !kn_str || !vn_str)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H_kv < 1 || n_new < 1 || D < 1 || max_len < 1 || pos < 0) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(pos) + n_new > max_len) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new)) return ATTN_ERR_ALIGNMENT;
+  const int64_t csz[4] = {B, H_kv, max_len, D}, nsz[4] = {B, H_kv, n_new, D};
+  attn_status_t st;
+  if ((st = check_strides(kc_str, csz)) || (st = check_strides(vc_str, csz)) || (st = check_strides(kn_str, nsz)) ||
+      (st = check_strides(vn_str, nsz)))
+    return st;
+  const DeviceState *dev = nullptr;
+  if ((st = device_state(&dev)) != ATTN_OK) return st;
+  KvWriteParams p{};
+  p.kc = k_cache;
+  p.vc = v_cache;
+  p.kn = k_new;
+  p.vn = v_new;
+  p.kc_sb = kc_str[0];
+  p.kc_sh = kc_str[1];
+  p.kc_sn = kc_str[2];
+  p.vc_sb = vc_str[0];
+  p.vc_sh = vc_str[1];
+  p.vc_sn = vc_str[2];
+  p.kn_sb = kn_str[0];
+  p.kn_sh = kn_str[1];
+  p.kn_sn = kn_str[2];
+  p.vn_sb = vn_str[0];
+  p.vn_sh = vn_str[1];
+  p.vn_sn = vn_str[2];
+  p.Hkv = H_kv;
+  p.n_new = n_new;
+  p.pos = pos;
+  p.D = D;
+  p.total_units = static_cast<int64_t>(B) * H_kv * n_new * (D / 8);
+  p.err = dev->err;
+  cudaError_t e = launch_kv_cache_write(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_get_device_error(void *stream) {
+  const DeviceState *dev = nullptr;
+  attn_status_t st = device_state(&dev);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (word == 0) return ATTN_OK;
+  const unsigned zero = 0;
+  if (cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+const char *attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_ALIGNMENT: return "ATTN_ERR_ALIGNMENT";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

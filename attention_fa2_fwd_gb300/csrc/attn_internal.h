@@ -1,0 +1,67 @@
+// attn_internal.h -- parameter blocks and launcher declarations shared by the
+// host ABI (attn_api.cu) and the kernel translation units.  Not installed.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn.h"
+
+namespace attn {
+
+// Prefill work tile: 128 query rows x 128 key/value rows per pipeline step.
+constexpr int kPrefillBM = 128;
+constexpr int kPrefillBN = 128;
+
+struct PrefillParams {
+  void *o;
+  float *lse;               // may be null
+  unsigned *err;            // device error word
+  int64_t o_sb, o_sh, o_sn; // output element strides (d stride is 1)
+  int Nq, Nkv, Hq, group, n_qtiles;
+  float scale_log2;         // scale * log2(e): scores are kept in base-2 units
+  // Tensor-map coordinate slot (1..3) of the n, h and b coordinates for the
+  // Q, K and V maps, packed as n | h << 2 | b << 4 (slot 0 is always d).
+  uint32_t slots_q, slots_k, slots_v;
+};
+
+struct DecodeParams {
+  const void *q, *kc, *vc;
+  void *o;
+  float *lse;               // may be null
+  float *ws_o, *ws_lse;     // split partials (used when nsplit > 1)
+  unsigned *err;
+  int64_t q_sb, q_sh;
+  int64_t kc_sb, kc_sh, kc_sn;
+  int64_t vc_sb, vc_sh, vc_sn;
+  int64_t o_sb, o_sh;
+  int Hq, group, nhc, cache_len, chunk, nsplit;
+  float scale_log2;
+};
+
+struct KvWriteParams {
+  void *kc, *vc;
+  const void *kn, *vn;
+  int64_t kc_sb, kc_sh, kc_sn, vc_sb, vc_sh, vc_sn;
+  int64_t kn_sb, kn_sh, kn_sn, vn_sb, vn_sh, vn_sn;
+  int Hkv, n_new, pos, D;
+  int64_t total_units;      // B * H_kv * n_new * (D / 8) 16-byte pieces per tensor
+  unsigned *err;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_prefill(int D, bool causal, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+                           const CUtensorMap &tv, const PrefillParams &p, int B, cudaStream_t stream);
+size_t prefill_smem_bytes(int D);
+
+// Decode: split selection helpers and launch.
+int decode_heads_per_cta(int group);
+int decode_tokens_per_step(int D);
+cudaError_t launch_decode(int D, bool bf16, int heads_per_cta, const DecodeParams &p, int B, int Hkv,
+                          cudaStream_t stream);
+
+cudaError_t launch_kv_cache_write(const KvWriteParams &p, cudaStream_t stream);
+
+}  // namespace attn

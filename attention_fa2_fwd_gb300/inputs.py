@@ -55,12 +55,27 @@ def prefill_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype="bf16", layout="bhnd", seed=42,
     return to_layout(q, layout), to_layout(k, layout), to_layout(v, layout)
 
 
-def decode_inputs(B, Hq, Hkv, L, D, dtype="bf16", seed=42):
-    """Per-token queries Q (B,Hq,L,D) and the token stream K, V (B,Hkv,L,D).
+def decode_stream(B, Hkv, L, D, dtype="bf16", seed=42):
+    """Key/value token streams K, V (B,H_kv,L,D): token t's key and value are K[:, :, t], V[:, :, t]."""
+    gen = torch.Generator().manual_seed(seed)
+    dt = DTYPES[dtype]
+    k = _draw((B, Hkv, L, D), gen, ("normal", 1.0)).to(dt)
+    v = _draw((B, Hkv, L, D), gen, ("normal", 1.0)).to(dt)
+    return k, v
 
-    Token t's query is Q[:, :, t]; its key/value are K[:, :, t], V[:, :, t].
+
+def decode_queries(B, Hq, D, steps, dtype="bf16", seed=42):
+    """Queries (B,H_q,len(steps),D) of the given decode steps, N(0,1).
+
+    Step t's query is drawn from its own generator (seeded from seed and t),
+    so a step's query does not depend on which other steps are requested.
     """
-    return prefill_inputs(B, Hq, Hkv, L, L, D, dtype=dtype, seed=seed)
+    dt = DTYPES[dtype]
+    out = torch.empty((B, Hq, len(steps), D), dtype=dt)
+    for j, t in enumerate(steps):
+        gen = torch.Generator().manual_seed(seed * 1_000_003 + 7919 * int(t) + 1)
+        out[:, :, j] = _draw((B, Hq, D), gen, ("normal", 1.0)).to(dt)
+    return out
 
 
 @dataclass(frozen=True)

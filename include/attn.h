@@ -1,0 +1,168 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention forward library
+ * (libattn_gb300.so).
+ *
+ * The library computes FlashAttention-2-style attention without ever
+ * materialising the (B, H_q, N_q, N_kv) score matrix:
+ *
+ *     O = softmax(scale * Q K^T + mask) V,   LSE = ln(sum_j exp(scale * q.k_j))
+ *
+ * Notation follows "Skill: Write a Triton Attention Kernel" (Inputs the agent
+ * should gather first): batch B, query heads H_q, key/value heads H_kv
+ * (H_q a multiple of H_kv; GQA group = H_q / H_kv, MQA when H_kv = 1), query
+ * length N_q, key/value length N_kv, head dimension D.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA tensors) on the
+ *   current CUDA device, unless stated otherwise.  The caller owns every
+ *   buffer.  The library allocates no device memory of its own; it keeps only
+ *   a small per-device cache of kernel attributes and function pointers.
+ * - Strides are in ELEMENTS and are given in (b, h, n, d) order as int64_t[4].
+ *   Any b/h/n strides are allowed (e.g. (B,H,N,D) or (B,N,H,D) memory), but
+ *   the d stride must be 1, and every other stride times the element size
+ *   (2 bytes) must be a multiple of 16 bytes; base pointers must be 16-byte
+ *   aligned.  These are the tensor-memory-accelerator (TMA) rules.
+ * - Q, K, V and O share one element type (attn_dtype_t).  LSE is always fp32,
+ *   contiguous.  Accumulation is fp32 throughout.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every call is stream-ordered and returns once its kernels are enqueued.
+ * - Argument errors are detected on the host before anything is launched and
+ *   are returned synchronously; nothing is enqueued in that case.  A failed
+ *   launch returns ATTN_ERR_CUDA.
+ * - Device-side failures (a pipeline wait that exceeded its time limit) are
+ *   recorded in a device error word; read and clear it with
+ *   attn_get_device_error().  While the word is non-zero, the library's
+ *   kernels return immediately without computing.
+ * - There is no CPU fallback and no other backend: every call runs the CUDA
+ *   kernels of this library or returns an error.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,     /* null pointer, size < 1, H_q % H_kv != 0, bad scale, range error */
+    ATTN_ERR_UNSUPPORTED = 2,     /* D not in {64, 128}, unknown dtype, device is not sm_103 */
+    ATTN_ERR_ALIGNMENT = 3,       /* d stride != 1, pointer or stride not 16-byte aligned */
+    ATTN_ERR_WORKSPACE = 4,       /* workspace missing or smaller than attn_decode_workspace_size() */
+    ATTN_ERR_CUDA = 5,            /* a CUDA runtime/driver call or a launch failed */
+    ATTN_ERR_DEVICE_TIMEOUT = 6   /* a kernel gave up on a pipeline wait (see attn_get_device_error) */
+} attn_status_t;
+
+typedef enum {
+    ATTN_F16 = 0,
+    ATTN_BF16 = 1
+} attn_dtype_t;
+
+/*
+ * attn_fwd_prefill -- fused attention forward over a whole sequence.
+ *
+ * Follows "Skill: Write a Triton Attention Kernel", Required reasoning process
+ * steps 1-9 (tiles of query rows, online softmax with running max m_i and sum
+ * l_i, rescale by alpha = exp(m_old - m_new), O = O_i / l_i after the loop,
+ * lse = m_i + log(l_i)), and Correctness requirements (mask before the max,
+ * -inf for keys past N_kv, rows past N_q not stored).
+ *
+ *   q    (B, H_q,  N_q,  D) element strides q_str[4]    read
+ *   k    (B, H_kv, N_kv, D) element strides k_str[4]    read
+ *   v    (B, H_kv, N_kv, D) element strides v_str[4]    read
+ *   o    (B, H_q,  N_q,  D) element strides o_str[4]    written (rows < N_q only)
+ *   lse  (B, H_q,  N_q) fp32 contiguous, natural log, or NULL to skip it
+ *   causal  0 or 1; 1 keeps key j for query i iff j <= i (top-left aligned,
+ *           positions compared with no offset, as the pages write the mask)
+ *   scale   softmax scale applied to Q K^T; must be finite and > 0
+ *           (1/sqrt(D) is the usual value)
+ *   D must be 64 or 128.  N_q, N_kv >= 1 and arbitrary (not block-aligned).
+ *
+ * Returns ATTN_OK after enqueueing one kernel on `stream`.
+ */
+attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void *o, float *lse,
+                               attn_dtype_t dtype, int B, int H_q, int H_kv, int N_q, int N_kv, int D,
+                               const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                               const int64_t o_str[4], int causal, float scale, void *stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of scratch attn_fwd_decode needs.
+ *
+ * Split-KV decode writes one partial output (D fp32) and one partial LSE per
+ * (b, q-head, split) and merges them.  The number of splits depends only on
+ * B, H_q, H_kv and the current device's SM count (never on cache_len), so a
+ * workspace sized once serves every cache length.  Returns 0 on bad
+ * arguments.  Host-only; reads the current device's SM count.
+ */
+size_t attn_decode_workspace_size(int B, int H_q, int H_kv, int D);
+
+/*
+ * attn_fwd_decode -- attention of ONE new query token per (batch, q-head) over
+ * a preallocated KV cache whose first cache_len positions are valid.
+ *
+ * Follows "Triton-FlashAttention", Phase 2 (a separate decode kernel; every
+ * cached position is valid, so there is no causal loop; cache_len is a
+ * runtime value, never a compile-time one), split over the KV sequence: each
+ * (b, kv-head, split) streams its share of the cache once for all H_q/H_kv
+ * query heads of the group and produces (O_s, lse_s); the splits are merged
+ * as lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s.
+ *
+ *   q        (B, H_q, 1, D)        strides q_str[4] (n stride ignored)   read
+ *   k_cache  (B, H_kv, max_len, D) strides kc_str[4]                     read rows < cache_len
+ *   v_cache  (B, H_kv, max_len, D) strides vc_str[4]                     read rows < cache_len
+ *   o        (B, H_q, 1, D)        strides o_str[4]                      written
+ *   lse      (B, H_q) fp32 contiguous, natural log, or NULL
+ *   cache_len   1 <= cache_len (rows [0, cache_len) of the cache are used)
+ *   workspace   device scratch of at least attn_decode_workspace_size(B, H_q, H_kv, D)
+ *               bytes (may be NULL when that size is 0); contents need not be
+ *               initialised; calls sharing one workspace must not overlap
+ *
+ * Returns ATTN_OK after enqueueing one or two kernels on `stream`.
+ */
+attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                              attn_dtype_t dtype, int B, int H_q, int H_kv, int cache_len, int D,
+                              const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
+                              const int64_t o_str[4], float scale, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
+ * kv_cache_write -- copy n_new tokens of K and V into a preallocated cache at
+ * positions [pos, pos + n_new).
+ *
+ * Follows "Triton-FlashAttention", Phase 2: the cache is a static buffer that
+ * is never regrown, and the write is kept apart from the attention kernel.
+ *
+ *   k_cache, v_cache  (B, H_kv, max_len, D) strides kc_str / vc_str   written
+ *   k_new, v_new      (B, H_kv, n_new, D)   strides kn_str / vn_str   read
+ *   0 <= pos, pos + n_new <= max_len
+ *
+ * Returns ATTN_OK after enqueueing one kernel on `stream`.
+ */
+attn_status_t kv_cache_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                             attn_dtype_t dtype, int B, int H_kv, int n_new, int D, int pos, int max_len,
+                             const int64_t kc_str[4], const int64_t vc_str[4], const int64_t kn_str[4],
+                             const int64_t vn_str[4], void *stream);
+
+/*
+ * attn_get_device_error -- synchronise `stream`, read the device error word of
+ * the current device and clear it.  Returns ATTN_OK if no kernel reported a
+ * failure, ATTN_ERR_DEVICE_TIMEOUT if one gave up on a wait, ATTN_ERR_CUDA if
+ * the synchronisation itself failed.
+ */
+attn_status_t attn_get_device_error(void *stream);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char *attn_status_string(attn_status_t status);
+
+/* attn_version -- library version as major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

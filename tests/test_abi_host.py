@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI (no GPU needed, nothing is launched).
+
+* the shared library loads and exports every function include/attn.h declares;
+* every argument error is reported synchronously with its status code.  Each
+  call below fails validation, which runs before any CUDA call, so the fake
+  (never dereferenced) pointers are never seen by a kernel.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_fa2_fwd_gb300 as A
+from attention_fa2_fwd_gb300.build import INCLUDE, build
+
+HEADER = os.path.join(INCLUDE, "attn.h")
+P = 0x7F0000000000  # 16-byte aligned fake device address
+BAD = P + 8         # misaligned
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return A.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_expected_functions():
+    assert declared_functions() == sorted(A.EXPORTS)
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert A.attn_version() >= 100
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "ATTN_OK"), (1, "ATTN_ERR_INVALID_ARG"), (2, "ATTN_ERR_UNSUPPORTED"),
+                       (3, "ATTN_ERR_ALIGNMENT"), (4, "ATTN_ERR_WORKSPACE"), (5, "ATTN_ERR_CUDA"),
+                       (6, "ATTN_ERR_DEVICE_TIMEOUT")]:
+        assert A.attn_status_string(code) == name
+    assert A.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+def contig(B, H, N, D):
+    return (H * N * D, N * D, D, 1)
+
+
+def prefill(**kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=None, dtype=A.ATTN_BF16, B=2, H_q=8, H_kv=2, N_q=64, N_kv=64, D=128,
+             q_str=contig(2, 8, 64, 128), k_str=contig(2, 2, 64, 128), v_str=contig(2, 2, 64, 128),
+             o_str=contig(2, 8, 64, 128), causal=1, scale=0.088, stream=None)
+    a.update(kw)
+    return A.attn_fwd_prefill(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(o=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(N_q=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(N_kv=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(H_kv=3), A.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), A.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), A.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-1.0), A.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), A.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), A.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), A.ATTN_ERR_UNSUPPORTED),
+    (dict(D=256), A.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=7), A.ATTN_ERR_UNSUPPORTED),
+    (dict(q=BAD), A.ATTN_ERR_ALIGNMENT),
+    (dict(v=BAD), A.ATTN_ERR_ALIGNMENT),
+    (dict(lse=P + 2), A.ATTN_ERR_ALIGNMENT),
+    (dict(q_str=(8 * 64 * 128, 64 * 128, 128, 2)), A.ATTN_ERR_ALIGNMENT),
+    (dict(k_str=(2 * 64 * 128, 64 * 128, 132, 1)), A.ATTN_ERR_ALIGNMENT),
+    (dict(o_str=(8 * 64 * 128, 64 * 128, -128, 1)), A.ATTN_ERR_INVALID_ARG),
+])
+def test_prefill_argument_errors(lib, kw, code):
+    assert prefill(**kw) == code
+
+
+def decode(**kw):
+    a = dict(q=P, k_cache=P, v_cache=P, o=P, lse=None, dtype=A.ATTN_BF16, B=2, H_q=32, H_kv=8, cache_len=100,
+             D=128, q_str=contig(2, 32, 1, 128), kc_str=contig(2, 8, 256, 128), vc_str=contig(2, 8, 256, 128),
+             o_str=contig(2, 32, 1, 128), scale=0.088, workspace=P, workspace_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return A.attn_fwd_decode(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(k_cache=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(cache_len=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(H_q=30), A.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), A.ATTN_ERR_INVALID_ARG),
+    (dict(D=80), A.ATTN_ERR_UNSUPPORTED),
+    (dict(k_cache=BAD), A.ATTN_ERR_ALIGNMENT),
+    (dict(kc_str=(8 * 256 * 128, 256 * 128, 128, 3)), A.ATTN_ERR_ALIGNMENT),
+])
+def test_decode_argument_errors(lib, kw, code):
+    assert decode(**kw) == code
+
+
+def cache_write(**kw):
+    a = dict(k_cache=P, v_cache=P, k_new=P, v_new=P, dtype=A.ATTN_BF16, B=2, H_kv=8, n_new=1, D=128, pos=10,
+             max_len=256, kc_str=contig(2, 8, 256, 128), vc_str=contig(2, 8, 256, 128),
+             kn_str=contig(2, 8, 1, 128), vn_str=contig(2, 8, 1, 128), stream=None)
+    a.update(kw)
+    return A.kv_cache_write(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k_new=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(pos=-1), A.ATTN_ERR_INVALID_ARG),
+    (dict(pos=256), A.ATTN_ERR_INVALID_ARG),
+    (dict(pos=250, n_new=7), A.ATTN_ERR_INVALID_ARG),
+    (dict(n_new=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(D=32), A.ATTN_ERR_UNSUPPORTED),
+    (dict(v_cache=BAD), A.ATTN_ERR_ALIGNMENT),
+])
+def test_cache_write_argument_errors(lib, kw, code):
+    assert cache_write(**kw) == code
+
+
+def test_workspace_size_rejects_bad_arguments(lib):
+    assert A.attn_decode_workspace_size(0, 32, 8, 128) == 0
+    assert A.attn_decode_workspace_size(2, 30, 8, 128) == 0
+    assert A.attn_decode_workspace_size(2, 32, 8, 96) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(A, "_lib", None)
+    monkeypatch.setattr(A, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(A.AttnLibraryMissing):
+        A.lib()

@@ -1,0 +1,138 @@
+"""GPU parity of kv_cache_write and attn_fwd_decode, through the C ABI.
+
+Decode workload: bf16, H_q=32, H_kv=8, D=128, B in {2, 64}; the cache is
+filled token by token with kv_cache_write and decoded at cache_len in
+{1, 33, 257, 1024, 4097, 8192}.  Checks: against the fp64 oracle (all heads,
+batches sampled at B=64), autoregressive equivalence with the causal prefill
+("Triton-FlashAttention", Phase 2: per-token decode outputs concatenated equal
+the prefill output), bit-exact cache writes with untouched neighbours.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_fa2_fwd_gb300 import inputs as I
+from tests.helpers import assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_fa2_fwd_gb300 as A
+    A.lib()
+    yield
+    A.check_device_error()
+
+
+def test_kv_cache_write_bit_exact():
+    import attention_fa2_fwd_gb300 as A
+    for D, dt in ((128, "bf16"), (64, "f16")):
+        B, Hkv, L = 3, 4, 50
+        kc0, vc0, _ = I.prefill_inputs(B, Hkv, Hkv, L, L, D, dt, seed=1)
+        kn, vn, _ = I.prefill_inputs(B, Hkv, Hkv, 7, 7, D, dt, seed=2)
+        kc, vc = kc0.cuda(), vc0.cuda()
+        A.write_kv_cache(kc, vc, kn.cuda(), vn.cuda(), 20)
+        torch.cuda.synchronize()
+        kr, vr = oracle.kv_cache_write(kc0.float().numpy(), vc0.float().numpy(), kn.float().numpy(),
+                                       vn.float().numpy(), 20)
+        assert np.array_equal(kc.cpu().float().numpy(), kr)
+        assert np.array_equal(vc.cpu().float().numpy(), vr)
+
+
+def test_kv_cache_write_strided_new_tokens():
+    """New tokens given as a (B,N,H,D)-memory view are written to a (B,H,N,D) cache."""
+    import attention_fa2_fwd_gb300 as A
+    B, Hkv, L, D = 2, 8, 16, 128
+    kc = torch.zeros((B, Hkv, L, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    kn, vn, _ = I.prefill_inputs(B, Hkv, Hkv, 3, 3, D, "bf16", layout="bnhd", seed=4)
+    kn_d = kn.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
+    vn_d = vn.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
+    A.write_kv_cache(kc, vc, kn_d, vn_d, L - 3)
+    torch.cuda.synchronize()
+    assert torch.equal(kc[:, :, L - 3:].cpu(), kn) and torch.equal(vc[:, :, L - 3:].cpu(), vn)
+    assert (kc[:, :, :L - 3] == 0).all() and (vc[:, :, :L - 3] == 0).all()
+
+
+def _fill_and_decode(B, L_max, lens, check_ar_upto=0, b_sample=None):
+    """Fill a cache token by token; decode; compare at `lens` with the oracle and
+    the first `check_ar_upto` decode steps with the causal prefill."""
+    import attention_fa2_fwd_gb300 as A
+    Hq, Hkv, D = 32, 8, 128
+    scale = 1 / np.sqrt(D)
+    k, v = I.decode_stream(B, Hkv, L_max, D, "bf16", seed=B)
+    steps = sorted(set(range(check_ar_upto)) | {L - 1 for L in lens})
+    col = {t: j for j, t in enumerate(steps)}
+    q = I.decode_queries(B, Hq, D, steps, "bf16", seed=B)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    kc = torch.zeros((B, Hkv, L_max, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ws = A.decode_workspace(B, Hq, Hkv, D)
+    outs, lses = {}, {}
+    n_ar = max(check_ar_upto, 1)
+    o_steps = torch.empty((B, Hq, n_ar, D), dtype=torch.bfloat16, device="cuda")
+    l_steps = torch.empty((B, Hq, n_ar), dtype=torch.float32, device="cuda")
+    for t in range(L_max):
+        A.write_kv_cache(kc, vc, kd[:, :, t:t + 1], vd[:, :, t:t + 1], t)
+        if t in col:
+            o, lse = A.decode(qd[:, :, col[t]], kc, vc, t + 1, workspace=ws)
+            if t < check_ar_upto:
+                o_steps[:, :, t] = o
+                l_steps[:, :, t] = lse
+            if (t + 1) in lens:
+                outs[t + 1], lses[t + 1] = o.clone(), lse.clone()
+    torch.cuda.synchronize()
+    A.check_device_error()
+    bs = np.arange(B) if b_sample is None else np.array(b_sample)
+    for L in sorted(lens):
+        o_ref, lse_ref = oracle.decode(np64(q[bs][:, :, col[L - 1]]), np64(k[bs]), np64(v[bs]), L, scale)
+        assert_close(np64(outs[L])[bs], o_ref, np64(lses[L])[bs], lse_ref, f"B={B} L={L}")
+    if check_ar_upto:
+        n = check_ar_upto
+        o_pre, l_pre = A.prefill(qd[:, :, :n], kd[:, :, :n], vd[:, :, :n], causal=True)
+        torch.cuda.synchronize()
+        assert_close(o_steps, np64(o_pre), l_steps, np64(l_pre), "autoregressive")
+
+
+def test_decode_b2_all_lengths_and_autoregressive():
+    _fill_and_decode(2, 8192, set(I.DECODE_LENS), check_ar_upto=8192)
+
+
+def test_decode_b64_lengths():
+    _fill_and_decode(64, 8192, set(I.DECODE_LENS), check_ar_upto=1024, b_sample=[0, 17, 42, 63])
+
+
+def test_decode_against_oracle_gqa_ratios():
+    """Group sizes 1..32 (MHA to MQA) and D = 64 / 128, non-aligned cache lengths."""
+    import attention_fa2_fwd_gb300 as A
+    for Hkv in (32, 16, 8, 4, 2, 1):
+        for D in (64, 128):
+            B, Hq, L = 2, 32, 300
+            k, v = I.decode_stream(B, Hkv, L, D, "f16", seed=Hkv * D)
+            lens = (1, 31, 33, 257, 300)
+            q = I.decode_queries(B, Hq, D, [c - 1 for c in lens], "f16", seed=Hkv * D)
+            kc, vc = k.cuda(), v.cuda()
+            for j, cl in enumerate(lens):
+                o, lse = A.decode(q[:, :, j].cuda(), kc, vc, cl)
+                torch.cuda.synchronize()
+                o_ref, lse_ref = oracle.decode(np64(q[:, :, j]), np64(k), np64(v), cl, 1 / np.sqrt(D))
+                assert_close(o, o_ref, lse, lse_ref, f"Hkv={Hkv} D={D} L={cl}")
+
+
+def test_decode_workspace_errors():
+    import attention_fa2_fwd_gb300 as A
+    B, Hq, Hkv, D, L = 2, 32, 8, 128, 4096
+    q = torch.zeros((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((B, Hkv, L, D), dtype=torch.bfloat16, device="cuda")
+    need = A.attn_decode_workspace_size(B, Hq, Hkv, D)
+    assert need > 0  # B=2 splits the cache over many CTAs
+    small = torch.empty(need // 8, dtype=torch.float32, device="cuda")
+    with pytest.raises(A.AttnError) as e:
+        A.decode(q, kc, kc, L, workspace=small)
+    assert e.value.status == A.ATTN_ERR_WORKSPACE

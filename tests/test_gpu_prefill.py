@@ -1,0 +1,168 @@
+"""GPU parity of attn_fwd_prefill against the fp64 oracle, through the C ABI.
+
+Workloads: the small MHA case, the GQA/MQA ratio x boundary sweep (every
+case checked element by element), the GQA causal prefill at N = 2048, 4096
+and 8192 and the (B,N,H,D)-strided cross-attention (sampled rows checked one
+by one against the oracle, plus size-independent properties), and the edge
+cases: N = 1, rows past N_q untouched, determinism, zero query, large scores.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_fa2_fwd_gb300 import inputs as I
+from tests.helpers import assert_close, np64, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_fa2_fwd_gb300 as A
+    A.lib()
+    yield
+    A.check_device_error()
+
+
+def run(q, k, v, causal, scale=None, **kw):
+    import attention_fa2_fwd_gb300 as A
+    o, lse = A.prefill(q.cuda() if not q.is_cuda else q, k.cuda() if not k.is_cuda else k,
+                       v.cuda() if not v.is_cuda else v, causal=causal, scale=scale, **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def ref(q, k, v, causal, scale):
+    return oracle.attention(np64(q), np64(k), np64(v), causal, scale)
+
+
+def test_mha_256_f16():
+    cfg = I.MHA_256
+    q, k, v = cfg.make()
+    o, lse = run(q, k, v, cfg.causal)
+    o_ref, lse_ref = ref(q, k, v, cfg.causal, cfg.scale)
+    assert_close(o, o_ref, lse, lse_ref, cfg.name)
+
+
+SWEEP = list(I.sweep_cases())
+
+
+@pytest.mark.parametrize("cfg", SWEEP, ids=[c.name for c in SWEEP])
+def test_sweep(cfg):
+    q, k, v = cfg.make()
+    o, lse = run(q, k, v, cfg.causal)
+    o_ref, lse_ref = ref(q, k, v, cfg.causal, cfg.scale)
+    assert_close(o, o_ref, lse, lse_ref, cfg.name)
+
+
+def _sampled(cfg, q, k, v, o, lse, n_random=48):
+    rows = sample_rows(cfg.B, cfg.Hq, cfg.Nq, n_random=n_random, seed=cfg.Nq)
+    o_ref, lse_ref = oracle.attention_rows(np64(q), np64(k), np64(v), cfg.causal, cfg.scale, rows)
+    og = np64(o)[rows[:, 0], rows[:, 1], rows[:, 2]]
+    lg = np64(lse)[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(og, o_ref, lg, lse_ref, cfg.name)
+
+
+@pytest.mark.parametrize("n", sorted(I.GQA_CAUSAL))
+def test_gqa_causal_prefill(n):
+    cfg = I.GQA_CAUSAL[n]
+    q, k, v = cfg.make()
+    o, lse = run(q, k, v, cfg.causal)
+    _sampled(cfg, q, k, v, o, lse)
+    # Properties at full size: causal row 0 equals V[kv_head, 0] exactly (one key, weight 1).
+    g = cfg.Hq // cfg.Hkv
+    v0 = v[:, :, 0, :].repeat_interleave(g, dim=1).cuda()
+    assert torch.equal(o[:, :, 0, :], v0)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("D", sorted(I.CROSS))
+def test_cross_attention_bnhd(D):
+    cfg = I.CROSS[D]
+    q, k, v = cfg.make()  # (B,H,N,D) views over (B,N,H,D) memory
+    assert q.stride()[1] == D and q.stride()[2] == cfg.Hq * D
+    qd = q.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
+    kd = k.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
+    vd = v.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
+    assert qd.stride() == q.stride() and kd.stride() == k.stride()
+    out = torch.empty((cfg.B, cfg.Nq, cfg.Hq, D), dtype=q.dtype, device="cuda").permute(0, 2, 1, 3)
+    o, lse = run(qd, kd, vd, False, out=out)
+    _sampled(cfg, q, k, v, o, lse, n_random=64)
+
+
+def test_n1_returns_v0():
+    for causal in (False, True):
+        q, k, v = I.prefill_inputs(2, 8, 2, 1, 1, 128, "bf16", seed=3)
+        o, lse = run(q, k, v, causal)
+        assert torch.equal(o.cpu(), v.repeat_interleave(4, dim=1))
+        s = (q.float() * k.repeat_interleave(4, dim=1).float()).sum(-1) / np.sqrt(128)
+        np.testing.assert_allclose(np64(lse), s.double().numpy(), atol=1e-3)
+
+
+def test_rows_past_nq_untouched():
+    """Rows >= N_q of a larger output buffer keep their contents (no write past N_q)."""
+    B, H, N, D = 1, 2, 33, 64
+    q, k, v = I.prefill_inputs(B, H, H, N, N, D, "f16", seed=5)
+    big = torch.full((B, H, N + 100, D), 7.0, dtype=torch.float16, device="cuda")
+    out = big[:, :, :N, :]
+    lse_big = torch.full((B * H * N + 64,), 9.0, dtype=torch.float32, device="cuda")
+    lse = lse_big[:B * H * N].view(B, H, N)
+    run(q, k, v, True, out=out, lse_out=lse)
+    assert (big[:, :, N:, :] == 7.0).all()
+    assert (lse_big[B * H * N:] == 9.0).all()
+    o_ref, lse_ref = ref(q, k, v, True, 1 / np.sqrt(D))
+    assert_close(out, o_ref, lse, lse_ref, "guard")
+
+
+def test_deterministic():
+    cfg = I.GQA_CAUSAL[2048]
+    q, k, v = (t.cuda() for t in cfg.make(seed=11))
+    o1, l1 = run(q, k, v, True)
+    o2, l2 = run(q, k, v, True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_zero_query_closed_form():
+    """Q = 0: O is the mean of the allowed V rows, LSE = ln(#allowed keys)."""
+    B, Hq, Hkv, N, D = 1, 4, 2, 257, 128
+    _, k, v = I.prefill_inputs(B, Hq, Hkv, N, N, D, "bf16", seed=9)
+    q = torch.zeros((B, Hq, N, D), dtype=torch.bfloat16)
+    for causal in (False, True):
+        o, lse = run(q, k, v, causal)
+        cnt = np.arange(1, N + 1) if causal else np.full(N, N)
+        np.testing.assert_allclose(np64(lse)[0, 0], np.log(cnt), atol=1e-3)
+        o_ref, lse_ref = ref(q, k, v, causal, 1 / np.sqrt(D))
+        assert_close(o, o_ref, lse, lse_ref, "zero-q")
+
+
+def test_large_scores_stable():
+    """Scores of magnitude ~ hundreds: no inf/nan, matches the oracle."""
+    B, H, N, D = 1, 2, 200, 64
+    q, k, v = I.prefill_inputs(B, H, H, N, N, D, "bf16", seed=13)
+    q = (q.float() * 12).to(torch.bfloat16)
+    for causal in (False, True):
+        o, lse = run(q, k, v, causal)
+        o_ref, lse_ref = ref(q, k, v, causal, 1 / np.sqrt(D))
+        assert_close(o, o_ref, lse, lse_ref, "large")
+
+
+def test_no_lse_pointer():
+    q, k, v = I.prefill_inputs(1, 2, 1, 65, 65, 64, "f16", seed=2)
+    o, lse = run(q, k, v, False, return_lse=False)
+    assert lse is None
+    o_ref, _ = ref(q, k, v, False, 1 / 8)
+    assert_close(o, o_ref)
+
+
+def test_unequal_lengths_causal_top_left():
+    """N_q != N_kv with causal: top-left alignment (key j kept for query i iff j <= i)."""
+    for Nq, Nkv in ((100, 300), (300, 100), (129, 1)):
+        q, k, v = I.prefill_inputs(2, 4, 2, Nq, Nkv, 64, "f16", seed=Nq + Nkv)
+        o, lse = run(q, k, v, True)
+        o_ref, lse_ref = ref(q, k, v, True, 1 / 8)
+        assert_close(o, o_ref, lse, lse_ref, f"{Nq}x{Nkv}")
