@@ -33,7 +33,8 @@ ATTN_F16 = 0
 ATTN_BF16 = 1
 
 # Every function that include/attn.h declares.
-EXPORTS = ("attn_fwd_prefill", "attn_decode_workspace_size", "attn_fwd_decode", "kv_cache_write",
+EXPORTS = ("attn_fwd_prefill", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
+           "kv_cache_write",
            "attn_get_device_error", "attn_status_string", "attn_version")
 
 
@@ -69,6 +70,8 @@ def lib() -> ctypes.CDLL:
                                            i64p, i64p, i64p, i64p, i32, f32, vp]
             L.attn_decode_workspace_size.restype = ctypes.c_size_t
             L.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+            L.attn_decode_splits.restype = i32
+            L.attn_decode_splits.argtypes = [i32, i32, i32, i32, i32]
             L.attn_fwd_decode.restype = i32
             L.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                           i64p, i64p, i64p, i64p, f32, vp, ctypes.c_size_t, vp]
@@ -100,6 +103,10 @@ def attn_fwd_prefill(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, 
 
 def attn_decode_workspace_size(B, H_q, H_kv, D) -> int:
     return int(lib().attn_decode_workspace_size(B, H_q, H_kv, D))
+
+
+def attn_decode_splits(B, H_q, H_kv, cache_len, D) -> int:
+    return int(lib().attn_decode_splits(B, H_q, H_kv, cache_len, D))
 
 
 def attn_fwd_decode(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, q_str, kc_str, vc_str, o_str,

@@ -141,6 +141,20 @@ int decode_max_splits(int B, int H_q, int H_kv, int sm_count) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, 64)));
 }
 
+// Split plan of one decode call: every split holds a multiple of the CTA's
+// step in keys (except the last), at least kMinChunk keys, and none is empty.
+void decode_plan(int B, int H_q, int H_kv, int cache_len, int D, int sm_count, int *nsplit_out, int *chunk_out) {
+  constexpr int kMinChunk = 256;
+  const int max_splits = decode_max_splits(B, H_q, H_kv, sm_count);
+  const int step = decode_tokens_per_step(D);
+  int nsplit = std::min<int>(max_splits, (cache_len + kMinChunk - 1) / kMinChunk);
+  nsplit = std::max(nsplit, 1);
+  int chunk = (cache_len + nsplit - 1) / nsplit;
+  chunk = (chunk + step - 1) / step * step;
+  *nsplit_out = (cache_len + chunk - 1) / chunk;
+  *chunk_out = chunk;
+}
+
 size_t decode_ws_bytes(int B, int H_q, int D, int splits) {
   if (splits <= 1) return 0;
   return static_cast<size_t>(B) * H_q * splits * (D + 1) * sizeof(float);
@@ -205,6 +219,15 @@ size_t attn_decode_workspace_size(int B, int H_q, int H_kv, int D) {
   return decode_ws_bytes(B, H_q, D, decode_max_splits(B, H_q, H_kv, dev->sm_count));
 }
 
+int attn_decode_splits(int B, int H_q, int H_kv, int cache_len, int D) {
+  if (B < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || cache_len < 1 || (D != 64 && D != 128)) return 0;
+  const DeviceState *dev = nullptr;
+  if (device_state(&dev) != ATTN_OK) return 0;
+  int nsplit = 1, chunk = cache_len;
+  decode_plan(B, H_q, H_kv, cache_len, D, dev->sm_count, &nsplit, &chunk);
+  return nsplit;
+}
+
 attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
                               attn_dtype_t dtype, int B, int H_q, int H_kv, int cache_len, int D,
                               const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
@@ -228,14 +251,8 @@ attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_
   const int group = H_q / H_kv;
   const int gh = decode_heads_per_cta(group);
   const int nhc = (group + gh - 1) / gh;
-  const int max_splits = decode_max_splits(B, H_q, H_kv, dev->sm_count);
-  const int step = decode_tokens_per_step(D);
-  constexpr int kMinChunk = 256;  // keys per split at least
-  int nsplit = std::min<int>(max_splits, (cache_len + kMinChunk - 1) / kMinChunk);
-  nsplit = std::max(nsplit, 1);
-  int chunk = (cache_len + nsplit - 1) / nsplit;
-  chunk = (chunk + step - 1) / step * step;
-  nsplit = (cache_len + chunk - 1) / chunk;  // every split non-empty
+  int nsplit = 1, chunk = cache_len;
+  decode_plan(B, H_q, H_kv, cache_len, D, dev->sm_count, &nsplit, &chunk);
   if (nsplit > 1) {
     const size_t need = decode_ws_bytes(B, H_q, D, nsplit);
     if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;

@@ -1,0 +1,81 @@
+"""Run one kernel of the library on one synthetic case, for profiling and timing.
+
+    python -m attention_fa2_fwd_gb300.run_case prefill [--B 2 --Hq 32 --Hkv 8 --N 8192 --D 128 --causal 1]
+    python -m attention_fa2_fwd_gb300.run_case decode  [--B 64 --Hq 32 --Hkv 8 --L 8192 --D 128]
+
+Inputs are seeded N(0,1) bf16 tensors drawn on the device.  Each iteration is
+timed with CUDA events on the launching stream (L2 flushed by a 256 MiB write
+before each); the per-iteration times and the derived TFLOPS or GB/s are
+printed.  Exits non-zero if a call or the device error word reports a failure.
+"""
+from __future__ import annotations
+
+import argparse
+import statistics
+
+import torch
+
+import attention_fa2_fwd_gb300 as A
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kind", choices=("prefill", "decode"))
+    ap.add_argument("--B", type=int)
+    ap.add_argument("--Hq", type=int, default=32)
+    ap.add_argument("--Hkv", type=int, default=8)
+    ap.add_argument("--N", type=int, default=8192)
+    ap.add_argument("--L", type=int, default=8192)
+    ap.add_argument("--D", type=int, default=128)
+    ap.add_argument("--causal", type=int, default=1)
+    ap.add_argument("--iters", type=int, default=5)
+    ap.add_argument("--dtype", choices=("bf16", "f16"), default="bf16")
+    a = ap.parse_args()
+    dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(42)
+
+    def randn(*s):
+        return torch.randn(s, generator=g, device=dev, dtype=torch.float32).to(dt)
+
+    flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    if a.kind == "prefill":
+        B = a.B or 2
+        q, k, v = randn(B, a.Hq, a.N, a.D), randn(B, a.Hkv, a.N, a.D), randn(B, a.Hkv, a.N, a.D)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, a.Hq, a.N), dtype=torch.float32, device=dev)
+        work = 4.0 * B * a.Hq * a.N * a.N * a.D / (2 if a.causal else 1)
+
+        def call():
+            A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse)
+        unit, scale = "TFLOPS", 1e12
+    else:
+        B = a.B or 64
+        kc, vc = randn(B, a.Hkv, a.L, a.D), randn(B, a.Hkv, a.L, a.D)
+        qd = randn(B, a.Hq, a.D)
+        od = torch.empty_like(qd)
+        lsed = torch.empty((B, a.Hq), dtype=torch.float32, device=dev)
+        ws = A.decode_workspace(B, a.Hq, a.Hkv, a.D, dev)
+        work = 2.0 * B * a.Hkv * a.L * a.D * 2
+
+        def call():
+            A.decode(qd, kc, vc, a.L, out=od, lse_out=lsed, workspace=ws)
+        unit, scale = "GB/s", 1e9
+    times = []
+    for _ in range(a.iters):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    A.check_device_error()
+    med = statistics.median(times)
+    print(f"{a.kind}: times_ms={[round(t, 4) for t in times]} median_ms={med:.4f} "
+          f"{unit}={work / (med * 1e-3) / scale:.1f}")
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,422 @@
+"""Benchmark of the fused attention forward hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  * prefill: causal GQA attention, B=2, H_q=32, H_kv=8, N=8192, D=128, bf16,
+    with LSE (attn_fwd_prefill);
+  * one decode step: B=64, H_q=32, H_kv=8, D=128, bf16 -- the new token is
+    written to the preallocated cache (kv_cache_write) and attends to the
+    8192 cached positions (attn_fwd_decode).
+
+Every kernel is timed with CUDA events on the stream it is launched on; the
+L2 cache (129 MB) is flushed by a 256 MiB write between timed kernels, outside
+the event pairs.  The JSON line reports prefill TFLOPS (4*B*H_q*N^2*D / 2 per
+forward) as ``value`` and decode K/V bytes per second (2*B*H_kv*L*D*2 bytes
+per step) beside it, each against the measured peaks in MEASURED_PEAKS.json.
+
+``--impl reference`` times the CPU fp64 oracle instead (host cores, a bounded
+sample of query rows of the same prefill workload per step).
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+path needs no exchange between GPUs); times are reduced with a MAX over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill TFLOPS & decode KV GB/s on 1 GB300 (fraction of peak), oracle-matched"
+FLUSH_BYTES = 256 << 20
+PREFILL = dict(B=2, Hq=32, Hkv=8, N=8192, D=128, causal=True)
+DECODE = dict(B=64, Hq=32, Hkv=8, L=8192, D=128)
+WORKLOAD = ("gqa_causal_prefill_b2_hq32_hkv8_n8192_d128_bf16"
+            " + decode_step_b64_hq32_hkv8_l8192_d128_bf16 (kv_cache_write + attn_fwd_decode)")
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def prefill_flops(B, Hq, N, D, causal, **_):
+    f = 4.0 * B * Hq * N * N * D
+    return f / 2 if causal else f
+
+
+def decode_bytes(B, Hkv, L, D, **_):
+    return 2 * B * Hkv * L * D * 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    import hashlib
+    path = os.path.join(PROFILES, "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)[kernel]
+        src = os.path.join(ROOT, "attention_fa2_fwd_gb300", "csrc", t["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != t["source_sha256"]:
+                return None
+        return float(t["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CUDA arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import attention_fa2_fwd_gb300 as A
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    A.lib()
+    stream = torch.cuda.current_stream(dev)
+    P, Dc = PREFILL, DECODE
+    gen = torch.Generator(device=dev).manual_seed(42 + rank)
+
+    def randn(*shape):
+        return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    q = randn(P["B"], P["Hq"], P["N"], P["D"])
+    k = randn(P["B"], P["Hkv"], P["N"], P["D"])
+    v = randn(P["B"], P["Hkv"], P["N"], P["D"])
+    o = torch.empty_like(q)
+    lse = torch.empty((P["B"], P["Hq"], P["N"]), dtype=torch.float32, device=dev)
+    # Decode: a cache holding L-1 tokens; each step writes token L-1 and attends to all L.
+    kc = randn(Dc["B"], Dc["Hkv"], Dc["L"], Dc["D"])
+    vc = randn(Dc["B"], Dc["Hkv"], Dc["L"], Dc["D"])
+    kn = randn(Dc["B"], Dc["Hkv"], 1, Dc["D"])
+    vn = randn(Dc["B"], Dc["Hkv"], 1, Dc["D"])
+    qd = randn(Dc["B"], Dc["Hq"], Dc["D"])
+    od = torch.empty_like(qd)
+    lsed = torch.empty((Dc["B"], Dc["Hq"]), dtype=torch.float32, device=dev)
+    ws = A.decode_workspace(Dc["B"], Dc["Hq"], Dc["Hkv"], Dc["D"], dev)
+    splits = A.attn_decode_splits(Dc["B"], Dc["Hq"], Dc["Hkv"], Dc["L"], Dc["D"])
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def do_prefill():
+        A.prefill(q, k, v, causal=True, out=o, lse_out=lse)
+
+    def do_decode():
+        A.write_kv_cache(kc, vc, kn, vn, Dc["L"] - 1)
+        A.decode(qd, kc, vc, Dc["L"], out=od, lse_out=lsed, workspace=ws)
+
+    def step(evs=None):
+        flush.zero_()
+        if evs:
+            evs[0].record(stream)
+        do_prefill()
+        if evs:
+            evs[1].record(stream)
+        flush.zero_()
+        if evs:
+            evs[2].record(stream)
+        do_decode()
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    A.check_device_error()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+        for _ in range(max(args.warmup, 10)):  # keep the GPU busy while the sampler starts
+            step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    r0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    r1.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    A.check_device_error()
+    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    region_ms = r0.elapsed_time(r1)
+    sums = torch.tensor([sum(pre_ms), sum(dec_ms), region_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(sums, op=dist.ReduceOp.MAX)
+    sum_pre, sum_dec, region_ms = (float(x) for x in sums.tolist())
+
+    flops = prefill_flops(**P)
+    kvb = decode_bytes(**Dc)
+    value = world * flops * args.steps / (sum_pre * 1e-3) / 1e12
+    decode_gbs = world * kvb * args.steps / (sum_dec * 1e-3) / 1e9
+
+    # End to end through the public API with host buffers (pinned), copies inside the timed region.
+    if True:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        n_e2e = max(3, min(args.steps, 10))
+        for _ in range(2):
+            A.prefill(dq.copy_(hq, non_blocking=True), dk.copy_(hk, non_blocking=True),
+                      dv.copy_(hv, non_blocking=True), causal=True, out=o, lse_out=lse)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            A.prefill(dq, dk, dv, causal=True, out=o, lse_out=lse)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = torch.tensor([e0.elapsed_time(e1) / n_e2e], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        e2e = {"value": round(world * flops / (float(e2e_ms) * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_call": round(float(e2e_ms), 4), "path": "pinned host Q,K,V -> attn_fwd_prefill -> host O,LSE"}
+
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    pre_avg = sum_pre / args.steps
+    dec_avg = sum_dec / args.steps
+    ach = flops / (pre_avg * 1e-3) / 1e12
+    ach_d = kvb / (dec_avg * 1e-3) / 1e9
+    tr = profiled_traffic("prefill_fwd")
+    tr_d = profiled_traffic("decode_split")
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round((sum_pre + sum_dec) / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, generated on device)",
+        "config": {"workload": WORKLOAD, "prefill": P, "decode": Dc,
+                   "l2": "flushed by a 256 MiB write before every timed kernel group (outside the event pairs)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "decode_splits": splits},
+        "prefill_ms": round(pre_avg, 4),
+        "prefill_ms_median": round(statistics.median(pre_ms), 4) if world == 1 else None,
+        "decode": {"value": round(decode_gbs, 1), "unit": "GB/s", "ms_per_step": round(dec_avg, 4),
+                   "kv_bytes_per_step": kvb, "kernels": "kv_cache_write + decode_split" + (" + decode_merge" if splits > 1 else "")},
+        "region_ms_incl_flush": round(region_ms, 3),
+        "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": tr,
+                     "peak_source": f"{peaks['source']} bf16 dense (burst)", "kernel": "prefill_fwd"},
+        "roofline_decode": {"bound": "hbm", "achieved": round(ach_d, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(ach_d / peaks["hbm_gbs"], 4), "traffic": tr_d,
+                            "peak_source": f"{peaks['source']} HBM copy", "kernel": "decode_split"},
+        "e2e": e2e,
+        "gpu_launches": args.steps * (1 + 1 + (2 if splits > 1 else 1)),
+        "clocks": clocks,
+    }
+    return line
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+
+def oracle_sample(rows_per_step: int, seed: int):
+    """A bounded sample of the prefill workload for the CPU oracle: query rows of one (b, h)."""
+    import numpy as np
+    import torch
+
+    P = PREFILL
+    g = torch.Generator().manual_seed(seed)
+    # One (b, h) of the workload: Q rows of head h and K/V of its kv head, N(0,1) bf16.
+    q = torch.randn((1, 1, P["N"], P["D"]), generator=g).to(torch.bfloat16).float().numpy()
+    k = torch.randn((1, 1, P["N"], P["D"]), generator=g).to(torch.bfloat16).float().numpy()
+    v = torch.randn((1, 1, P["N"], P["D"]), generator=g).to(torch.bfloat16).float().numpy()
+    rng = np.random.default_rng(seed)
+    rows = rng.integers(0, P["N"], size=rows_per_step)
+    sel = np.stack([np.zeros_like(rows), np.zeros_like(rows), rows], axis=1)
+    flops = float(np.sum(4.0 * P["D"] * (rows + 1)))  # causal: row i attends to i+1 keys
+    return q, k, v, sel, flops
+
+
+def time_oracle(target_s: float, seed=0):
+    """Time the oracle on growing samples until about target_s seconds; returns (TFLOPS, rows, secs, cores)."""
+    import oracle
+    cores = oracle.default_threads()
+    rows = 64
+    total_f, total_t, total_rows = 0.0, 0.0, 0
+    while total_t < target_s:
+        q, k, v, sel, f = oracle_sample(rows, seed)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, True, 1 / math.sqrt(PREFILL["D"]), sel, nthreads=cores)
+        dt = time.perf_counter() - t0
+        total_f += f
+        total_t += dt
+        total_rows += rows
+        seed += 1
+        rows = min(rows * 2, 1 << 16)
+    return total_f / total_t / 1e12, total_rows, total_t, cores
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: host cores, bounded row samples of the prefill workload per step."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    cores = oracle.default_threads()
+    rows_per_step = 512
+    for i in range(args.warmup):
+        q, k, v, sel, _ = oracle_sample(rows_per_step, 1000 + i)
+        oracle.attention_rows(q, k, v, True, 1 / math.sqrt(PREFILL["D"]), sel, nthreads=cores)
+    tot_f, tot_t = 0.0, 0.0
+    for i in range(args.steps):
+        q, k, v, sel, f = oracle_sample(rows_per_step, i)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, True, 1 / math.sqrt(PREFILL["D"]), sel, nthreads=cores)
+        tot_t += time.perf_counter() - t0
+        tot_f += f
+    val = tot_f / tot_t / 1e12
+    sample = (f"{rows_per_step} random query rows of one (b, h) of the causal prefill workload per step "
+              f"(N=8192, D=128; FLOPs counted as 4*D*(i+1) per row i)")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16-rounded)",
+        "config": {"workload": WORKLOAD, "prefill": PREFILL, "decode": DECODE},
+        "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_ours(args, rank, world, local_rank)
+        if line is not None:
+            if world == 1:
+                tf, rows, secs, cores = time_oracle(args.cpu_baseline_seconds)
+                line["cpu_baseline"] = {
+                    "value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                    "sample": (f"{rows} random query rows of single (b, h) heads of the causal prefill workload "
+                               f"(N=8192, D=128), {secs:.1f} s on the host cores; FLOPs 4*D*(i+1) per row i")}
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -101,6 +101,14 @@ attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void
 size_t attn_decode_workspace_size(int B, int H_q, int H_kv, int D);
 
 /*
+ * attn_decode_splits -- number of KV splits attn_fwd_decode uses for these
+ * sizes on the current device (1 means one kernel and no workspace traffic;
+ * more means a split kernel plus a merge kernel).  Returns 0 on bad
+ * arguments.  Host-only.
+ */
+int attn_decode_splits(int B, int H_q, int H_kv, int cache_len, int D);
+
+/*
  * attn_fwd_decode -- attention of ONE new query token per (batch, q-head) over
  * a preallocated KV cache whose first cache_len positions are valid.
  *

@@ -127,12 +127,33 @@ def test_decode_against_oracle_gqa_ratios():
 
 def test_decode_workspace_errors():
     import attention_fa2_fwd_gb300 as A
-    B, Hq, Hkv, D, L = 2, 32, 8, 128, 4096
+    B, Hq, Hkv, D, L = 2, 32, 8, 128, 8192
     q = torch.zeros((B, Hq, D), dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros((B, Hkv, L, D), dtype=torch.bfloat16, device="cuda")
     need = A.attn_decode_workspace_size(B, Hq, Hkv, D)
     assert need > 0  # B=2 splits the cache over many CTAs
-    small = torch.empty(need // 8, dtype=torch.float32, device="cuda")
+    assert A.attn_decode_splits(B, Hq, Hkv, L, D) > 1
+    small = torch.empty(16, dtype=torch.float32, device="cuda")
     with pytest.raises(A.AttnError) as e:
         A.decode(q, kc, kc, L, workspace=small)
     assert e.value.status == A.ATTN_ERR_WORKSPACE
+    # A workspace of attn_decode_workspace_size bytes serves every cache length.
+    ws = A.decode_workspace(B, Hq, Hkv, D)
+    for cl in (1, 255, 256, 257, 4097, 8192):
+        A.decode(q, kc, kc, cl, workspace=ws)
+    torch.cuda.synchronize()
+
+
+def test_decode_split_count_does_not_change_result():
+    """B=2 uses many splits, B=64 few; the same (b, h) rows must agree within tolerance."""
+    import attention_fa2_fwd_gb300 as A
+    Hq, Hkv, D, L = 32, 8, 128, 4097
+    k, v = I.decode_stream(2, Hkv, L, D, "bf16", seed=77)
+    q = I.decode_queries(2, Hq, D, [L - 1], "bf16", seed=77)[:, :, 0]
+    o2, l2 = A.decode(q.cuda(), k.cuda(), v.cuda(), L)
+    kk = k.repeat(32, 1, 1, 1).cuda()
+    vv = v.repeat(32, 1, 1, 1).cuda()
+    o64, l64 = A.decode(q.repeat(32, 1, 1).cuda(), kk, vv, L)
+    torch.cuda.synchronize()
+    assert A.attn_decode_splits(2, Hq, Hkv, L, D) != A.attn_decode_splits(64, Hq, Hkv, L, D)
+    assert_close(o64[:2], np64(o2), l64[:2], np64(l2), "splits")
