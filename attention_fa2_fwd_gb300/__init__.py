@@ -34,8 +34,8 @@ ATTN_BF16 = 1
 
 # Every function that include/attn.h declares.
 EXPORTS = ("attn_fwd_prefill", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
-           "kv_cache_write",
-           "attn_get_device_error", "attn_status_string", "attn_version")
+           "attn_fwd_decode_noalloc", "kv_cache_write", "attn_get_device_error", "attn_status_string",
+           "attn_version")
 
 
 class AttnLibraryMissing(RuntimeError):
@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_decode.restype = i32
             L.attn_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                           i64p, i64p, i64p, i64p, f32, vp, ctypes.c_size_t, vp]
+            L.attn_fwd_decode_noalloc.restype = i32
+            L.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                                  i64p, i64p, i64p, i64p, f32, vp]
             L.kv_cache_write.restype = i32
             L.kv_cache_write.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                          i64p, i64p, i64p, i64p, vp]
@@ -114,6 +117,19 @@ def attn_fwd_decode(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len,
     return lib().attn_fwd_decode(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, _strides(q_str),
                                  _strides(kc_str), _strides(vc_str), _strides(o_str), float(scale), workspace,
                                  workspace_bytes, stream)
+
+
+def attn_fwd_decode_noalloc(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, q_str, kc_str, vc_str,
+                            o_str, scale, stream) -> int:
+    """attn_fwd_decode without a workspace argument, for callers that may not allocate device memory.
+
+    The split partials go to a 4 MiB scratch array inside the library (shared
+    by every call on the device; overlapping calls race on it).  Returns
+    ATTN_ERR_WORKSPACE if the call would need more than 4 MiB of scratch.
+    """
+    return lib().attn_fwd_decode_noalloc(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D,
+                                         _strides(q_str), _strides(kc_str), _strides(vc_str), _strides(o_str),
+                                         float(scale), stream)
 
 
 def kv_cache_write(k_cache, v_cache, k_new, v_new, dtype, B, H_kv, n_new, D, pos, max_len, kc_str, vc_str, kn_str,

@@ -362,3 +362,62 @@ const char *attn_status_string(attn_status_t status) {
 int attn_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// attn_fwd_decode_noalloc: decode whose split scratch lives in a fixed array
+// compiled into the library instead of a caller-provided buffer.
+namespace attn {
+namespace {
+
+// Scratch for the split partials of attn_fwd_decode_noalloc.  It lives in the
+// library image, so every device that loads the library holds these bytes
+// until the process exits, and every call on a device shares them.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The name
+// g_noalloc_scratch means nothing to the device in host code, so the address
+// is looked up once per device, with that device current.
+attn_status_t noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                                      attn_dtype_t dtype, int B, int H_q, int H_kv, int cache_len, int D,
+                                      const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
+                                      const int64_t o_str[4], float scale, void *stream) {
+  // Sizes first: the scratch this call would need must fit the fixed array.
+  if (B < 1 || H_q < 1 || H_kv < 1 || cache_len < 1 || H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  const DeviceState *dev = nullptr;
+  attn_status_t st = device_state(&dev);
+  if (st != ATTN_OK) return st;
+  int nsplit = 1, chunk = cache_len;
+  decode_plan(B, H_q, H_kv, cache_len, D, dev->sm_count, &nsplit, &chunk);
+  if (decode_ws_bytes(B, H_q, D, nsplit) > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != ATTN_OK) return st;
+  // Nothing in the scratch has to start at zero: each partial the merge kernel
+  // reads is written earlier in the same call.
+  return attn_fwd_decode(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, q_str, kc_str, vc_str,
+                         o_str, scale, scratch, kNoAllocScratchBytes, stream);
+}
+
+}  // extern "C"

@@ -156,6 +156,41 @@ attn_status_t kv_cache_write(void *k_cache, void *v_cache, const void *k_new, co
                              const int64_t vn_str[4], void *stream);
 
 /*
+ * attn_fwd_decode_noalloc -- attn_fwd_decode for callers that may not allocate
+ * device memory.  (The pages have no counterpart of this entry point; it is a
+ * convenience of this library.)
+ *
+ * Some callers cannot call cudaMalloc or hand the library a workspace: a
+ * plugin whose host framework owns every device allocation through its own
+ * planner and forbids allocating after start-up, or a latency-critical serving
+ * loop that must never hit cudaMalloc's implicit device synchronisation or an
+ * out-of-memory failure in the middle of a request.  This entry point takes
+ * the same arguments as attn_fwd_decode minus the workspace; the split
+ * partials go to a scratch array of 4 MiB compiled into the library, which
+ * every device that loads the library keeps until the process exits.  It
+ * allocates nothing and calls no allocating routine.
+ *
+ *   Limit: the call needs 4 * B * H_q * splits * (D + 1) bytes of scratch
+ *   (splits = attn_decode_splits(...), 0 bytes when splits == 1); if that
+ *   exceeds 4 MiB it returns ATTN_ERR_WORKSPACE and launches nothing.
+ *   Otherwise arguments, errors and results are those of attn_fwd_decode.
+ *
+ *   Set-up: the first call on a device looks up the device address of the
+ *   scratch array (with that device current) and caches it; make that first
+ *   call before capturing any stream.
+ *
+ *   Sharing: every call on a device uses the same scratch array, and the array
+ *   keeps whatever the previous call left in it (nothing in it needs to start
+ *   at zero).  Two calls whose kernels overlap on the GPU -- on different
+ *   streams, or from different host threads -- race on the array and corrupt
+ *   each other's results: order such calls on one stream.
+ */
+attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                                      attn_dtype_t dtype, int B, int H_q, int H_kv, int cache_len, int D,
+                                      const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
+                                      const int64_t o_str[4], float scale, void *stream);
+
+/*
  * attn_get_device_error -- synchronise `stream`, read the device error word of
  * the current device and clear it.  Returns ATTN_OK if no kernel reported a
  * failure, ATTN_ERR_DEVICE_TIMEOUT if one gave up on a wait, ATTN_ERR_CUDA if

@@ -1,0 +1,78 @@
+"""attn_fwd_decode_noalloc: decode for callers that may not allocate device memory.
+
+Some callers cannot call cudaMalloc or pass the library a workspace -- a
+plugin whose host framework owns all device memory, or a serving loop that
+must not risk an allocation's device synchronisation or failure mid-request.
+For them the library keeps a 4 MiB scratch array of its own.  This test calls
+that entry point through the C ABI and checks its output against the
+workspace-taking attn_fwd_decode on the same inputs, for two calls in a row
+(the second call finds the first call's partials still in the shared scratch
+array and must not be affected by them).
+
+The file is named so that pytest collects it last.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attention_fa2_fwd_gb300 import inputs as I
+from tests.helpers import assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def A():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_fa2_fwd_gb300 as A
+    A.lib()
+    return A
+
+
+def _call_noalloc(A, q, kc, vc, cache_len):
+    B, Hq, D = q.shape
+    Hkv = kc.shape[1]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    q4, o4 = q.unsqueeze(2), o.unsqueeze(2)
+    st = A.attn_fwd_decode_noalloc(q4.data_ptr(), kc.data_ptr(), vc.data_ptr(), o4.data_ptr(), lse.data_ptr(),
+                                   A.ATTN_BF16, B, Hq, Hkv, cache_len, D, q4.stride(), kc.stride(), vc.stride(),
+                                   o4.stride(), 1.0 / math.sqrt(D), torch.cuda.current_stream().cuda_stream)
+    assert st == A.ATTN_OK, A.attn_status_string(st)
+    return o, lse
+
+
+def test_noalloc_decode_matches_workspace_decode_twice(A):
+    Hq, Hkv, D, L = 32, 8, 128, 4097
+    # B=2 splits the cache many ways, so the scratch array is really used.
+    assert A.attn_decode_splits(2, Hq, Hkv, L, D) > 1
+    k, v = I.decode_stream(2, Hkv, L, D, "bf16", seed=21)
+    kc, vc = k.cuda(), v.cuda()
+    queries = I.decode_queries(2, Hq, D, [L - 1, 2000], "bf16", seed=21).cuda()
+    for j, cache_len in enumerate((L, 2001)):
+        q = queries[:, :, j].contiguous()
+        o_ref, lse_ref = A.decode(q, kc, vc, cache_len)
+        o, lse = _call_noalloc(A, q, kc, vc, cache_len)
+        torch.cuda.synchronize()
+        A.check_device_error()
+        assert_close(o, np64(o_ref), lse, np64(lse_ref), f"call {j + 1}")
+
+
+def test_noalloc_decode_rejects_scratch_beyond_limit(A):
+    # B=75, H_q=64, H_kv=8 splits each kv head in two on a 152-SM GB300, which
+    # needs 4 * 75 * 64 * 2 * 129 bytes (4.95 MB) of partials: more than 4 MiB.
+    B, Hq, Hkv, D, L = 75, 64, 8, 128, 8192
+    splits = A.attn_decode_splits(B, Hq, Hkv, L, D)
+    need = 4 * B * Hq * splits * (D + 1) if splits > 1 else 0
+    if need <= (4 << 20):
+        pytest.skip("on this device the case fits the scratch array")
+    P = 0x7F0000000000  # never dereferenced: the size check returns before any launch
+    st = A.attn_fwd_decode_noalloc(P, P, P, P, None, A.ATTN_BF16, B, Hq, Hkv, L, D, (Hq * D, D, D, 1),
+                                   (Hkv * L * D, L * D, D, 1), (Hkv * L * D, L * D, D, 1), (Hq * D, D, D, 1),
+                                   0.088, None)
+    assert st == A.ATTN_ERR_WORKSPACE
