@@ -81,6 +81,21 @@ def profiled_traffic(kernel: str):
         return None
 
 
+def reduce_max(values, world, device):
+    """Element-wise MAX of per-rank timings over all ranks (identity for one process)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def aggregate_throughput(units_per_rank, world, steps, max_ms_total):
+    """Whole-job rate: units every rank processed in `steps` steps over the slowest rank's time (ms)."""
+    return world * units_per_rank * steps / (max_ms_total * 1e-3)
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
 
@@ -218,15 +233,12 @@ def run_ours(args, rank, world, local_rank):
     pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
     region_ms = r0.elapsed_time(r1)
-    sums = torch.tensor([sum(pre_ms), sum(dec_ms), region_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(sums, op=dist.ReduceOp.MAX)
-    sum_pre, sum_dec, region_ms = (float(x) for x in sums.tolist())
+    sum_pre, sum_dec, region_ms = reduce_max([sum(pre_ms), sum(dec_ms), region_ms], world, dev)
 
     flops = prefill_flops(**P)
     kvb = decode_bytes(**Dc)
-    value = world * flops * args.steps / (sum_pre * 1e-3) / 1e12
-    decode_gbs = world * kvb * args.steps / (sum_dec * 1e-3) / 1e9
+    value = aggregate_throughput(flops, world, args.steps, sum_pre) / 1e12
+    decode_gbs = aggregate_throughput(kvb, world, args.steps, sum_dec) / 1e9
 
     # End to end through the public API with host buffers (pinned), copies inside the timed region.
     if True:
@@ -252,14 +264,12 @@ def run_ours(args, rank, world, local_rank):
             hl.copy_(lse, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = torch.tensor([e0.elapsed_time(e1) / n_e2e], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+        e2e_ms = reduce_max([e0.elapsed_time(e1) / n_e2e], world, dev)[0]
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
         d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-        e2e = {"value": round(world * flops / (float(e2e_ms) * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+        e2e = {"value": round(aggregate_throughput(flops, world, 1, e2e_ms) / 1e12, 2), "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_call": round(float(e2e_ms), 4), "path": "pinned host Q,K,V -> attn_fwd_prefill -> host O,LSE"}
+               "ms_per_call": round(e2e_ms, 4), "path": "pinned host Q,K,V -> attn_fwd_prefill -> host O,LSE"}
 
     if rank != 0:
         return None

@@ -141,8 +141,9 @@ attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_
  * kv_cache_write -- copy n_new tokens of K and V into a preallocated cache at
  * positions [pos, pos + n_new).
  *
- * Follows "Triton-FlashAttention", Phase 2: the cache is a static buffer that
- * is never regrown, and the write is kept apart from the attention kernel.
+ * Follows "Triton-FlashAttention", Phase 2: the cache is allocated once with
+ * room for max_len positions and filled in place (no reallocation as it
+ * grows), and writing into it is a call of its own, apart from attention.
  *
  *   k_cache, v_cache  (B, H_kv, max_len, D) strides kc_str / vc_str   written
  *   k_new, v_new      (B, H_kv, n_new, D)   strides kn_str / vn_str   read

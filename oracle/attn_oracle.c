@@ -24,8 +24,8 @@
  *                        offset between the query and key sequences)
  *     4. softmax        m = max_j s_j, e_j = exp(s_j - m), l = sum_j e_j
  *     5. output         O[b,h,i,:] = sum_j (e_j / l) * V[b,hk,j,:]
- *                       (Correctness requirements: O / l must equal the
- *                        true softmax-weighted sum of V)
+ *                       (Correctness requirements: after the loop O / l
+ *                        is the softmax-weighted average of the V rows)
  *     6. log-sum-exp    LSE[b,h,i] = m + ln(l)
  *                       (step 8: natural log, and not m alone)
  *
@@ -34,7 +34,7 @@
  * score row instead.  exp/log are the C library's, in double precision.
  *
  * Decode (one new query token over a cache of cache_len valid positions,
- * "Triton-FlashAttention", Phase 2: every cached position is valid) is the
+ * "Triton-FlashAttention", Phase 2: all cache_len cached positions take part) is the
  * same definition with N_q = 1, N_kv = cache_len and no causal mask.
  *
  * Layout: every tensor is a dense, contiguous fp64 array in (b, h, n, d)
