@@ -130,23 +130,37 @@ attn_status_t make_map(CUtensorMap *map, const void *base, bool bf16, const int6
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Largest number of KV splits decode may use for these sizes on this device.
+// Number of KV splits decode uses on long caches for these sizes on this
+// device: the fewest splits that give at least one full wave of resident
+// CTAs (kDecodeCtasPerSm per SM) with the last wave at least 85 % full;
+// failing that, the split count (<= 64) whose last wave is fullest.
 int decode_max_splits(int B, int H_q, int H_kv, int sm_count) {
   const int group = H_q / H_kv;
   const int gh = decode_heads_per_cta(group);
   const int nhc = (group + gh - 1) / gh;
-  const int64_t ctas = static_cast<int64_t>(B) * H_kv * nhc;
-  const int64_t target = 4LL * sm_count;
-  int64_t s = (target + ctas - 1) / ctas;
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, 64)));
+  const double ctas = static_cast<double>(B) * H_kv * nhc;
+  const double slots = static_cast<double>(kDecodeCtasPerSm) * sm_count;
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= 64; ++s) {
+    const double waves = ctas * s / slots;
+    const double eff = waves / std::ceil(waves);
+    if (waves >= 1.0 && eff >= 0.85) return s;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
 }
 
-// Split plan of one decode call: every split holds a multiple of the CTA's
-// step in keys (except the last), at least kMinChunk keys, and none is empty.
+// Split plan of one decode call: every split holds a multiple of the stage
+// size in keys (except the last), at least kMinChunk keys, and none is empty.
 void decode_plan(int B, int H_q, int H_kv, int cache_len, int D, int sm_count, int *nsplit_out, int *chunk_out) {
   constexpr int kMinChunk = 256;
+  (void)D;
   const int max_splits = decode_max_splits(B, H_q, H_kv, sm_count);
-  const int step = decode_tokens_per_step(D);
+  const int step = kDecodeStageTokens;
   int nsplit = std::min<int>(max_splits, (cache_len + kMinChunk - 1) / kMinChunk);
   nsplit = std::max(nsplit, 1);
   int chunk = (cache_len + nsplit - 1) / nsplit;
@@ -285,7 +299,13 @@ attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_
   p.nsplit = nsplit;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   if (static_cast<int64_t>(H_kv) * nhc > 65535) return ATTN_ERR_INVALID_ARG;
-  cudaError_t e = launch_decode(D, dtype == ATTN_BF16, gh, p, B, H_kv, static_cast<cudaStream_t>(stream));
+  // Tensor maps over the valid rows only: rows >= cache_len read as zeros.
+  CUtensorMap tk, tv;
+  const bool bf16 = dtype == ATTN_BF16;
+  if ((st = make_map(&tk, k_cache, bf16, csz, kc_str, kDecodeStageTokens, &p.slots_k)) ||
+      (st = make_map(&tv, v_cache, bf16, csz, vc_str, kDecodeStageTokens, &p.slots_v)))
+    return st;
+  cudaError_t e = launch_decode(D, bf16, gh, tk, tv, p, B, H_kv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

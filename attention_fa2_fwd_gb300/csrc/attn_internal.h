@@ -14,6 +14,9 @@ namespace attn {
 // Prefill work tile: 128 query rows x 128 key/value rows per pipeline step.
 constexpr int kPrefillBM = 128;
 constexpr int kPrefillBN = 128;
+// Decode: cache rows per shared-memory stage, and CTAs resident per SM.
+constexpr int kDecodeStageTokens = 64;
+constexpr int kDecodeCtasPerSm = 2;
 
 struct PrefillParams {
   void *o;
@@ -39,6 +42,7 @@ struct DecodeParams {
   int64_t o_sb, o_sh;
   int Hq, group, nhc, cache_len, chunk, nsplit;
   float scale_log2;
+  uint32_t slots_k, slots_v;  // tensor-map coordinate slots, as for prefill
 };
 
 struct KvWriteParams {
@@ -56,11 +60,11 @@ cudaError_t launch_prefill(int D, bool causal, bool bf16, const CUtensorMap &tq,
                            const CUtensorMap &tv, const PrefillParams &p, int B, cudaStream_t stream);
 size_t prefill_smem_bytes(int D);
 
-// Decode: split selection helpers and launch.
+// Decode: heads served by one CTA, and launch (split kernel, plus the merge
+// kernel when nsplit > 1).
 int decode_heads_per_cta(int group);
-int decode_tokens_per_step(int D);
-cudaError_t launch_decode(int D, bool bf16, int heads_per_cta, const DecodeParams &p, int B, int Hkv,
-                          cudaStream_t stream);
+cudaError_t launch_decode(int D, bool bf16, int heads_per_cta, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const DecodeParams &p, int B, int Hkv, cudaStream_t stream);
 
 cudaError_t launch_kv_cache_write(const KvWriteParams &p, cudaStream_t stream);
 

@@ -2,22 +2,27 @@
 //
 // Decode ("Triton-FlashAttention", Phase 2): one new query token per
 // (batch, q-head) attends to the first cache_len rows of a preallocated cache.
-// The work is HBM-bound (every cached K/V byte is read once per step), so
-// this path stays on the CUDA cores and is built for streaming:
+// The work is HBM-bound -- every cached K/V byte is read once per step -- so it
+// runs on the CUDA cores and is organised around streaming the cache:
 //
-//   decode_split: one CTA per (split, kv-head [x head chunk], batch).  The
+//   decode_split: one CTA per (split, kv-head [x head chunk], batch), two CTAs
+//     resident per SM.  A producer warp streams the split's keys and values
+//     through a 3-deep ring of 64-token shared-memory stages with TMA tensor
+//     loads (128-byte swizzle), so the bytes in flight cost no registers.  The
 //     CTA reads its share of the cache ONCE for all H_q/H_kv query heads of
-//     the group.  Each row of K or V is read by D/8 lanes with 128-bit
-//     non-caching loads (a warp covers 256/D consecutive tokens per load,
-//     fully coalesced), next-step rows are prefetched while the current
-//     step is reduced, dot products are finished with xor warp shuffles
-//     across the lanes of a row, and every group of lanes keeps its own
-//     online-softmax state (running max, running sum, unnormalised output
-//     slice), in base-2 units.  The groups of a CTA are merged through shared
-//     memory at the end.
-//   decode_merge: when the cache is split over several CTAs, combines the
-//     partials of every (b, q-head): lse = ln sum_s e^{lse_s},
-//     O = sum_s e^{lse_s - lse} O_s.
+//     the group.  Four consumer warps each take 16 tokens of a stage:
+//       scores   lane = (token, half of D): one 16-byte swizzled shared load per
+//                8 dimensions, packed fma.rn.f32x2 against the pre-scaled
+//                query, one xor-16 shuffle to join the two halves;
+//       softmax  a warp-wide max per head (xor shuffles), base-2 exponentials,
+//                per-lane partial sums (reduced once at the end);
+//       P . V    lane = (token slot, 16-byte slice of D), P broadcast from
+//                shared memory, packed FMAs into per-lane accumulators.
+//     Each warp keeps its own online-softmax state; warps merge through shared
+//     memory at the end, and the result is either the output (one split) or a
+//     partial (O_s, lse_s) in the workspace.
+//   decode_merge: combines the partials of every (b, q-head):
+//     lse = ln sum_s e^{lse_s}, O = sum_s e^{lse_s - lse} O_s.
 //
 // kv_cache_write: copies new tokens into cache rows [pos, pos + n) with one
 // 16-byte piece per thread.
@@ -30,35 +35,62 @@
 namespace attn {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kWarps = kThreads / 32;
-constexpr int kU = 4;  // tokens per lane group per step
+constexpr int kTok = kDecodeStageTokens;  // tokens per stage
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kTokPerWarp = kTok / kConsumerWarps;  // 16
 constexpr float kLn2 = 0.693147180559945309f;
+static_assert(kTokPerWarp == 16, "score mapping assumes 16 tokens per warp and stage");
 
-__device__ __forceinline__ uint4 ld_stream(const void *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+template <int D, int GH>
+struct DecCfg {
+  static constexpr int KCH = D / 64;                  // 128-byte boxes per row
+  static constexpr int CPR = D / 8;                   // 16-byte chunks per row
+  static constexpr int TPI = 32 / CPR;                // tokens per P.V step of a warp
+  static constexpr uint32_t BOX_BYTES = kTok * 128;   // one TMA box: kTok rows x 64 elements
+  static constexpr uint32_t KV_BYTES = kTok * D * 2;  // K (or V) of one stage
+  static constexpr uint32_t STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr uint32_t OFF_Q = kStages * STAGE_BYTES;          // fp32 [GH][D]
+  static constexpr uint32_t OFF_P = OFF_Q + GH * D * 4;             // fp32 [warps][16][GH]
+  static constexpr uint32_t OFF_ML = OFF_P + kConsumerWarps * kTokPerWarp * GH * 4;  // m, l [warps][GH]
+  static constexpr uint32_t OFF_BAR = OFF_ML + 2 * kConsumerWarps * GH * 4;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 2 * kStages * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+  // End-of-CTA merge area, placed over the (then idle) stage ring: fp32 [warps][TPI][GH][D].
+  static constexpr uint32_t MERGE_BYTES = kConsumerWarps * TPI * GH * D * 4;
+  static_assert(MERGE_BYTES <= kStages * STAGE_BYTES, "merge area must fit in the stage ring");
+};
+
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 unf2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
   return v;
 }
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
+// Two 16-bit values of one 32-bit word as a packed fp32 pair (element order kept).
 template <bool BF16>
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if constexpr (BF16) {
-      __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
-      float2 t = __bfloat1622float2(h);
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
-    } else {
-      __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
-      float2 t = __half22float2(h);
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
-    }
+__device__ __forceinline__ uint64_t widen2(uint32_t w) {
+  if constexpr (BF16) {
+    return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  } else {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    return f2(t.x, t.y);
   }
 }
 
@@ -70,184 +102,253 @@ __device__ __forceinline__ void store_out(void *base, int64_t idx, float x) {
     reinterpret_cast<__half *>(base)[idx] = __float2half_rn(x);
 }
 
-template <int D, int GH, bool BF16>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
-  constexpr int LPT = D / 8;       // lanes per token row (16 bytes each)
-  constexpr int GPW = 32 / LPT;    // lane groups per warp
-  constexpr int NG = kWarps * GPW; // lane groups per CTA
-  constexpr int U = (GH >= 8) ? 2 : kU;  // tokens per lane group per step
-  constexpr int STEP = NG * U;     // tokens per CTA step
-  __shared__ float sm_m[NG][GH];
-  __shared__ float sm_l[NG][GH];
-  __shared__ float sm_acc[NG][GH][D];
+// Byte offset of 16-byte chunk c (of CPR) of row r inside a stage tensor laid
+// out as KCH boxes of [kTok rows][128 B] with the 128-byte TMA swizzle.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * (kTok * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
 
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, int d, int n, int h, int b,
+                                         uint32_t slots, uint32_t bar) {
+  const int sn = slots & 3, sh = (slots >> 2) & 3;
+  const int c1 = (sn == 1) ? n : (sh == 1) ? h : b;
+  const int c2 = (sn == 2) ? n : (sh == 2) ? h : b;
+  const int c3 = (sn == 3) ? n : (sh == 3) ? h : b;
+  tma_load_4d(dst, map, d, c1, c2, c3, bar);
+}
+
+template <int D, int GH, bool BF16>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const DecodeParams p) {
+  using C = DecCfg<D, GH>;
+  extern __shared__ uint8_t smem_raw[];
   if (load_volatile(p.err) != 0) return;
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (sbase - raw);
+  float *sq = reinterpret_cast<float *>(smem + C::OFF_Q);
+  float *sp = reinterpret_cast<float *>(smem + C::OFF_P);
+  float *sm_m = reinterpret_cast<float *>(smem + C::OFF_ML);
+  float *sm_l = sm_m + kConsumerWarps * GH;
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto FULL = [&](int s) -> uint32_t { return bar0 + 8u * s; };
+  auto EMPTY = [&](int s) -> uint32_t { return bar0 + 8u * (kStages + s); };
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC);
 
   const int split = blockIdx.x;
   const int hk = blockIdx.y / p.nhc, hc = blockIdx.y % p.nhc;
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gi = warp * GPW + lane / LPT;
-  const int d0 = (lane % LPT) * 8;
-  const int h_first = hk * p.group + hc * GH;  // first q head of this CTA
-  const int nh = min(GH, p.group - hc * GH);   // q heads actually handled
-
-  // Query slices, pre-multiplied by scale * log2(e).
-  float qf[GH][8];
-#pragma unroll
-  for (int i = 0; i < GH; ++i) {
-    if (i < nh) {
-      const char *qp = reinterpret_cast<const char *>(p.q) +
-                       2 * (static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(h_first + i) * p.q_sh + d0);
-      float f[8];
-      unpack8<BF16>(*reinterpret_cast<const uint4 *>(qp), f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qf[i][e] = f[e] * p.scale_log2;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qf[i][e] = 0.f;
-    }
-  }
-
-  float m[GH], l[GH], acc[GH][8];
-#pragma unroll
-  for (int i = 0; i < GH; ++i) {
-    m[i] = -INFINITY;
-    l[i] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
-  }
-
+  const int h_first = hk * p.group + hc * GH;
+  const int nh = min(GH, p.group - hc * GH);
   const int t_begin = split * p.chunk;
   const int t_end = min(t_begin + p.chunk, p.cache_len);
-  const char *kbase = reinterpret_cast<const char *>(p.kc) +
-                      2 * (static_cast<int64_t>(b) * p.kc_sb + static_cast<int64_t>(hk) * p.kc_sh + d0);
-  const char *vbase = reinterpret_cast<const char *>(p.vc) +
-                      2 * (static_cast<int64_t>(b) * p.vc_sb + static_cast<int64_t>(hk) * p.vc_sh + d0);
-  const int64_t kstep = 2 * p.kc_sn, vstep = 2 * p.vc_sn;
+  const int n_tiles = (t_end - t_begin + kTok - 1) / kTok;
 
-  // Raw 16-byte pieces of the current step; the next step's are loaded while
-  // this one is reduced.
-  uint4 kr[U], vr[U];
-  auto load_step = [&](int base, uint4 (&kk)[U], uint4 (&vv)[U]) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int t = base + u * NG + gi;
-      if (t < t_end) {
-        kk[u] = ld_stream(kbase + t * kstep);
-        vv[u] = ld_stream(vbase + t * vstep);
-      } else {
-        kk[u] = make_uint4(0, 0, 0, 0);
-        vv[u] = make_uint4(0, 0, 0, 0);
-      }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(EMPTY(s), kConsumerWarps);
     }
-  };
-  load_step(t_begin, kr, vr);
-  for (int base = t_begin; base < t_end; base += STEP) {
-    uint4 kn[U], vn[U];
-    const bool more = base + STEP < t_end;
-    if (more) load_step(base + STEP, kn, vn);
-
-    float s[U][GH];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float kf[8];
-      unpack8<BF16>(kr[u], kf);
-#pragma unroll
-      for (int i = 0; i < GH; ++i) {
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaf(qf[i][e], kf[e], a);
-        s[u][i] = a;
-      }
-    }
-#pragma unroll
-    for (int off = LPT / 2; off >= 1; off >>= 1)
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int i = 0; i < GH; ++i) s[u][i] += __shfl_xor_sync(0xffffffffu, s[u][i], off);
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (base + u * NG + gi >= t_end) {
-#pragma unroll
-        for (int i = 0; i < GH; ++i) s[u][i] = -INFINITY;
-      }
-    }
-    float pw[U][GH];
-#pragma unroll
-    for (int i = 0; i < GH; ++i) {
-      float mx = s[0][i];
-#pragma unroll
-      for (int u = 1; u < U; ++u) mx = fmaxf(mx, s[u][i]);
-      const float m_new = fmaxf(m[i], mx);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = fast_exp2(m[i] - m_use);
-      l[i] *= alpha;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[i][e] *= alpha;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        pw[u][i] = fast_exp2(s[u][i] - m_use);
-        l[i] += pw[u][i];
-      }
-      m[i] = m_new;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float vf[8];
-      unpack8<BF16>(vr[u], vf);
-#pragma unroll
-      for (int i = 0; i < GH; ++i)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(pw[u][i], vf[e], acc[i][e]);
-    }
-    if (more) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        kr[u] = kn[u];
-        vr[u] = vn[u];
-      }
-    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
   }
-
-  // Merge the lane groups of this CTA.
-  if ((lane % LPT) == 0) {
-#pragma unroll
-    for (int i = 0; i < GH; ++i) {
-      sm_m[gi][i] = m[i];
-      sm_l[gi][i] = l[i];
+  // Query rows of this CTA's heads, pre-multiplied by scale * log2(e).
+  for (int idx = threadIdx.x; idx < GH * D; idx += kThreads) {
+    const int i = idx / D, d = idx % D;
+    float x = 0.f;
+    if (i < nh) {
+      const int64_t off = static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(h_first + i) * p.q_sh + d;
+      if constexpr (BF16)
+        x = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.q)[off]);
+      else
+        x = __half2float(reinterpret_cast<const __half *>(p.q)[off]);
     }
+    sq[idx] = x * p.scale_log2;
   }
-#pragma unroll
-  for (int i = 0; i < GH; ++i)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sm_acc[gi][i][d0 + e] = acc[i][e];
   __syncthreads();
 
-  for (int idx = threadIdx.x; idx < nh * D; idx += kThreads) {
-    const int i = idx / D, d = idx % D;
-    float M = -INFINITY;
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages && !(ok = mbar_wait(EMPTY(st), ((j / kStages) - 1) & 1, abort_flag, p.err))) break;
+        const uint32_t dst = sbase + st * C::STAGE_BYTES;
+        const int t0 = t_begin + j * kTok;
+        mbar_arrive_expect_tx(FULL(st), C::STAGE_BYTES);
 #pragma unroll
-    for (int g = 0; g < NG; ++g) M = fmaxf(M, sm_m[g][i]);
-    const float M_use = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f, A = 0.f;
-#pragma unroll
-    for (int g = 0; g < NG; ++g) {
-      const float w = fast_exp2(sm_m[g][i] - M_use);
-      L = fmaf(sm_l[g][i], w, L);
-      A = fmaf(sm_acc[g][i][d], w, A);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_tile(dst + c * C::BOX_BYTES, &tmK, c * 64, t0, hk, b, p.slots_k, FULL(st));
+          tma_tile(dst + C::KV_BYTES + c * C::BOX_BYTES, &tmV, c * 64, t0, hk, b, p.slots_v, FULL(st));
+        }
+        ++issued;
+      }
+      if (!ok) {
+        for (int i = max(0, issued - kStages); i < issued; ++i)
+          mbar_wait(FULL(i % kStages), (i / kStages) & 1, nullptr, p.err);
+      }
     }
-    const int hq = h_first + i;
-    const float o = (L > 0.f) ? A / L : 0.f;
-    const float lse = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
-    if (p.nsplit == 1) {
-      store_out<BF16>(p.o, static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(hq) * p.o_sh + d, o);
-      if (d == 0 && p.lse != nullptr) p.lse[static_cast<int64_t>(b) * p.Hq + hq] = lse;
-    } else {
-      const int64_t row = (static_cast<int64_t>(b) * p.Hq + hq) * p.nsplit + split;
-      p.ws_o[row * D + d] = o;
-      if (d == 0) p.ws_lse[row] = lse;
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ consumer warps
+    const int tl = lane & 15;           // token of this lane within the warp's 16 (scores)
+    const int half = lane >> 4;         // which half of D this lane's score covers
+    const int row = warp * kTokPerWarp + tl;
+    const int slot = lane / C::CPR;     // token slot for P . V
+    const int sub = lane % C::CPR;      // 16-byte slice of D for P . V
+    float m[GH];
+    float lpart[GH];
+    uint64_t acc[GH][4];
+#pragma unroll
+    for (int i = 0; i < GH; ++i) {
+      m[i] = -INFINITY;
+      lpart[i] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][e] = 0;  // +0.0f, +0.0f
+    }
+    float *pw = sp + warp * kTokPerWarp * GH;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j % kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(FULL(st), (j / kStages) & 1, abort_flag, p.err));
+      if (!ok) break;
+      const uint8_t *sk = smem + st * C::STAGE_BYTES;
+      const uint8_t *sv = sk + C::KV_BYTES;
+
+      // scores of this lane's token over its half of D
+      uint64_t s2[GH];
+#pragma unroll
+      for (int i = 0; i < GH; ++i) s2[i] = 0;
+#pragma unroll
+      for (int cc = 0; cc < C::CPR / 2; ++cc) {
+        const int c = half * (C::CPR / 2) + cc;
+        const uint4 kw = *reinterpret_cast<const uint4 *>(sk + swz(row, c));
+        const uint64_t k01 = widen2<BF16>(kw.x), k23 = widen2<BF16>(kw.y);
+        const uint64_t k45 = widen2<BF16>(kw.z), k67 = widen2<BF16>(kw.w);
+#pragma unroll
+        for (int i = 0; i < GH; ++i) {
+          const ulonglong2 qa = *reinterpret_cast<const ulonglong2 *>(sq + i * D + c * 8);
+          const ulonglong2 qb = *reinterpret_cast<const ulonglong2 *>(sq + i * D + c * 8 + 4);
+          s2[i] = ffma2(qa.x, k01, s2[i]);
+          s2[i] = ffma2(qa.y, k23, s2[i]);
+          s2[i] = ffma2(qb.x, k45, s2[i]);
+          s2[i] = ffma2(qb.y, k67, s2[i]);
+        }
+      }
+      const bool valid = t_begin + j * kTok + row < t_end;
+      float s[GH];
+#pragma unroll
+      for (int i = 0; i < GH; ++i) {
+        const float2 v = unf2(s2[i]);
+        float x = v.x + v.y;
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+        s[i] = valid ? x : -INFINITY;
+      }
+      // online softmax over this warp's 16 tokens (both halves hold the same scores)
+      float pr[GH];
+#pragma unroll
+      for (int i = 0; i < GH; ++i) {
+        float mx = s[i];
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new = fmaxf(m[i], mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = fast_exp2(m[i] - m_use);
+        pr[i] = fast_exp2(s[i] - m_use);
+        lpart[i] = lpart[i] * alpha + (half == 0 ? pr[i] : 0.f);
+        const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] = fmul2(acc[i][e], a2);
+        m[i] = m_new;
+      }
+      if (half == 0) {
+#pragma unroll
+        for (int i = 0; i < GH; ++i) pw[tl * GH + i] = pr[i];
+      }
+      __syncwarp();
+      // P . V over the warp's 16 tokens
+#pragma unroll
+      for (int it = 0; it < kTokPerWarp / C::TPI; ++it) {
+        const int t = it * C::TPI + slot;
+        const int r2 = warp * kTokPerWarp + t;
+        const uint4 vw = *reinterpret_cast<const uint4 *>(sv + swz(r2, sub));
+        const uint64_t v01 = widen2<BF16>(vw.x), v23 = widen2<BF16>(vw.y);
+        const uint64_t v45 = widen2<BF16>(vw.z), v67 = widen2<BF16>(vw.w);
+#pragma unroll
+        for (int i = 0; i < GH; ++i) {
+          const float pv = pw[t * GH + i];
+          const uint64_t p2 = f2(pv, pv);
+          acc[i][0] = ffma2(p2, v01, acc[i][0]);
+          acc[i][1] = ffma2(p2, v23, acc[i][1]);
+          acc[i][2] = ffma2(p2, v45, acc[i][2]);
+          acc[i][3] = ffma2(p2, v67, acc[i][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(EMPTY(st));
+    }
+    // per-warp sum of the partial row sums
+#pragma unroll
+    for (int i = 0; i < GH; ++i) {
+      float x = lpart[i];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      lpart[i] = x;
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < GH; ++i) {
+        sm_m[warp * GH + i] = ok ? m[i] : -INFINITY;
+        sm_l[warp * GH + i] = ok ? lpart[i] : 0.f;
+      }
+    }
+    // Every stage this CTA loaded has been consumed, so the ring is idle; wait
+    // for all consumers to be past it before reusing it for the merge.
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+    float *mg = reinterpret_cast<float *>(smem);  // [warps][TPI][GH][D]
+#pragma unroll
+    for (int i = 0; i < GH; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 v = unf2(acc[i][e]);
+        float *dst = mg + ((warp * C::TPI + slot) * GH + i) * D + sub * 8 + 2 * e;
+        dst[0] = v.x;
+        dst[1] = v.y;
+      }
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+    for (int idx = threadIdx.x; idx < nh * D; idx += kConsumerWarps * 32) {
+      const int i = idx / D, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * GH + i]);
+      const float M_use = (M == -INFINITY) ? 0.f : M;
+      float L = 0.f, A = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float wt = fast_exp2(sm_m[w * GH + i] - M_use);
+        L = fmaf(sm_l[w * GH + i], wt, L);
+        float a = 0.f;
+#pragma unroll
+        for (int sl = 0; sl < C::TPI; ++sl) a += mg[((w * C::TPI + sl) * GH + i) * D + d];
+        A = fmaf(a, wt, A);
+      }
+      const int hq = h_first + i;
+      const float o = (L > 0.f) ? A / L : 0.f;
+      const float lse = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
+      if (p.nsplit == 1) {
+        store_out<BF16>(p.o, static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(hq) * p.o_sh + d, o);
+        if (d == 0 && p.lse != nullptr) p.lse[static_cast<int64_t>(b) * p.Hq + hq] = lse;
+      } else {
+        const int64_t r = (static_cast<int64_t>(b) * p.Hq + hq) * p.nsplit + split;
+        p.ws_o[r * D + d] = o;
+        if (d == 0) p.ws_lse[r] = lse;
+      }
     }
   }
 }
@@ -257,6 +358,7 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int d = threadIdx.x;
+  if (load_volatile(p.err) != 0) return;
   const float *ls = p.ws_lse + static_cast<int64_t>(bh) * p.nsplit;
   const float *os = p.ws_o + static_cast<int64_t>(bh) * p.nsplit * D;
   float M = -INFINITY;
@@ -301,10 +403,16 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(const KvWriteParams
 }
 
 template <int D, int GH, bool BF16>
-cudaError_t launch_split(const DecodeParams &p, int B, int Hkv, cudaStream_t stream) {
+cudaError_t launch_split(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int B, int Hkv,
+                         cudaStream_t stream) {
+  using C = DecCfg<D, GH>;
+  auto kern = decode_split_kernel<D, GH, BF16>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES));
+  if (e != cudaSuccess) return e;
   dim3 grid(p.nsplit, Hkv * p.nhc, B);
-  decode_split_kernel<D, GH, BF16><<<grid, kThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tk, tv, p);
+  e = cudaGetLastError();
   if (e != cudaSuccess || p.nsplit == 1) return e;
   decode_merge_kernel<D, BF16><<<B * p.Hq, D, 0, stream>>>(p);
   return cudaGetLastError();
@@ -319,11 +427,10 @@ int decode_heads_per_cta(int group) {
   return 8;
 }
 
-int decode_tokens_per_step(int D) { return kWarps * (32 / (D / 8)) * kU; }  // a multiple of every U
-
-cudaError_t launch_decode(int D, bool bf16, int gh, const DecodeParams &p, int B, int Hkv, cudaStream_t stream) {
+cudaError_t launch_decode(int D, bool bf16, int gh, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const DecodeParams &p, int B, int Hkv, cudaStream_t stream) {
 #define ATTN_DECODE_CASE(DD, GG, BB) \
-  if (D == DD && gh == GG && bf16 == BB) return launch_split<DD, GG, BB>(p, B, Hkv, stream);
+  if (D == DD && gh == GG && bf16 == BB) return launch_split<DD, GG, BB>(tk, tv, p, B, Hkv, stream);
 #define ATTN_DECODE_GH(DD, BB) \
   ATTN_DECODE_CASE(DD, 1, BB) ATTN_DECODE_CASE(DD, 2, BB) ATTN_DECODE_CASE(DD, 4, BB) ATTN_DECODE_CASE(DD, 8, BB)
   ATTN_DECODE_GH(128, true)

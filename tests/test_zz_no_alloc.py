@@ -64,9 +64,10 @@ def test_noalloc_decode_matches_workspace_decode_twice(A):
 
 
 def test_noalloc_decode_rejects_scratch_beyond_limit(A):
-    # B=75, H_q=64, H_kv=8 splits each kv head in two on a 152-SM GB300, which
-    # needs 4 * 75 * 64 * 2 * 129 bytes (4.95 MB) of partials: more than 4 MiB.
-    B, Hq, Hkv, D, L = 75, 64, 8, 128, 8192
+    # B=64, H_q=32, H_kv=8 at cache_len 8192 splits each kv head in four on a
+    # 152-SM GB300, which needs 4 * 64 * 32 * 4 * 129 bytes (4.2 MB) of
+    # partials: more than the 4 MiB array.
+    B, Hq, Hkv, D, L = 64, 32, 8, 128, 8192
     splits = A.attn_decode_splits(B, Hq, Hkv, L, D)
     need = 4 * B * Hq * splits * (D + 1) if splits > 1 else 0
     if need <= (4 << 20):
