@@ -220,7 +220,7 @@ attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void
   p.Nkv = N_kv;
   p.Hq = H_q;
   p.group = H_q / H_kv;
-  p.n_qtiles = (N_q + kPrefillBM - 1) / kPrefillBM;
+  p.n_qtiles = (N_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   cudaError_t e = launch_prefill(D, causal != 0, bf16, tq, tk, tv, p, B, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

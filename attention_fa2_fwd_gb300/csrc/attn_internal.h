@@ -23,7 +23,7 @@ struct PrefillParams {
   float *lse;               // may be null
   unsigned *err;            // device error word
   int64_t o_sb, o_sh, o_sn; // output element strides (d stride is 1)
-  int Nq, Nkv, Hq, group, n_qtiles;
+  int Nq, Nkv, Hq, group, n_qtiles;  // n_qtiles: CTAs along N_q (each covers 2 x 128 rows)
   float scale_log2;         // scale * log2(e): scores are kept in base-2 units
   // Tensor-map coordinate slot (1..3) of the n, h and b coordinates for the
   // Q, K and V maps, packed as n | h << 2 | b << 4 (slot 0 is always d).
@@ -58,7 +58,6 @@ struct KvWriteParams {
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_prefill(int D, bool causal, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                            const CUtensorMap &tv, const PrefillParams &p, int B, cudaStream_t stream);
-size_t prefill_smem_bytes(int D);
 
 // Decode: heads served by one CTA, and launch (split kernel, plus the merge
 // kernel when nsplit > 1).

@@ -1,28 +1,37 @@
 // prefill.cu -- fused attention forward (prefill) for sm_103a.
 //
-// One CTA computes one 128-row query tile of one (batch, q-head):
-//   warp 0      TMA producer: Q tile once, then K and V tiles of 128 keys into
-//               a ring of shared-memory stages (128-byte swizzled).
-//   warp 1      TMEM allocator and tcgen05 MMA issuer (one thread):
-//                 S_j  = Q K_j^T        (SS form, fp32 in TMEM, double-buffered)
-//                 O   += P_j V_j        (TS form, P read from TMEM)
-//   warps 2..5  softmax warpgroup, one thread per query row (TMEM lane):
-//               mask, row max, online-softmax update, P = exp2(S - m) packed
-//               to 16-bit into TMEM, rescale of O by alpha, final O / l and LSE.
+// One CTA computes TWO 128-row query tiles (rows q0..q0+255) of one
+// (batch, q-head), so the tensor core always has one tile's matrix products
+// to run while the other tile's softmax is computed:
+//   warps 0-3   softmax warpgroup of tile 0, one thread per query row (TMEM lane)
+//   warps 4-7   softmax warpgroup of tile 1
+//   warp 8      TMA producer: both Q tiles once, then K and V tiles of 128 keys
+//               into a ring of shared-memory stages (128-byte swizzle)
+//   warp 9      TMEM allocator and tcgen05 MMA issuer (one thread), per KV tile j:
+//                 S0_j = Q0 K_j^T;  O1 += P1_{j-1} V_{j-1};  S1_j = Q1 K_j^T;  O0 += P0_j V_j
+//               (SS form for Q K^T, TS form with P read from TMEM for P V)
+//   warps 10-11 idle (they complete the register split of their warpgroup)
 //
 // The algorithm is the online softmax of "Skill: Write a Triton Attention
 // Kernel" (Required reasoning process, steps 4-9): running max m and sum l in
-// fp32, alpha = exp(m_old - m_new) applied to O and l before the new block is
-// added, O / l once after the loop, lse = m + ln l.  Scores are kept in base-2
-// units (scale * log2 e folded into one multiply) so exp becomes ex2; the LSE
-// is converted back to natural log on store.  The causal mask (key j kept for
-// query i iff j <= i) and the key-length mask set scores to -inf before the
-// max, and only tiles that straddle the diagonal or the end of the keys pay
-// for it; tiles past the diagonal are never loaded (loop bound
-// min(N_kv, q0 + 128)).
+// fp32, O and l rescaled by alpha = exp(m_old - m_new) before a block is
+// added, O / l once after the loop, lse = m + ln l.  Details of this kernel:
+//   * scores are kept in base-2 units (scale * log2 e folded into one FMA), so
+//     the exponential is one ex2; the LSE is converted back on store;
+//   * the running max of a row is only raised when the block max exceeds it
+//     by more than 8 (base 2).  P = 2^(s - m) then stays below 2^8, the rescale
+//     of O (TMEM load, multiply, store) is skipped for most blocks, and O / l is
+//     unchanged because O and l always share the same m;
+//   * the causal mask (key j kept for query i iff j <= i) and the key-length
+//     mask set scores to -inf before the max; only tiles that straddle the
+//     diagonal or the end of the keys pay for it, and KV tiles past the
+//     diagonal of a query tile are never computed for it;
+//   * P (16-bit) overwrites the first half of its S columns in TMEM; in-order
+//     execution of the MMAs keeps the next S from landing before P V has read P,
+//     and makes P_i(j-1) V_{j-1} complete before S_i(j) is signalled, so the
+//     softmax warpgroup may rescale O_i as soon as it sees S_i(j).
 //
-// TMEM columns (512 allocated): S0 [0,128) S1 [128,256) O [256,256+D)
-// P0 [256+D, 320+D) P1 [320+D, 384+D).
+// TMEM columns (512): S0/P0 [0,128) S1/P1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -32,24 +41,28 @@
 namespace attn {
 namespace {
 
-constexpr int kBM = kPrefillBM;
-constexpr int kBN = kPrefillBN;
-constexpr int kThreads = 192;
+constexpr int kBM = kPrefillBM;  // rows per query tile
+constexpr int kBN = kPrefillBN;  // keys per KV tile
+constexpr int kThreads = 384;
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleThreshold = 8.0f;  // base-2 units
+constexpr int kSoftmaxRegs = 208;
+constexpr int kOtherRegs = 72;
 
 template <int D>
 struct Cfg {
   static constexpr int KCH = D / 64;                  // 128-byte chunks along D
   static constexpr int ST = (D == 128) ? 2 : 3;       // K/V pipeline stages
-  static constexpr uint32_t CHUNK_Q = kBM * 128;      // bytes of one 64-column chunk of Q
+  static constexpr uint32_t CHUNK_Q = kBM * 128;      // bytes of one 64-column chunk of a Q tile
   static constexpr uint32_t CHUNK_KV = kBN * 128;
-  static constexpr uint32_t Q_BYTES = kBM * D * 2;
+  static constexpr uint32_t QT_BYTES = kBM * D * 2;   // one Q tile
   static constexpr uint32_t KV_BYTES = kBN * D * 2;
-  static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL = 256;
-  static constexpr uint32_t P_COL0 = 256 + D, P_COL1 = 256 + D + kBN / 2;
+  // TMEM column of S_t / P_t and of O_t for query tile t
+  static __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(t) * 128u; }
+  static __device__ __forceinline__ uint32_t o_col(int t) { return 256u + static_cast<uint32_t>(t) * D; }
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * QT_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + ST * KV_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_V + ST * KV_BYTES;
   // barrier indices
@@ -58,17 +71,18 @@ struct Cfg {
   static constexpr int B_KE = 1 + ST;       // + stage
   static constexpr int B_VF = 1 + 2 * ST;   // + stage
   static constexpr int B_VE = 1 + 3 * ST;   // + stage
-  static constexpr int B_SF = 1 + 4 * ST;   // + buffer (2)
-  static constexpr int B_PF = 3 + 4 * ST;   // + buffer (2)
-  static constexpr int B_OR = 5 + 4 * ST;   // O += P V completed
-  static constexpr int B_DONE = 6 + 4 * ST; // every MMA completed
-  static constexpr int NBAR = 7 + 4 * ST;
+  static constexpr int B_SF = 1 + 4 * ST;   // + tile (2): S_i(j) computed
+  static constexpr int B_PF = 3 + 4 * ST;   // + tile (2): P_i(j) stored (and O_i rescaled)
+  static constexpr int B_OD = 5 + 4 * ST;   // + tile (2): last P_i V done
+  static constexpr int B_DONE = 7 + 4 * ST; // every MMA completed
+  static constexpr int NBAR = 8 + 4 * ST;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
   // + slack for 1024-byte alignment; at least 116 KB so that only one CTA (which
   // holds all 512 TMEM columns) is resident per SM.
   static constexpr uint32_t SMEM_BYTES = (SMEM_USED + 1024 > 116u * 1024) ? SMEM_USED + 1024 : 116u * 1024;
-  static_assert(P_COL1 + kBN / 2 <= TMEM_COLS, "TMEM budget");
+  static_assert(256 + 2 * D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 227u * 1024, "shared memory budget");
 };
 
 __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, int d, int n, int h, int b,
@@ -91,6 +105,15 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -111,12 +134,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int pair = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
   const int h = blockIdx.y, b = blockIdx.z;
   const int hk = h / p.group;
-  const int q0 = qt * kBM;
-  const int kv_end = CAUSAL ? min(p.Nkv, q0 + kBM) : p.Nkv;
-  const int n_kv = (kv_end + kBN - 1) / kBN;
+  const int q0 = pair * 2 * kBM;  // first row of tile 0; tile 1 starts at q0 + 128
+  const int nkv_all = (p.Nkv + kBN - 1) / kBN;
+  // KV tiles needed by each query tile (causal: up to and including its diagonal tile)
+  const int n_kv0 = CAUSAL ? min(nkv_all, (q0 + kBM + kBN - 1) / kBN) : nkv_all;
+  const int n_kv1 = CAUSAL ? min(nkv_all, (q0 + 2 * kBM + kBN - 1) / kBN) : nkv_all;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_Q), 1);
@@ -129,18 +154,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(C::B_SF + i), 1);
       mbar_init(BAR(C::B_PF + i), 4);  // one arrival per softmax warp
+      mbar_init(BAR(C::B_OD + i), 1);
     }
-    mbar_init(BAR(C::B_OR), 1);
     mbar_init(BAR(C::B_DONE), 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -150,106 +175,140 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int issued_k = 0, issued_v = 0;
-      bool ok = true;
-      mbar_arrive_expect_tx(BAR(C::B_Q), C::Q_BYTES);
+  if (warp >= 8) {
+    setmaxnreg_dec<kOtherRegs>();
+    if (warp == 8) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        int issued_k = 0, issued_v = 0;
+        bool ok = true;
+        mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QT_BYTES);
 #pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        tma_tile(sQ + c * C::CHUNK_Q, &tmQ, c * 64, q0, h, b, p.slots_q, BAR(C::B_Q));
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % ST;
-        const uint32_t ph = (j / ST) & 1;
-        if (j >= ST && !(ok = mbar_wait(BAR(C::B_KE + st), ph ^ 1, abort_flag, p.err))) break;
-        mbar_arrive_expect_tx(BAR(C::B_KF + st), C::KV_BYTES);
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_tile(sK + st * C::KV_BYTES + c * C::CHUNK_KV, &tmK, c * 64, j * kBN, hk, b, p.slots_k,
-                   BAR(C::B_KF + st));
-        ++issued_k;
-        if (j >= ST && !(ok = mbar_wait(BAR(C::B_VE + st), ph ^ 1, abort_flag, p.err))) break;
-        mbar_arrive_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_tile(sQ + t * C::QT_BYTES + c * C::CHUNK_Q, &tmQ, c * 64, q0 + t * kBM, h, b, p.slots_q,
+                     BAR(C::B_Q));
+        for (int j = 0; j < n_kv1; ++j) {
+          const int st = j % ST;
+          const uint32_t ph = (j / ST) & 1;
+          if (j >= ST && !(ok = mbar_wait(BAR(C::B_KE + st), ph ^ 1, abort_flag, p.err))) break;
+          mbar_arrive_expect_tx(BAR(C::B_KF + st), C::KV_BYTES);
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_tile(sV + st * C::KV_BYTES + c * C::CHUNK_KV, &tmV, c * 64, j * kBN, hk, b, p.slots_v,
-                   BAR(C::B_VF + st));
-        ++issued_v;
-      }
-      if (!ok) {
-        // Let every copy already issued land before shared memory is released.
-        mbar_wait(BAR(C::B_Q), 0, nullptr, p.err);
-        for (int i = max(0, issued_k - ST); i < issued_k; ++i)
-          mbar_wait(BAR(C::B_KF + i % ST), (i / ST) & 1, nullptr, p.err);
-        for (int i = max(0, issued_v - ST); i < issued_v; ++i)
-          mbar_wait(BAR(C::B_VF + i % ST), (i / ST) & 1, nullptr, p.err);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f16(BF16, kBM, kBN, false, false);
-      constexpr uint32_t idesc_pv = idesc_f16(BF16, kBM, D, false, true);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i % ST;
-        const int pb = i & 1;
-        if (!mbar_wait(BAR(C::B_PF + pb), (i >> 1) & 1, abort_flag, p.err)) return false;
-        if (!mbar_wait(BAR(C::B_VF + st), (i / ST) & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
-        const uint32_t vbase = sV + st * C::KV_BYTES;
-        const uint32_t pcol = tmem + (pb ? C::P_COL1 : C::P_COL0);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_tile(sK + st * C::KV_BYTES + c * C::CHUNK_KV, &tmK, c * 64, j * kBN, hk, b, p.slots_k,
+                     BAR(C::B_KF + st));
+          ++issued_k;
+          if (j >= ST && !(ok = mbar_wait(BAR(C::B_VE + st), ph ^ 1, abort_flag, p.err))) break;
+          mbar_arrive_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // V is MN-major: 16 keys per MMA = 16 rows of 128 B; D in 64-column blocks CHUNK_KV apart.
-          const uint64_t bdesc = smem_desc_sw128(vbase + kk * 16 * 128, C::CHUNK_KV, 1024);
-          mma_ts(tmem + C::O_COL, pcol + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_tile(sV + st * C::KV_BYTES + c * C::CHUNK_KV, &tmV, c * 64, j * kBN, hk, b, p.slots_v,
+                     BAR(C::B_VF + st));
+          ++issued_v;
         }
-        tc_commit(BAR(C::B_VE + st));
-        tc_commit(BAR(C::B_OR));
-        return true;
-      };
-      bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, p.err);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % ST;
-        const int sb = j & 1;
-        if (!(ok = mbar_wait(BAR(C::B_KF + st), (j / ST) & 1, abort_flag, p.err))) break;
-        tc_fence_after();
-        const uint32_t kbase = sK + st * C::KV_BYTES;
-        const uint32_t scol = tmem + (sb ? C::S_COL1 : C::S_COL0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // Q and K are K-major: 16 elements (32 B) per MMA inside a 128-byte swizzle row.
-          const uint64_t adesc = smem_desc_sw128(sQ + (kk / 4) * C::CHUNK_Q + (kk % 4) * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(kbase + (kk / 4) * C::CHUNK_KV + (kk % 4) * 32, 16, 1024);
-          mma_ss(scol, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+        if (!ok) {
+          // Let every copy already issued land before shared memory is released.
+          mbar_wait(BAR(C::B_Q), 0, nullptr, p.err);
+          for (int i = max(0, issued_k - ST); i < issued_k; ++i)
+            mbar_wait(BAR(C::B_KF + i % ST), (i / ST) & 1, nullptr, p.err);
+          for (int i = max(0, issued_v - ST); i < issued_v; ++i)
+            mbar_wait(BAR(C::B_VF + i % ST), (i / ST) & 1, nullptr, p.err);
         }
-        tc_commit(BAR(C::B_SF + sb));
-        tc_commit(BAR(C::B_KE + st));
-        if (j > 0) ok = issue_pv(j - 1);
       }
-      if (ok) issue_pv(n_kv - 1);
-      tc_commit(BAR(C::B_DONE));
-      mbar_wait(BAR(C::B_DONE), 0, nullptr, p.err);
+      __syncwarp();
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = idesc_f16(BF16, kBM, kBN, false, false);
+        constexpr uint32_t idesc_pv = idesc_f16(BF16, kBM, D, false, true);
+        auto issue_s = [&](int t, uint32_t kbase) {
+          const uint32_t qbase = sQ + t * C::QT_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // Q and K are K-major: 16 elements (32 B) per MMA inside a 128-byte swizzle row.
+            const uint64_t adesc = smem_desc_sw128(qbase + (kk / 4) * C::CHUNK_Q + (kk % 4) * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(kbase + (kk / 4) * C::CHUNK_KV + (kk % 4) * 32, 16, 1024);
+            mma_ss(tmem + C::s_col(t), adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(BAR(C::B_SF + t));
+        };
+        auto issue_pv = [&](int t, int j, uint32_t vbase) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            // V is MN-major: 16 keys per MMA = 16 rows of 128 B; D in 64-column blocks CHUNK_KV apart.
+            const uint64_t bdesc = smem_desc_sw128(vbase + kk * 16 * 128, C::CHUNK_KV, 1024);
+            mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+        };
+        bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, p.err);
+        bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
+        for (int j = 0; ok && j < n_kv1; ++j) {
+          const int st = j % ST;
+          const uint32_t ph = (j / ST) & 1;
+          if (!(ok = mbar_wait(BAR(C::B_KF + st), ph, abort_flag, p.err))) break;
+          tc_fence_after();
+          const uint32_t kbase = sK + st * C::KV_BYTES;
+          if (j < n_kv0) issue_s(0, kbase);
+          if (j > 0) {
+            // O1 += P1_{j-1} V_{j-1}
+            const int sp = (j - 1) % ST;
+            if (!(ok = mbar_wait(BAR(C::B_PF + 1), (j - 1) & 1, abort_flag, p.err))) break;
+            if (!v_waited && !(ok = mbar_wait(BAR(C::B_VF + sp), ((j - 1) / ST) & 1, abort_flag, p.err))) break;
+            tc_fence_after();
+            issue_pv(1, j - 1, sV + sp * C::KV_BYTES);
+            tc_commit(BAR(C::B_VE + sp));
+          }
+          issue_s(1, kbase);
+          tc_commit(BAR(C::B_KE + st));
+          v_waited = false;
+          if (j < n_kv0) {
+            // O0 += P0_j V_j
+            if (!(ok = mbar_wait(BAR(C::B_PF + 0), j & 1, abort_flag, p.err))) break;
+            if (!(ok = mbar_wait(BAR(C::B_VF + st), ph, abort_flag, p.err))) break;
+            v_waited = true;
+            tc_fence_after();
+            issue_pv(0, j, sV + st * C::KV_BYTES);
+            if (j == n_kv0 - 1) tc_commit(BAR(C::B_OD + 0));
+          }
+        }
+        if (ok) {
+          const int jl = n_kv1 - 1;
+          const int sp = jl % ST;
+          ok = mbar_wait(BAR(C::B_PF + 1), jl & 1, abort_flag, p.err) &&
+               (v_waited || mbar_wait(BAR(C::B_VF + sp), (jl / ST) & 1, abort_flag, p.err));
+          if (ok) {
+            tc_fence_after();
+            issue_pv(1, jl, sV + sp * C::KV_BYTES);
+            tc_commit(BAR(C::B_VE + sp));
+            tc_commit(BAR(C::B_OD + 1));
+          }
+        }
+        tc_commit(BAR(C::B_DONE));
+        mbar_wait(BAR(C::B_DONE), 0, nullptr, p.err);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warpgroup
+    // ------------------------------------------------------------ softmax warpgroups
+    setmaxnreg_inc<kSoftmaxRegs>();
+    const int t = warp >> 2;                            // query tile of this warpgroup
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;                 // query row in the tile == TMEM lane
+    const int r = quarter * 32 + lane;                  // row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int q_row = q0 + r;
+    const int q_tile0 = q0 + t * kBM;
+    const int q_row = q_tile0 + r;
+    const int n_kv = t ? n_kv1 : n_kv0;
     const float sl2 = p.scale_log2;
+    const uint32_t scol = tmem + lane_off + C::s_col(t);
+    const uint32_t ocol = tmem + lane_off + C::o_col(t);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF + sb), (j >> 1) & 1, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF + t), j & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
-      const uint32_t scol = tmem + lane_off + (sb ? C::S_COL1 : C::S_COL0);
 #pragma unroll
       for (int i = 0; i < 4; ++i) tmem_ld_32x32b_x32(scol + i * 32, sr[i]);
       tmem_wait_ld();
@@ -257,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 4; ++i) reg_fence(sr[i]);
 
       const int kv0 = j * kBN;
-      const bool need_mask = (kv0 + kBN > p.Nkv) || (CAUSAL && kv0 + kBN - 1 > q0);
+      const bool need_mask = (kv0 + kBN > p.Nkv) || (CAUSAL && kv0 + kBN - 1 > q_tile0);
       float mx = -INFINITY;
       if (need_mask) {
         const int lim = (CAUSAL ? min(p.Nkv, q_row + 1) : p.Nkv) - kv0;  // columns c < lim are kept
@@ -276,9 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sr[i][c]));
       }
-      const float m_new = fmaxf(m, mx * sl2);
+      // Raise the running max only when the block max exceeds it by more than
+      // the threshold; otherwise keep it (alpha = 1, no rescale of O).
+      const float mb = mx * sl2;
+      const bool raise = (m == -INFINITY) || (mb > m + kRescaleThreshold);
+      const float m_new = raise ? fmaxf(m, mb) : m;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = fast_exp2(m - m_use);
+      const float alpha = raise ? fast_exp2(m - m_use) : 1.f;
       float rs = 0.f;
       uint32_t pk[2][32];
 #pragma unroll
@@ -292,36 +355,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       l = l * alpha + rs;
       m = m_new;
-
-      if (j > 0) {
-        // O += P_{j-1} V_{j-1} must have completed before O is rescaled and before
-        // this P buffer (last read by P_{j-2} V_{j-2}) is overwritten.
-        ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OR), (j - 1) & 1, abort_flag, p.err));
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // P_i(j) over the first 64 columns of S_i (S_i(j) is already in registers).
+      tmem_st_32x32b_x32(scol, pk[0]);
+      tmem_st_32x32b_x32(scol + 32, pk[1]);
+      // P_i(j-1) V_{j-1} completed before S_i(j) was signalled: O_i is stable.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int i = 0; i < D / 32; ++i) {
-            uint32_t ov[32];
-            const uint32_t ocol = tmem + lane_off + C::O_COL + i * 32;
-            tmem_ld_32x32b_x32(ocol, ov);
-            tmem_wait_ld();
-            reg_fence(ov);
+        for (int i = 0; i < D / 32; ++i) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(ocol + i * 32, ov);
+          tmem_wait_ld();
+          reg_fence(ov);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-            tmem_st_32x32b_x32(ocol, ov);
-          }
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st_32x32b_x32(ocol + i * 32, ov);
         }
       }
-      const uint32_t pcol = tmem + lane_off + (sb ? C::P_COL1 : C::P_COL0);
-      tmem_st_32x32b_x32(pcol, pk[0]);
-      tmem_st_32x32b_x32(pcol + 32, pk[1]);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(C::B_PF + sb));
+      if (lane == 0) mbar_arrive(BAR(C::B_PF + t));
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OR), (n_kv - 1) & 1, abort_flag, p.err));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OD + t), 0, abort_flag, p.err));
     if (ok) {
       // -------------------------------------------------------- epilogue: O / l, LSE
       tc_fence_after();
@@ -333,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) {
         uint32_t ov[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + C::O_COL + i * 32, ov);
+        tmem_ld_32x32b_x32(ocol + i * 32, ov);
         tmem_wait_ld();
         reg_fence(ov);
         uint32_t packed[16];
@@ -354,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -365,7 +420,13 @@ cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        int B, cudaStream_t stream) {
   auto kern = prefill_fwd_kernel<D, CAUSAL, BF16>;
   constexpr uint32_t smem = Cfg<D>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  // setmaxnreg redistributes the registers the CTA was launched with; a split
+  // larger than that pool would never be granted, so refuse to launch then.
+  cudaFuncAttributes attr{};
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * kThreads < 256 * kSoftmaxRegs + 128 * kOtherRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_qtiles, p.Hq, B);
   kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
@@ -373,8 +434,6 @@ cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 }
 
 }  // namespace
-
-size_t prefill_smem_bytes(int D) { return D == 128 ? Cfg<128>::SMEM_BYTES : Cfg<64>::SMEM_BYTES; }
 
 cudaError_t launch_prefill(int D, bool causal, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
                            const CUtensorMap &tv, const PrefillParams &p, int B, cudaStream_t stream) {
