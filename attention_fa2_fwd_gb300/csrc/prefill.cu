@@ -317,24 +317,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int kv0 = j * kBN;
       const bool need_mask = (kv0 + kBN > p.Nkv) || (CAUSAL && kv0 + kBN - 1 > q_tile0);
-      float mx = -INFINITY;
       if (need_mask) {
         const int lim = (CAUSAL ? min(p.Nkv, q_row + 1) : p.Nkv) - kv0;  // columns c < lim are kept
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            float x = __uint_as_float(sr[i][c]);
-            x = (i * 32 + c < lim) ? x : -INFINITY;
-            sr[i][c] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
-          }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(sr[i][c]));
+          for (int c = 0; c < 32; ++c)
+            if (i * 32 + c >= lim) sr[i][c] = __float_as_uint(-INFINITY);
       }
+      // Row max: four independent chains of 3-input maxima.
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < 32; c += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mq[u] = fmax3(mq[u], __uint_as_float(sr[i][c + 2 * u]), __uint_as_float(sr[i][c + 2 * u + 1]));
+      const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
       // Raise the running max only when the block max exceeds it by more than
       // the threshold; otherwise keep it (alpha = 1, no rescale of O).
       const float mb = mx * sl2;
@@ -342,17 +342,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = raise ? fmaxf(m, mb) : m;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = raise ? fast_exp2(m - m_use) : 1.f;
-      float rs = 0.f;
+      // P = 2^(s * scale * log2 e - m), two columns per packed FMA; row sum in
+      // four packed partial sums.
+      const uint64_t sl2x2 = pack_f2(sl2, sl2), negm2 = pack_f2(-m_use, -m_use);
+      uint64_t rs2[4] = {0, 0, 0, 0};
       uint32_t pk[2][32];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[i][c]), sl2, -m_use));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[i][c + 1]), sl2, -m_use));
-          rs += p0 + p1;
+          const uint64_t e2 = ffma_f2(pack_f2(__uint_as_float(sr[i][c]), __uint_as_float(sr[i][c + 1])), sl2x2, negm2);
+          const float2 e = unpack_f2(e2);
+          const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+          rs2[(c >> 1) & 3] = fadd_f2(rs2[(c >> 1) & 3], pack_f2(p0, p1));
           pk[i >> 1][(i & 1) * 16 + c / 2] = pack2<BF16>(p0, p1);
         }
+      const float2 r01 = unpack_f2(fadd_f2(rs2[0], rs2[1])), r23 = unpack_f2(fadd_f2(rs2[2], rs2[3]));
+      const float rs = (r01.x + r01.y) + (r23.x + r23.y);
       l = l * alpha + rs;
       m = m_new;
       // P_i(j) over the first 64 columns of S_i (S_i(j) is already in registers).
