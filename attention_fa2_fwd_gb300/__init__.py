@@ -28,14 +28,15 @@ ATTN_ERR_ALIGNMENT = 3
 ATTN_ERR_WORKSPACE = 4
 ATTN_ERR_CUDA = 5
 ATTN_ERR_DEVICE_TIMEOUT = 6
+ATTN_ERR_DEVICE_INDEX = 7
 
 ATTN_F16 = 0
 ATTN_BF16 = 1
 
 # Every function that include/attn.h declares.
 EXPORTS = ("attn_fwd_prefill", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
-           "attn_fwd_decode_noalloc", "kv_cache_write", "attn_get_device_error", "attn_status_string",
-           "attn_version")
+           "attn_fwd_decode_noalloc", "kv_cache_write", "attn_fwd_decode_paged", "kv_cache_write_paged",
+           "attn_get_device_error", "attn_status_string", "attn_version")
 
 
 class AttnLibraryMissing(RuntimeError):
@@ -81,6 +82,14 @@ def lib() -> ctypes.CDLL:
             L.kv_cache_write.restype = i32
             L.kv_cache_write.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                          i64p, i64p, i64p, i64p, vp]
+            i64 = ctypes.c_int64
+            L.attn_fwd_decode_paged.restype = i32
+            L.attn_fwd_decode_paged.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                                vp, i32, i64, vp, i32, i64p, i64p, i64p, i64p, f32, vp,
+                                                ctypes.c_size_t, vp]
+            L.kv_cache_write_paged.restype = i32
+            L.kv_cache_write_paged.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, i64,
+                                               vp, i64p, i64p, i64p, i64p, vp]
             L.attn_get_device_error.restype = i32
             L.attn_get_device_error.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
@@ -136,6 +145,23 @@ def kv_cache_write(k_cache, v_cache, k_new, v_new, dtype, B, H_kv, n_new, D, pos
                    vn_str, stream) -> int:
     return lib().kv_cache_write(k_cache, v_cache, k_new, v_new, dtype, B, H_kv, n_new, D, pos, max_len,
                                 _strides(kc_str), _strides(vc_str), _strides(kn_str), _strides(vn_str), stream)
+
+
+def attn_fwd_decode_paged(q, k_pages, v_pages, o, lse, dtype, B, H_q, H_kv, D, num_pages, page_size, block_table,
+                          max_pages, bt_stride, cache_lens, max_cache_len, q_str, kp_str, vp_str, o_str, scale,
+                          workspace, workspace_bytes, stream) -> int:
+    return lib().attn_fwd_decode_paged(q, k_pages, v_pages, o, lse, dtype, B, H_q, H_kv, D, num_pages, page_size,
+                                       block_table, max_pages, bt_stride, cache_lens, max_cache_len,
+                                       _strides(q_str), _strides(kp_str), _strides(vp_str), _strides(o_str),
+                                       float(scale), workspace, workspace_bytes, stream)
+
+
+def kv_cache_write_paged(k_pages, v_pages, k_new, v_new, dtype, B, H_kv, n_new, D, num_pages, page_size,
+                         block_table, max_pages, bt_stride, positions, kp_str, vp_str, kn_str, vn_str,
+                         stream) -> int:
+    return lib().kv_cache_write_paged(k_pages, v_pages, k_new, v_new, dtype, B, H_kv, n_new, D, num_pages,
+                                      page_size, block_table, max_pages, bt_stride, positions, _strides(kp_str),
+                                      _strides(vp_str), _strides(kn_str), _strides(vn_str), stream)
 
 
 def attn_get_device_error(stream=None) -> int:
@@ -244,6 +270,60 @@ def write_kv_cache(k_cache, v_cache, k_new, v_new, pos: int, stream=None):
                         _dtype_code(k_cache), B, Hkv, n, D, int(pos), max_len, k_cache.stride(), v_cache.stride(),
                         k_new.stride(), v_new.stride(), _stream_handle(stream))
     _check(st, "kv_cache_write")
+
+
+def _int32_cuda(t, name):
+    import torch
+    if t.dtype != torch.int32 or not t.is_cuda:
+        raise TypeError(f"{name} must be an int32 CUDA tensor")
+    return t
+
+
+def decode_paged(q, k_pages, v_pages, block_table, cache_lens, max_cache_len: int, scale: float | None = None,
+                 return_lse: bool = True, out=None, lse_out=None, workspace=None, stream=None):
+    """Decode over paged caches with per-request lengths.
+
+    q (B,H_q,D); k_pages, v_pages (num_pages,H_kv,page_size,D); block_table int32 (B,max_pages) and
+    cache_lens int32 (B) on the device; max_cache_len a host upper bound of cache_lens.
+    Returns (O (B,H_q,D), LSE (B,H_q)).
+    """
+    import torch
+    q4 = q if q.dim() == 4 else q.unsqueeze(2)
+    B, Hq, _, D = q4.shape
+    num_pages, Hkv, page_size, _ = k_pages.shape
+    bt = _int32_cuda(block_table, "block_table")
+    cl = _int32_cuda(cache_lens, "cache_lens")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = out if out is not None else torch.empty((B, Hq, D), dtype=q.dtype, device=q.device)
+    o4 = o.unsqueeze(2) if o.dim() == 3 else o
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, D, q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = attn_fwd_decode_paged(q4.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o4.data_ptr(),
+                               lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, D,
+                               num_pages, page_size, bt.data_ptr(), bt.shape[1], bt.stride(0), cl.data_ptr(),
+                               int(max_cache_len), q4.stride(), k_pages.stride(), v_pages.stride(), o4.stride(),
+                               scale, ws_ptr, ws_bytes, _stream_handle(stream))
+    _check(st, "attn_fwd_decode_paged")
+    return o, lse
+
+
+def write_kv_cache_paged(k_pages, v_pages, k_new, v_new, block_table, positions, stream=None):
+    """Write k_new/v_new (B,H_kv,n,D) at positions[b] + t of each request's paged cache (in place)."""
+    num_pages, Hkv, page_size, D = k_pages.shape
+    B, _, n, _ = k_new.shape
+    bt = _int32_cuda(block_table, "block_table")
+    pos = _int32_cuda(positions, "positions")
+    st = kv_cache_write_paged(k_pages.data_ptr(), v_pages.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                              _dtype_code(k_pages), B, Hkv, n, D, num_pages, page_size, bt.data_ptr(), bt.shape[1],
+                              bt.stride(0), pos.data_ptr(), k_pages.stride(), v_pages.stride(), k_new.stride(),
+                              v_new.stride(), _stream_handle(stream))
+    _check(st, "kv_cache_write_paged")
 
 
 def check_device_error(stream=None):

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "ptx.cuh"
 
 namespace attn {
 namespace {
@@ -305,7 +306,7 @@ attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_
   if ((st = make_map(&tk, k_cache, bf16, csz, kc_str, kDecodeStageTokens, &p.slots_k)) ||
       (st = make_map(&tv, v_cache, bf16, csz, vc_str, kDecodeStageTokens, &p.slots_v)))
     return st;
-  cudaError_t e = launch_decode(D, bf16, gh, tk, tv, p, B, H_kv, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_decode(D, bf16, false, gh, tk, tv, p, B, H_kv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -349,7 +350,141 @@ attn_status_t kv_cache_write(void *k_cache, void *v_cache, const void *k_new, co
   p.D = D;
   p.total_units = static_cast<int64_t>(B) * H_kv * n_new * (D / 8);
   p.err = dev->err;
-  cudaError_t e = launch_kv_cache_write(p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_kv_cache_write(p, false, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Page geometry shared by the paged entry points.
+static attn_status_t check_pages(int num_pages, int page_size, const int32_t *block_table, int max_pages,
+                                 int64_t bt_stride) {
+  if (num_pages < 1 || max_pages < 1 || block_table == nullptr || bt_stride < max_pages) return ATTN_ERR_INVALID_ARG;
+  if (!(page_size == 16 || page_size == 32 || (page_size >= 64 && page_size % 64 == 0))) return ATTN_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3) != 0) return ATTN_ERR_ALIGNMENT;
+  if (static_cast<int64_t>(max_pages) * page_size > INT_MAX) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status_t attn_fwd_decode_paged(const void *q, const void *k_pages, const void *v_pages, void *o, float *lse,
+                                    attn_dtype_t dtype, int B, int H_q, int H_kv, int D, int num_pages,
+                                    int page_size, const int32_t *block_table, int max_pages, int64_t bt_stride,
+                                    const int32_t *cache_lens, int max_cache_len, const int64_t q_str[4],
+                                    const int64_t kp_str[4], const int64_t vp_str[4], const int64_t o_str[4],
+                                    float scale, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!q || !k_pages || !v_pages || !o || !cache_lens || !q_str || !kp_str || !vp_str || !o_str)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H_q < 1 || H_kv < 1 || D < 1 || H_q % H_kv != 0 || max_cache_len < 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f) || B > 65535) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  attn_status_t st;
+  if ((st = check_pages(num_pages, page_size, block_table, max_pages, bt_stride)) != ATTN_OK) return st;
+  if (static_cast<int64_t>(max_cache_len) > static_cast<int64_t>(max_pages) * page_size) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3)) || (reinterpret_cast<uintptr_t>(cache_lens) & 3))
+    return ATTN_ERR_ALIGNMENT;
+  const int64_t qsz[4] = {B, H_q, 1, D}, psz[4] = {num_pages, H_kv, page_size, D};
+  if ((st = check_strides(q_str, qsz)) || (st = check_strides(kp_str, psz)) || (st = check_strides(vp_str, psz)) ||
+      (st = check_strides(o_str, qsz)))
+    return st;
+  const DeviceState *dev = nullptr;
+  if ((st = device_state(&dev)) != ATTN_OK) return st;
+
+  const int group = H_q / H_kv;
+  const int gh = decode_heads_per_cta(group);
+  const int nhc = (group + gh - 1) / gh;
+  int nsplit = 1, chunk = max_cache_len;
+  decode_plan(B, H_q, H_kv, max_cache_len, D, dev->sm_count, &nsplit, &chunk);
+  if (nsplit > 1) {
+    const size_t need = decode_ws_bytes(B, H_q, D, nsplit);
+    if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15) != 0) return ATTN_ERR_ALIGNMENT;
+  }
+  if (static_cast<int64_t>(H_kv) * nhc > 65535) return ATTN_ERR_INVALID_ARG;
+  DecodeParams p{};
+  p.q = q;
+  p.kc = k_pages;
+  p.vc = v_pages;
+  p.o = o;
+  p.lse = lse;
+  p.ws_o = static_cast<float *>(workspace);
+  p.ws_lse = nsplit > 1 ? static_cast<float *>(workspace) + static_cast<size_t>(B) * H_q * nsplit * D : nullptr;
+  p.err = dev->err;
+  p.q_sb = q_str[0];
+  p.q_sh = q_str[1];
+  p.o_sb = o_str[0];
+  p.o_sh = o_str[1];
+  p.Hq = H_q;
+  p.group = group;
+  p.nhc = nhc;
+  p.cache_len = max_cache_len;
+  p.chunk = chunk;
+  p.nsplit = nsplit;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.block_table = block_table;
+  p.cache_lens = cache_lens;
+  p.bt_stride = bt_stride;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  // Tensor maps over the page pool: (d, row in page, kv head, page).
+  CUtensorMap tk, tv;
+  const bool bf16 = dtype == ATTN_BF16;
+  const int rows = page_size < kDecodeStageTokens ? page_size : kDecodeStageTokens;
+  if ((st = make_map(&tk, k_pages, bf16, psz, kp_str, rows, &p.slots_k)) ||
+      (st = make_map(&tv, v_pages, bf16, psz, vp_str, rows, &p.slots_v)))
+    return st;
+  cudaError_t e = launch_decode(D, bf16, true, gh, tk, tv, p, B, H_kv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t kv_cache_write_paged(void *k_pages, void *v_pages, const void *k_new, const void *v_new,
+                                   attn_dtype_t dtype, int B, int H_kv, int n_new, int D, int num_pages,
+                                   int page_size, const int32_t *block_table, int max_pages, int64_t bt_stride,
+                                   const int32_t *positions, const int64_t kp_str[4], const int64_t vp_str[4],
+                                   const int64_t kn_str[4], const int64_t vn_str[4], void *stream) {
+  if (!k_pages || !v_pages || !k_new || !v_new || !positions || !kp_str || !vp_str || !kn_str || !vn_str)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H_kv < 1 || n_new < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  attn_status_t st;
+  if ((st = check_pages(num_pages, page_size, block_table, max_pages, bt_stride)) != ATTN_OK) return st;
+  if (!aligned16(k_pages) || !aligned16(v_pages) || !aligned16(k_new) || !aligned16(v_new) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3))
+    return ATTN_ERR_ALIGNMENT;
+  const int64_t psz[4] = {num_pages, H_kv, page_size, D}, nsz[4] = {B, H_kv, n_new, D};
+  if ((st = check_strides(kp_str, psz)) || (st = check_strides(vp_str, psz)) || (st = check_strides(kn_str, nsz)) ||
+      (st = check_strides(vn_str, nsz)))
+    return st;
+  const DeviceState *dev = nullptr;
+  if ((st = device_state(&dev)) != ATTN_OK) return st;
+  KvWriteParams p{};
+  p.kc = k_pages;
+  p.vc = v_pages;
+  p.kn = k_new;
+  p.vn = v_new;
+  p.kc_sb = kp_str[0];
+  p.kc_sh = kp_str[1];
+  p.kc_sn = kp_str[2];
+  p.vc_sb = vp_str[0];
+  p.vc_sh = vp_str[1];
+  p.vc_sn = vp_str[2];
+  p.kn_sb = kn_str[0];
+  p.kn_sh = kn_str[1];
+  p.kn_sn = kn_str[2];
+  p.vn_sb = vn_str[0];
+  p.vn_sh = vn_str[1];
+  p.vn_sn = vn_str[2];
+  p.Hkv = H_kv;
+  p.n_new = n_new;
+  p.D = D;
+  p.total_units = static_cast<int64_t>(B) * H_kv * n_new * (D / 8);
+  p.err = dev->err;
+  p.block_table = block_table;
+  p.positions = positions;
+  p.bt_stride = bt_stride;
+  p.page_size = page_size;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  cudaError_t e = launch_kv_cache_write(p, true, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -363,7 +498,7 @@ attn_status_t attn_get_device_error(void *stream) {
   if (word == 0) return ATTN_OK;
   const unsigned zero = 0;
   if (cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
-  return ATTN_ERR_DEVICE_TIMEOUT;
+  return (word & kErrWaitTimeout) ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_ERR_DEVICE_INDEX;
 }
 
 const char *attn_status_string(attn_status_t status) {
@@ -375,6 +510,7 @@ const char *attn_status_string(attn_status_t status) {
     case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+    case ATTN_ERR_DEVICE_INDEX: return "ATTN_ERR_DEVICE_INDEX";
   }
   return "ATTN_ERR_UNKNOWN";
 }

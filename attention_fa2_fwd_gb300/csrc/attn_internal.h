@@ -43,6 +43,11 @@ struct DecodeParams {
   int Hq, group, nhc, cache_len, chunk, nsplit;
   float scale_log2;
   uint32_t slots_k, slots_v;  // tensor-map coordinate slots, as for prefill
+  // Paged caches only (cache_len then is the host's upper bound of the lengths):
+  const int32_t *block_table;  // (B, max_pages) page ids, row stride bt_stride
+  const int32_t *cache_lens;   // (B) tokens per request
+  int64_t bt_stride;
+  int page_size, max_pages, num_pages;
 };
 
 struct KvWriteParams {
@@ -53,6 +58,12 @@ struct KvWriteParams {
   int Hkv, n_new, pos, D;
   int64_t total_units;      // B * H_kv * n_new * (D / 8) 16-byte pieces per tensor
   unsigned *err;
+  // Paged caches only: kc/vc are page pools (num_pages, H_kv, page_size, D);
+  // token t of request b goes to position positions[b] + t.
+  const int32_t *block_table;
+  const int32_t *positions;
+  int64_t bt_stride;
+  int page_size, max_pages, num_pages;
 };
 
 // Launchers (return cudaSuccess or the launch error).
@@ -62,9 +73,9 @@ cudaError_t launch_prefill(int D, bool causal, bool bf16, const CUtensorMap &tq,
 // Decode: heads served by one CTA, and launch (split kernel, plus the merge
 // kernel when nsplit > 1).
 int decode_heads_per_cta(int group);
-cudaError_t launch_decode(int D, bool bf16, int heads_per_cta, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const DecodeParams &p, int B, int Hkv, cudaStream_t stream);
+cudaError_t launch_decode(int D, bool bf16, bool paged, int heads_per_cta, const CUtensorMap &tk,
+                          const CUtensorMap &tv, const DecodeParams &p, int B, int Hkv, cudaStream_t stream);
 
-cudaError_t launch_kv_cache_write(const KvWriteParams &p, cudaStream_t stream);
+cudaError_t launch_kv_cache_write(const KvWriteParams &p, bool paged, cudaStream_t stream);
 
 }  // namespace attn

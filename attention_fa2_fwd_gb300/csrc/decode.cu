@@ -117,7 +117,11 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, i
   tma_load_4d(dst, map, d, c1, c2, c3, bar);
 }
 
-template <int D, int GH, bool BF16>
+// PAGED: the cache is a pool of pages (num_pages, H_kv, page_size, D); request
+// b's tokens sit in the pages listed by block_table[b] and its length is
+// cache_lens[b].  A stage is loaded as 64 / min(page_size, 64) boxes, one per
+// page it touches, and only for rows below the request's length.
+template <int D, int GH, bool BF16, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeParams p) {
@@ -143,9 +147,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h_first = hk * p.group + hc * GH;
   const int nh = min(GH, p.group - hc * GH);
+  int len = p.cache_len;
+  if constexpr (PAGED) {
+    len = p.cache_lens[b];
+    if (len < 0 || len > p.cache_len) {
+      if (threadIdx.x == 0) atomicOr(p.err, kErrBadIndex);
+      len = len < 0 ? 0 : p.cache_len;
+    }
+  }
   const int t_begin = split * p.chunk;
-  const int t_end = min(t_begin + p.chunk, p.cache_len);
-  const int n_tiles = (t_end - t_begin + kTok - 1) / kTok;
+  const int t_end = min(t_begin + p.chunk, len);
+  const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTok - 1) / kTok : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -181,11 +193,36 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (j >= kStages && !(ok = mbar_wait(EMPTY(st), ((j / kStages) - 1) & 1, abort_flag, p.err))) break;
         const uint32_t dst = sbase + st * C::STAGE_BYTES;
         const int t0 = t_begin + j * kTok;
-        mbar_arrive_expect_tx(FULL(st), C::STAGE_BYTES);
+        if constexpr (!PAGED) {
+          mbar_arrive_expect_tx(FULL(st), C::STAGE_BYTES);
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_tile(dst + c * C::BOX_BYTES, &tmK, c * 64, t0, hk, b, p.slots_k, FULL(st));
-          tma_tile(dst + C::KV_BYTES + c * C::BOX_BYTES, &tmV, c * 64, t0, hk, b, p.slots_v, FULL(st));
+          for (int c = 0; c < C::KCH; ++c) {
+            tma_tile(dst + c * C::BOX_BYTES, &tmK, c * 64, t0, hk, b, p.slots_k, FULL(st));
+            tma_tile(dst + C::KV_BYTES + c * C::BOX_BYTES, &tmV, c * 64, t0, hk, b, p.slots_v, FULL(st));
+          }
+        } else {
+          // Boxes of `rows` tokens, each inside one page; rows past the length
+          // are not loaded (the consumers mask them), so the stage expects only
+          // the bytes of the boxes issued.
+          const int rows = p.page_size < kTok ? p.page_size : kTok;
+          const int nbox = (min(t_end - t0, kTok) + rows - 1) / rows;
+          mbar_arrive_expect_tx(FULL(st), static_cast<uint32_t>(nbox * rows) * (2u * D * 2u));
+          for (int x = 0; x < nbox; ++x) {
+            const int tok = t0 + x * rows;
+            const int pidx = tok / p.page_size;
+            int page = (pidx < p.max_pages) ? p.block_table[static_cast<int64_t>(b) * p.bt_stride + pidx] : -1;
+            if (page < 0 || page >= p.num_pages) {
+              atomicOr(p.err, kErrBadIndex);
+              page = p.num_pages;  // out of the tensor map: the box reads as zeros
+            }
+            const int row = tok % p.page_size;
+            const uint32_t off = static_cast<uint32_t>(x * rows * 128);
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c) {
+              tma_tile(dst + c * C::BOX_BYTES + off, &tmK, c * 64, row, hk, page, p.slots_k, FULL(st));
+              tma_tile(dst + C::KV_BYTES + c * C::BOX_BYTES + off, &tmV, c * 64, row, hk, page, p.slots_v, FULL(st));
+            }
+          }
         }
         ++issued;
       }
@@ -277,7 +314,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int it = 0; it < kTokPerWarp / C::TPI; ++it) {
         const int t = it * C::TPI + slot;
         const int r2 = warp * kTokPerWarp + t;
-        const uint4 vw = *reinterpret_cast<const uint4 *>(sv + swz(r2, sub));
+        uint4 vw = *reinterpret_cast<const uint4 *>(sv + swz(r2, sub));
+        if constexpr (PAGED) {
+          // Rows past the length were not loaded: keep stale bytes out of P V.
+          if (t_begin + j * kTok + r2 >= t_end) vw = make_uint4(0, 0, 0, 0);
+        }
         const uint64_t v01 = widen2<BF16>(vw.x), v23 = widen2<BF16>(vw.y);
         const uint64_t v45 = widen2<BF16>(vw.z), v67 = widen2<BF16>(vw.w);
 #pragma unroll
@@ -402,11 +443,48 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(const KvWriteParams
   }
 }
 
-template <int D, int GH, bool BF16>
+// Paged cache write: token t of request b goes to position positions[b] + t,
+// i.e. row (pos % page_size) of page block_table[b][pos / page_size].  A page
+// id or position out of range skips the write and records kErrBadIndex.
+__global__ void __launch_bounds__(256) kv_cache_write_paged_kernel(const KvWriteParams p) {
+  if (load_volatile(p.err) != 0) return;
+  const int pieces = p.D / 8;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < 2 * p.total_units;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool is_v = u >= p.total_units;
+    int64_t x = is_v ? u - p.total_units : u;
+    const int e = static_cast<int>(x % pieces) * 8;
+    x /= pieces;
+    const int t = static_cast<int>(x % p.n_new);
+    x /= p.n_new;
+    const int hk = static_cast<int>(x % p.Hkv);
+    const int64_t b = x / p.Hkv;
+    const int pos = p.positions[b] + t;
+    const int pidx = pos >= 0 ? pos / p.page_size : -1;
+    const int page = (pidx >= 0 && pidx < p.max_pages) ? p.block_table[b * p.bt_stride + pidx] : -1;
+    if (page < 0 || page >= p.num_pages) {
+      atomicOr(p.err, kErrBadIndex);
+      continue;
+    }
+    const int row = pos % p.page_size;
+    const char *src;
+    char *dst;
+    if (!is_v) {
+      src = reinterpret_cast<const char *>(p.kn) + 2 * (b * p.kn_sb + hk * p.kn_sh + t * p.kn_sn + e);
+      dst = reinterpret_cast<char *>(p.kc) + 2 * (page * p.kc_sb + hk * p.kc_sh + row * p.kc_sn + e);
+    } else {
+      src = reinterpret_cast<const char *>(p.vn) + 2 * (b * p.vn_sb + hk * p.vn_sh + t * p.vn_sn + e);
+      dst = reinterpret_cast<char *>(p.vc) + 2 * (page * p.vc_sb + hk * p.vc_sh + row * p.vc_sn + e);
+    }
+    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+  }
+}
+
+template <int D, int GH, bool BF16, bool PAGED>
 cudaError_t launch_split(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int B, int Hkv,
                          cudaStream_t stream) {
   using C = DecCfg<D, GH>;
-  auto kern = decode_split_kernel<D, GH, BF16>;
+  auto kern = decode_split_kernel<D, GH, BF16, PAGED>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
@@ -427,10 +505,12 @@ int decode_heads_per_cta(int group) {
   return 8;
 }
 
-cudaError_t launch_decode(int D, bool bf16, int gh, const CUtensorMap &tk, const CUtensorMap &tv,
+cudaError_t launch_decode(int D, bool bf16, bool paged, int gh, const CUtensorMap &tk, const CUtensorMap &tv,
                           const DecodeParams &p, int B, int Hkv, cudaStream_t stream) {
-#define ATTN_DECODE_CASE(DD, GG, BB) \
-  if (D == DD && gh == GG && bf16 == BB) return launch_split<DD, GG, BB>(tk, tv, p, B, Hkv, stream);
+#define ATTN_DECODE_CASE(DD, GG, BB)                                                             \
+  if (D == DD && gh == GG && bf16 == BB)                                                         \
+    return paged ? launch_split<DD, GG, BB, true>(tk, tv, p, B, Hkv, stream)                     \
+                 : launch_split<DD, GG, BB, false>(tk, tv, p, B, Hkv, stream);
 #define ATTN_DECODE_GH(DD, BB) \
   ATTN_DECODE_CASE(DD, 1, BB) ATTN_DECODE_CASE(DD, 2, BB) ATTN_DECODE_CASE(DD, 4, BB) ATTN_DECODE_CASE(DD, 8, BB)
   ATTN_DECODE_GH(128, true)
@@ -442,11 +522,14 @@ cudaError_t launch_decode(int D, bool bf16, int gh, const CUtensorMap &tk, const
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_kv_cache_write(const KvWriteParams &p, cudaStream_t stream) {
+cudaError_t launch_kv_cache_write(const KvWriteParams &p, bool paged, cudaStream_t stream) {
   const int64_t work = 2 * p.total_units;
   int64_t blocks = (work + 255) / 256;
   if (blocks > 65535 * 8) blocks = 65535 * 8;
-  kv_cache_write_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  if (paged)
+    kv_cache_write_paged_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  else
+    kv_cache_write_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

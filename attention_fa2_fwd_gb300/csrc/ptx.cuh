@@ -17,6 +17,7 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 // Device error codes (bits of the device error word).
 constexpr unsigned kErrWaitTimeout = 1u;
+constexpr unsigned kErrBadIndex = 2u;  // a page id, cache length or position read from device memory was out of range
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -30,8 +30,9 @@
  * - Argument errors are detected on the host before anything is launched and
  *   are returned synchronously; nothing is enqueued in that case.  A failed
  *   launch returns ATTN_ERR_CUDA.
- * - Device-side failures (a pipeline wait that exceeded its time limit) are
- *   recorded in a device error word; read and clear it with
+ * - Device-side failures (a pipeline wait that exceeded its time limit, or an
+ *   out-of-range page id, length or position read from device memory by the
+ *   paged calls) are recorded in a device error word; read and clear it with
  *   attn_get_device_error().  While the word is non-zero, the library's
  *   kernels return immediately without computing.
  * - There is no CPU fallback and no other backend: every call runs the CUDA
@@ -54,7 +55,8 @@ typedef enum {
     ATTN_ERR_ALIGNMENT = 3,       /* d stride != 1, pointer or stride not 16-byte aligned */
     ATTN_ERR_WORKSPACE = 4,       /* workspace missing or smaller than attn_decode_workspace_size() */
     ATTN_ERR_CUDA = 5,            /* a CUDA runtime/driver call or a launch failed */
-    ATTN_ERR_DEVICE_TIMEOUT = 6   /* a kernel gave up on a pipeline wait (see attn_get_device_error) */
+    ATTN_ERR_DEVICE_TIMEOUT = 6,  /* a kernel gave up on a pipeline wait (see attn_get_device_error) */
+    ATTN_ERR_DEVICE_INDEX = 7     /* a kernel read an out-of-range page id, length or position */
 } attn_status_t;
 
 typedef enum {
@@ -192,10 +194,64 @@ attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k_cache, const 
                                       const int64_t o_str[4], float scale, void *stream);
 
 /*
+ * attn_fwd_decode_paged -- decode for a batch of requests whose KV caches live
+ * in pages of a shared pool and whose lengths differ.
+ *
+ * Extends attn_fwd_decode to the serving layout the "Triton-FlashAttention"
+ * page lists as deferred ("Deferred / explicitly out of scope": batched, paged
+ * decode across requests with differing cache lengths).  Request b's cache is
+ * the sequence of pages block_table[b][0], block_table[b][1], ...; its first
+ * cache_lens[b] rows are attended to by its one query token.
+ *
+ *   q            (B, H_q, 1, D) strides q_str[4]                            read
+ *   k_pages      (num_pages, H_kv, page_size, D) strides kp_str[4], in
+ *                (page, head, row, d) order                                 read
+ *   v_pages      same shape, strides vp_str[4]                              read
+ *   block_table  int32 device array (B, max_pages), row stride bt_stride
+ *                elements (>= max_pages); entries past a request's last page
+ *                are never read                                             read
+ *   cache_lens   int32 device array (B); 0 <= cache_lens[b] <= max_cache_len  read
+ *   max_cache_len  host upper bound of the lengths (<= max_pages * page_size);
+ *                it sizes the split of each request's cache over CTAs
+ *   page_size    16, 32 or a multiple of 64 (rows per page)
+ *   o, lse       as attn_fwd_decode; a request of length 0 gets O = 0, LSE = -inf
+ *   workspace    as attn_fwd_decode (attn_decode_workspace_size)
+ *
+ * A page id outside [0, num_pages) or a length outside [0, max_cache_len]
+ * found on the device is recorded as ATTN_ERR_DEVICE_INDEX (the page reads as
+ * zeros, the length is clamped); argument errors are returned before launch.
+ */
+attn_status_t attn_fwd_decode_paged(const void *q, const void *k_pages, const void *v_pages, void *o, float *lse,
+                                    attn_dtype_t dtype, int B, int H_q, int H_kv, int D, int num_pages,
+                                    int page_size, const int32_t *block_table, int max_pages, int64_t bt_stride,
+                                    const int32_t *cache_lens, int max_cache_len, const int64_t q_str[4],
+                                    const int64_t kp_str[4], const int64_t vp_str[4], const int64_t o_str[4],
+                                    float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * kv_cache_write_paged -- write n_new tokens per request into a paged cache.
+ *
+ * Token t of request b goes to position positions[b] + t of its cache, i.e. row
+ * (pos % page_size) of page block_table[b][pos / page_size] (the page layout
+ * of attn_fwd_decode_paged).  positions is an int32 device array (B).  A write
+ * whose page index or page id is out of range is skipped and recorded as
+ * ATTN_ERR_DEVICE_INDEX.
+ *
+ *   k_pages, v_pages  (num_pages, H_kv, page_size, D) strides kp_str / vp_str   written
+ *   k_new, v_new      (B, H_kv, n_new, D) strides kn_str / vn_str               read
+ */
+attn_status_t kv_cache_write_paged(void *k_pages, void *v_pages, const void *k_new, const void *v_new,
+                                   attn_dtype_t dtype, int B, int H_kv, int n_new, int D, int num_pages,
+                                   int page_size, const int32_t *block_table, int max_pages, int64_t bt_stride,
+                                   const int32_t *positions, const int64_t kp_str[4], const int64_t vp_str[4],
+                                   const int64_t kn_str[4], const int64_t vn_str[4], void *stream);
+
+/*
  * attn_get_device_error -- synchronise `stream`, read the device error word of
  * the current device and clear it.  Returns ATTN_OK if no kernel reported a
- * failure, ATTN_ERR_DEVICE_TIMEOUT if one gave up on a wait, ATTN_ERR_CUDA if
- * the synchronisation itself failed.
+ * failure, ATTN_ERR_DEVICE_TIMEOUT if one gave up on a wait,
+ * ATTN_ERR_DEVICE_INDEX if a paged call met an out-of-range page id, length or
+ * position, ATTN_ERR_CUDA if the synchronisation itself failed.
  */
 attn_status_t attn_get_device_error(void *stream);
 

@@ -16,6 +16,12 @@ Definitions followed (see the header of ``attn_oracle.c`` for the steps):
 * ``kv_cache_write``: "Triton-FlashAttention", Phase 2 (the preallocated-cache
   write helper kept apart from the attention math) -- a plain copy of the new
   tokens into positions [pos, pos + n) of the cache.
+* ``gather_pages``, ``decode_paged``, ``kv_cache_write_paged``: the paged,
+  per-request-length decode that "Triton-FlashAttention" lists as deferred
+  work (Deferred / explicitly out of scope).  Row t of request b's cache is row
+  t % page_size of page block_table[b][t // page_size] of a shared pool;
+  decode_paged is ``decode`` over each request's gathered rows, and a request
+  of length 0 gives O = 0, LSE = -inf.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (hand-derived fixtures, closed forms, invariants and planted-mistake checks).
@@ -179,3 +185,54 @@ def kv_cache_write(k_cache, v_cache, k_new, v_new, pos: int):
     kc[:, :, pos:pos + n, :] = k_new
     vc[:, :, pos:pos + n, :] = v_new
     return kc, vc
+
+
+def gather_pages(pages, block_table_row, length: int):
+    """Rows [0, length) of one request's paged cache, as (H_kv, length, D).
+
+    pages: (num_pages, H_kv, page_size, D); row t of the request is row
+    t % page_size of page block_table_row[t // page_size].
+    """
+    pages = np.asarray(pages)
+    page_size = pages.shape[2]
+    out = np.empty((pages.shape[1], length, pages.shape[3]), dtype=pages.dtype)
+    for t in range(length):
+        out[:, t, :] = pages[int(block_table_row[t // page_size]), :, t % page_size, :]
+    return out
+
+
+def decode_paged(q, k_pages, v_pages, block_table, cache_lens, scale: float, nthreads: int | None = None):
+    """Decode of each request b over its own cache_lens[b] paged rows.
+
+    q: (B, H_q, D); pages: (num_pages, H_kv, page_size, D); block_table (B, max_pages).
+    Returns (O (B, H_q, D), LSE (B, H_q)); a request of length 0 gets O = 0, LSE = -inf.
+    """
+    q = _f64(q)
+    B, Hq, D = q.shape
+    o = np.zeros((B, Hq, D))
+    lse = np.full((B, Hq), -np.inf)
+    for b in range(B):
+        n = int(cache_lens[b])
+        if n == 0:
+            continue
+        kc = gather_pages(k_pages, block_table[b], n)[None]
+        vc = gather_pages(v_pages, block_table[b], n)[None]
+        ob, lb = decode(q[b:b + 1], kc, vc, n, scale, nthreads)
+        o[b], lse[b] = ob[0], lb[0]
+    return o, lse
+
+
+def kv_cache_write_paged(k_pages, v_pages, k_new, v_new, block_table, positions):
+    """Copies of the page pools with token t of request b (k_new[b, :, t]) at
+    row (p % page_size) of page block_table[b][p // page_size], p = positions[b] + t."""
+    kp = np.array(k_pages, copy=True)
+    vp = np.array(v_pages, copy=True)
+    k_new, v_new = np.asarray(k_new), np.asarray(v_new)
+    page_size = kp.shape[2]
+    for b in range(k_new.shape[0]):
+        for t in range(k_new.shape[2]):
+            pos = int(positions[b]) + t
+            page = int(block_table[b][pos // page_size])
+            kp[page, :, pos % page_size, :] = k_new[b, :, t, :]
+            vp[page, :, pos % page_size, :] = v_new[b, :, t, :]
+    return kp, vp

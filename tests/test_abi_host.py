@@ -47,7 +47,7 @@ def test_library_exports_every_declared_function(lib):
 def test_status_strings(lib):
     for code, name in [(0, "ATTN_OK"), (1, "ATTN_ERR_INVALID_ARG"), (2, "ATTN_ERR_UNSUPPORTED"),
                        (3, "ATTN_ERR_ALIGNMENT"), (4, "ATTN_ERR_WORKSPACE"), (5, "ATTN_ERR_CUDA"),
-                       (6, "ATTN_ERR_DEVICE_TIMEOUT")]:
+                       (6, "ATTN_ERR_DEVICE_TIMEOUT"), (7, "ATTN_ERR_DEVICE_INDEX")]:
         assert A.attn_status_string(code) == name
     assert A.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
 
@@ -144,3 +144,52 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(A, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(A.AttnLibraryMissing):
         A.lib()
+
+
+def decode_paged(**kw):
+    a = dict(q=P, k_pages=P, v_pages=P, o=P, lse=None, dtype=A.ATTN_BF16, B=2, H_q=32, H_kv=8, D=128,
+             num_pages=100, page_size=16, block_table=P, max_pages=64, bt_stride=64, cache_lens=P,
+             max_cache_len=1000, q_str=contig(2, 32, 1, 128), kp_str=contig(100, 8, 16, 128),
+             vp_str=contig(100, 8, 16, 128), o_str=contig(2, 32, 1, 128), scale=0.088, workspace=P,
+             workspace_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return A.attn_fwd_decode_paged(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(block_table=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(cache_lens=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(max_cache_len=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(max_cache_len=64 * 16 + 1), A.ATTN_ERR_INVALID_ARG),
+    (dict(bt_stride=10), A.ATTN_ERR_INVALID_ARG),
+    (dict(num_pages=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(page_size=24), A.ATTN_ERR_UNSUPPORTED),
+    (dict(page_size=96), A.ATTN_ERR_UNSUPPORTED),
+    (dict(block_table=P + 2), A.ATTN_ERR_ALIGNMENT),
+    (dict(cache_lens=P + 1), A.ATTN_ERR_ALIGNMENT),
+    (dict(D=80), A.ATTN_ERR_UNSUPPORTED),
+    (dict(H_q=30), A.ATTN_ERR_INVALID_ARG),
+])
+def test_decode_paged_argument_errors(lib, kw, code):
+    assert decode_paged(**kw) == code
+
+
+def cache_write_paged(**kw):
+    a = dict(k_pages=P, v_pages=P, k_new=P, v_new=P, dtype=A.ATTN_BF16, B=2, H_kv=8, n_new=1, D=128,
+             num_pages=100, page_size=16, block_table=P, max_pages=64, bt_stride=64, positions=P,
+             kp_str=contig(100, 8, 16, 128), vp_str=contig(100, 8, 16, 128), kn_str=contig(2, 8, 1, 128),
+             vn_str=contig(2, 8, 1, 128), stream=None)
+    a.update(kw)
+    return A.kv_cache_write_paged(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(positions=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(block_table=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(n_new=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(page_size=8), A.ATTN_ERR_UNSUPPORTED),
+    (dict(positions=P + 2), A.ATTN_ERR_ALIGNMENT),
+    (dict(k_new=P + 8), A.ATTN_ERR_ALIGNMENT),
+])
+def test_cache_write_paged_argument_errors(lib, kw, code):
+    assert cache_write_paged(**kw) == code

@@ -74,6 +74,8 @@ def check_golden(orc):
     for path in files:
         with open(path) as f:
             g = json.load(f)
+        if "shape" not in g:  # paged-layout fixtures are checked by test_paged_golden
+            continue
         s = g["shape"]
         q = np.array(g["q"], dtype=np.float64).reshape(s["B"], s["Hq"], s["Nq"], s["D"])
         k = np.array(g["k"], dtype=np.float64).reshape(s["B"], s["Hkv"], s["Nkv"], s["D"])
@@ -381,3 +383,72 @@ def test_planted_mistakes_are_caught(name):
             except AssertionError:
                 caught.append(check.__name__)
         assert caught, f"mutant '{name}' passed every pin"
+
+
+# ----------------------------------------------------------------------------- paged layout
+
+def test_paged_golden():
+    with open(os.path.join(GOLDEN, "paged_gather_d1.json")) as f:
+        g = json.load(f)
+    o, lse = oracle.decode_paged(np.array(g["q"]), np.array(g["k_pages"]), np.array(g["v_pages"]),
+                                 np.array(g["block_table"]), np.array(g["cache_lens"]), g["scale"])
+    np.testing.assert_allclose(o, np.array(g["expected"]["o"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, np.array(g["expected"]["lse"]), rtol=0, atol=1e-12)
+
+
+def _paged_from_contiguous(kc, page_size, perm):
+    """Split a contiguous cache (B, H, L, D) into a page pool whose page ids are shuffled by perm."""
+    B, H, L, D = kc.shape
+    npb = L // page_size
+    pool = np.empty((B * npb, H, page_size, D))
+    table = np.empty((B, npb), dtype=np.int64)
+    for b in range(B):
+        for i in range(npb):
+            pid = perm[b * npb + i]
+            pool[pid] = kc[b, :, i * page_size:(i + 1) * page_size, :]
+            table[b, i] = pid
+    return pool, table
+
+
+def test_paged_equals_contiguous_under_any_page_order():
+    r = _rng("paged")
+    B, Hq, Hkv, L, D, ps = 3, 8, 2, 48, 16, 16
+    q = r.normal(size=(B, Hq, D))
+    kc, vc = r.normal(size=(B, Hkv, L, D)), r.normal(size=(B, Hkv, L, D))
+    lens = np.array([48, 17, 1])
+    for perm in (np.arange(B * (L // ps)), r.permutation(B * (L // ps))):
+        kp, table = _paged_from_contiguous(kc, ps, perm)
+        vp, _ = _paged_from_contiguous(vc, ps, perm)
+        o, lse = oracle.decode_paged(q, kp, vp, table, lens, 0.25)
+        for b in range(B):
+            ob, lb = oracle.decode(q[b:b + 1], kc[b:b + 1], vc[b:b + 1], int(lens[b]), 0.25)
+            np.testing.assert_array_equal(o[b], ob[0])
+            np.testing.assert_array_equal(lse[b], lb[0])
+
+
+def test_paged_length_zero_convention():
+    q = np.ones((1, 2, 4))
+    pool = np.ones((1, 1, 16, 4))
+    o, lse = oracle.decode_paged(q, pool, pool, np.zeros((1, 1), dtype=np.int64), np.array([0]), 1.0)
+    assert (o == 0).all() and np.isneginf(lse).all()
+
+
+def test_paged_write_then_gather_roundtrip():
+    r = _rng("pwrite")
+    B, H, D, ps, npages = 2, 2, 8, 16, 6
+    kp, vp = np.zeros((npages, H, ps, D)), np.zeros((npages, H, ps, D))
+    table = np.array([[4, 1, 5], [0, 3, 2]])
+    pos = np.array([14, 0])
+    kn, vn = r.normal(size=(B, H, 5, D)), r.normal(size=(B, H, 5, D))
+    kp2, vp2 = oracle.kv_cache_write_paged(kp, vp, kn, vn, table, pos)
+    for b in range(B):
+        got = oracle.gather_pages(kp2, table[b], pos[b] + 5)[:, pos[b]:, :]
+        np.testing.assert_array_equal(got, kn[b])
+        got = oracle.gather_pages(vp2, table[b], pos[b] + 5)[:, pos[b]:, :]
+        np.testing.assert_array_equal(got, vn[b])
+    # request 0 wrote rows 14, 15 of page 4 and rows 0..2 of page 1; nothing else changed
+    touched = np.zeros((npages, ps), dtype=bool)
+    touched[4, 14:] = True
+    touched[1, :3] = True
+    touched[0, :5] = True
+    assert (kp2[~touched[:, None, :, None].repeat(H, 1).repeat(D, 3)] == 0).all()
