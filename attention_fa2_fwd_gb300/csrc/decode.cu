@@ -190,9 +190,24 @@ __global__ void __launch_bounds__(kThreads, 2)
       bool ok = true;
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % kStages;
-        if (j >= kStages && !(ok = mbar_wait(EMPTY(st), ((j / kStages) - 1) & 1, abort_flag, p.err))) break;
         const uint32_t dst = sbase + st * C::STAGE_BYTES;
         const int t0 = t_begin + j * kTok;
+        // Paged: this stage's page ids are read before the wait for a free
+        // stage, so their latency hides behind it.
+        constexpr int kMaxBox = kTok / 16;
+        int pg[kMaxBox];
+        int rows = kTok, nbox = 1;
+        if constexpr (PAGED) {
+          rows = p.page_size < kTok ? p.page_size : kTok;
+          nbox = (min(t_end - t0, kTok) + rows - 1) / rows;
+#pragma unroll
+          for (int x = 0; x < kMaxBox; ++x) {
+            const int pidx = (t0 + x * rows) / p.page_size;
+            pg[x] = (x < nbox && pidx < p.max_pages) ? __ldg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + pidx)
+                                                    : -1;
+          }
+        }
+        if (j >= kStages && !(ok = mbar_wait(EMPTY(st), ((j / kStages) - 1) & 1, abort_flag, p.err))) break;
         if constexpr (!PAGED) {
           mbar_arrive_expect_tx(FULL(st), C::STAGE_BYTES);
 #pragma unroll
@@ -204,18 +219,16 @@ __global__ void __launch_bounds__(kThreads, 2)
           // Boxes of `rows` tokens, each inside one page; rows past the length
           // are not loaded (the consumers mask them), so the stage expects only
           // the bytes of the boxes issued.
-          const int rows = p.page_size < kTok ? p.page_size : kTok;
-          const int nbox = (min(t_end - t0, kTok) + rows - 1) / rows;
           mbar_arrive_expect_tx(FULL(st), static_cast<uint32_t>(nbox * rows) * (2u * D * 2u));
-          for (int x = 0; x < nbox; ++x) {
-            const int tok = t0 + x * rows;
-            const int pidx = tok / p.page_size;
-            int page = (pidx < p.max_pages) ? p.block_table[static_cast<int64_t>(b) * p.bt_stride + pidx] : -1;
+#pragma unroll
+          for (int x = 0; x < kMaxBox; ++x) {
+            if (x >= nbox) break;
+            int page = pg[x];
             if (page < 0 || page >= p.num_pages) {
               atomicOr(p.err, kErrBadIndex);
               page = p.num_pages;  // out of the tensor map: the box reads as zeros
             }
-            const int row = tok % p.page_size;
+            const int row = (t0 + x * rows) % p.page_size;
             const uint32_t off = static_cast<uint32_t>(x * rows * 128);
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c) {

@@ -2,6 +2,7 @@
 
     python -m attention_fa2_fwd_gb300.run_case prefill [--B 2 --Hq 32 --Hkv 8 --N 8192 --D 128 --causal 1]
     python -m attention_fa2_fwd_gb300.run_case decode  [--B 64 --Hq 32 --Hkv 8 --L 8192 --D 128]
+    python -m attention_fa2_fwd_gb300.run_case decode_paged [--page-size 16 --ragged 1 ...]
 
 Inputs are seeded N(0,1) bf16 tensors drawn on the device.  Each iteration is
 timed with CUDA events on the launching stream (L2 flushed by a 256 MiB write
@@ -20,7 +21,7 @@ import attention_fa2_fwd_gb300 as A
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=("prefill", "decode"))
+    ap.add_argument("kind", choices=("prefill", "decode", "decode_paged"))
     ap.add_argument("--B", type=int)
     ap.add_argument("--Hq", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=8)
@@ -30,6 +31,8 @@ def main():
     ap.add_argument("--causal", type=int, default=1)
     ap.add_argument("--iters", type=int, default=5)
     ap.add_argument("--dtype", choices=("bf16", "f16"), default="bf16")
+    ap.add_argument("--page-size", type=int, default=16)
+    ap.add_argument("--ragged", type=int, default=0, help="decode_paged: lengths uniform in [L/2, L]")
     a = ap.parse_args()
     dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
     dev = torch.device("cuda", 0)
@@ -50,6 +53,28 @@ def main():
         def call():
             A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse)
         unit, scale = "TFLOPS", 1e12
+    elif a.kind == "decode_paged":
+        B = a.B or 64
+        ps = a.page_size
+        max_pages = (a.L + ps - 1) // ps
+        num_pages = B * max_pages
+        kp, vp = randn(num_pages, a.Hkv, ps, a.D), randn(num_pages, a.Hkv, ps, a.D)
+        perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(7)).to(torch.int32)
+        table = perm.view(B, max_pages).to(dev)
+        if a.ragged:
+            lens = torch.randint(a.L // 2, a.L + 1, (B,), generator=torch.Generator().manual_seed(8))
+        else:
+            lens = torch.full((B,), a.L)
+        lens = lens.to(torch.int32).to(dev)
+        qd = randn(B, a.Hq, a.D)
+        od = torch.empty_like(qd)
+        lsed = torch.empty((B, a.Hq), dtype=torch.float32, device=dev)
+        ws = A.decode_workspace(B, a.Hq, a.Hkv, a.D, dev)
+        work = 2.0 * a.Hkv * a.D * 2 * float(lens.sum())
+
+        def call():
+            A.decode_paged(qd, kp, vp, table, lens, a.L, out=od, lse_out=lsed, workspace=ws)
+        unit, scale = "GB/s", 1e9
     else:
         B = a.B or 64
         kc, vc = randn(B, a.Hkv, a.L, a.D), randn(B, a.Hkv, a.L, a.D)
