@@ -34,7 +34,7 @@ ATTN_F16 = 0
 ATTN_BF16 = 1
 
 # Every function that include/attn.h declares.
-EXPORTS = ("attn_fwd_prefill", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
+EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_varlen", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
            "attn_fwd_decode_noalloc", "kv_cache_write", "attn_fwd_decode_paged", "kv_cache_write_paged",
            "attn_get_device_error", "attn_status_string", "attn_version")
 
@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_prefill.restype = i32
             L.attn_fwd_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                            i64p, i64p, i64p, i64p, i32, f32, vp]
+            L.attn_fwd_prefill_varlen.restype = i32
+            L.attn_fwd_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, i32,
+                                                  i32, i32, i64p, i64p, i64p, i64p, i32, f32, vp]
             L.attn_decode_workspace_size.restype = ctypes.c_size_t
             L.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
             L.attn_decode_splits.restype = i32
@@ -111,6 +114,15 @@ def attn_fwd_prefill(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, 
     return lib().attn_fwd_prefill(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, _strides(q_str),
                                   _strides(k_str), _strides(v_str), _strides(o_str), int(causal), float(scale),
                                   stream)
+
+
+def attn_fwd_prefill_varlen(q, k, v, o, lse, dtype, B, H_q, H_kv, D, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                            max_seqlen_k, total_q, total_k, q_str, k_str, v_str, o_str, causal, scale,
+                            stream) -> int:
+    s3 = ctypes.c_int64 * 3
+    return lib().attn_fwd_prefill_varlen(q, k, v, o, lse, dtype, B, H_q, H_kv, D, cu_seqlens_q, cu_seqlens_k,
+                                         max_seqlen_q, max_seqlen_k, total_q, total_k, s3(*q_str), s3(*k_str),
+                                         s3(*v_str), s3(*o_str), int(causal), float(scale), stream)
 
 
 def attn_decode_workspace_size(B, H_q, H_kv, D) -> int:
@@ -221,6 +233,35 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_ls
                           q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
                           _stream_handle(stream))
     _check(st, "attn_fwd_prefill")
+    return o, lse
+
+
+def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                   causal: bool = False, scale: float | None = None, return_lse: bool = True, out=None,
+                   lse_out=None, stream=None):
+    """Attention over packed sequences of different lengths.
+
+    q (total_q, H_q, D); k, v (total_k, H_kv, D); cu_seqlens_q / cu_seqlens_k int32 CUDA tensors (B + 1).
+    Returns (O (total_q, H_q, D), LSE (H_q, total_q) fp32 or None).
+    """
+    import torch
+    total_q, Hq, D = q.shape
+    total_k, Hkv, _ = k.shape
+    cq = _int32_cuda(cu_seqlens_q, "cu_seqlens_q")
+    ck = _int32_cuda(cu_seqlens_k, "cu_seqlens_k")
+    B = cq.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = out if out is not None else torch.empty((total_q, Hq, D), dtype=q.dtype, device=q.device)
+    lse = None
+    if return_lse:
+        lse = lse_out if lse_out is not None else torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    st = attn_fwd_prefill_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, D,
+                                 cq.data_ptr(), ck.data_ptr(), int(max_seqlen_q), int(max_seqlen_k), total_q, total_k,
+                                 q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
+                                 _stream_handle(stream))
+    _check(st, "attn_fwd_prefill_varlen")
     return o, lse
 
 

@@ -223,7 +223,62 @@ attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void
   p.group = H_q / H_kv;
   p.n_qtiles = (N_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  cudaError_t e = launch_prefill(D, causal != 0, bf16, tq, tk, tv, p, B, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_prefill(D, causal != 0, bf16, false, tq, tk, tv, p, B, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_fwd_prefill_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                                      attn_dtype_t dtype, int B, int H_q, int H_kv, int D, const int32_t *cu_seqlens_q,
+                                      const int32_t *cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, int total_q,
+                                      int total_k, const int64_t q_str[3], const int64_t k_str[3],
+                                      const int64_t v_str[3], const int64_t o_str[3], int causal, float scale,
+                                      void *stream) {
+  if (!q || !k || !v || !o || !cu_seqlens_q || !cu_seqlens_k || !q_str || !k_str || !v_str || !o_str)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H_q < 1 || H_kv < 1 || D < 1 || max_seqlen_q < 1 || max_seqlen_k < 1 || total_q < 1 || total_k < 1)
+    return ATTN_ERR_INVALID_ARG;
+  if (max_seqlen_q > total_q || max_seqlen_k > total_k) return ATTN_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f) || B > 65535 || H_q > 65535) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3)) || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3))
+    return ATTN_ERR_ALIGNMENT;
+  // Packed tensors seen as (1, H, total, D) with (b, h, n, d) strides.
+  const int64_t qsz[4] = {1, H_q, total_q, D}, kvsz[4] = {1, H_kv, total_k, D};
+  const int64_t q4[4] = {0, q_str[1], q_str[0], q_str[2]}, k4[4] = {0, k_str[1], k_str[0], k_str[2]};
+  const int64_t v4[4] = {0, v_str[1], v_str[0], v_str[2]}, o4[4] = {0, o_str[1], o_str[0], o_str[2]};
+  attn_status_t st;
+  if ((st = check_strides(q4, qsz)) || (st = check_strides(k4, kvsz)) || (st = check_strides(v4, kvsz)) ||
+      (st = check_strides(o4, qsz)))
+    return st;
+  const DeviceState *dev = nullptr;
+  if ((st = device_state(&dev)) != ATTN_OK) return st;
+  const bool bf16 = dtype == ATTN_BF16;
+  CUtensorMap tq, tk, tv;
+  PrefillParams p{};
+  if ((st = make_map(&tq, q, bf16, qsz, q4, kPrefillBM, &p.slots_q)) ||
+      (st = make_map(&tk, k, bf16, kvsz, k4, kPrefillBN, &p.slots_k)) ||
+      (st = make_map(&tv, v, bf16, kvsz, v4, kPrefillBN, &p.slots_v)))
+    return st;
+  p.o = o;
+  p.lse = lse;
+  p.err = dev->err;
+  p.o_sb = 0;
+  p.o_sh = o4[1];
+  p.o_sn = o4[2];
+  p.Nq = max_seqlen_q;
+  p.Nkv = max_seqlen_k;
+  p.Hq = H_q;
+  p.group = H_q / H_kv;
+  p.n_qtiles = (max_seqlen_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  cudaError_t e = launch_prefill(D, causal != 0, bf16, true, tq, tk, tv, p, B, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -28,6 +28,11 @@ struct PrefillParams {
   // Tensor-map coordinate slot (1..3) of the n, h and b coordinates for the
   // Q, K and V maps, packed as n | h << 2 | b << 4 (slot 0 is always d).
   uint32_t slots_q, slots_k, slots_v;
+  // Variable-length batches only: packed Q/K/V/O rows; sequence b owns rows
+  // [cu_q[b], cu_q[b+1]) of Q and O and [cu_k[b], cu_k[b+1]) of K and V; Nq / Nkv
+  // then are the host's bounds on the per-sequence lengths; LSE is (H_q, total_q).
+  const int32_t *cu_q, *cu_k;
+  int total_q, total_k;
 };
 
 struct DecodeParams {
@@ -67,7 +72,7 @@ struct KvWriteParams {
 };
 
 // Launchers (return cudaSuccess or the launch error).
-cudaError_t launch_prefill(int D, bool causal, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+cudaError_t launch_prefill(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq, const CUtensorMap &tk,
                            const CUtensorMap &tv, const PrefillParams &p, int B, cudaStream_t stream);
 
 // Decode: heads served by one CTA, and launch (split kernel, plus the merge

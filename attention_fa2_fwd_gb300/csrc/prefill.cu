@@ -75,7 +75,9 @@ struct Cfg {
   static constexpr int B_PF = 3 + 4 * ST;   // + tile (2): P_i(j) stored (and O_i rescaled)
   static constexpr int B_OD = 5 + 4 * ST;   // + tile (2): last P_i V done
   static constexpr int B_DONE = 7 + 4 * ST; // every MMA completed
-  static constexpr int NBAR = 8 + 4 * ST;
+  static constexpr int B_VZ = 8 + 4 * ST;   // variable length: V rows past the sequence zeroed
+  static constexpr int B_VT = 9 + 4 * ST;   // variable length: the tail V tile has landed
+  static constexpr int NBAR = 10 + 4 * ST;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
   // + slack for 1024-byte alignment; at least 116 KB so that only one CTA (which
@@ -114,7 +116,12 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <int D, bool CAUSAL, bool BF16>
+// VARLEN: the batch is packed; sequence b's rows are found through cu_q / cu_k
+// (see PrefillParams), tensor maps span the packed tensors, and the last V tile
+// of a sequence -- whose tail rows belong to the next sequence -- gets those
+// rows zeroed by warp 10 before P V reads it, so nothing from another sequence
+// (not even a non-finite value times a zero weight) reaches the result.
+template <int D, bool CAUSAL, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -138,10 +145,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = blockIdx.y, b = blockIdx.z;
   const int hk = h / p.group;
   const int q0 = pair * 2 * kBM;  // first row of tile 0; tile 1 starts at q0 + 128
-  const int nkv_all = (p.Nkv + kBN - 1) / kBN;
+  int q_base = 0, k_base = 0, Nq = p.Nq, Nkv = p.Nkv, bc = b;  // bc: batch coordinate of the tensor maps
+  if constexpr (VARLEN) {
+    const int qs = p.cu_q[b], qe = p.cu_q[b + 1], ks = p.cu_k[b], ke = p.cu_k[b + 1];
+    if (qs < 0 || qe < qs || qe > p.total_q || qe - qs > p.Nq || ks < 0 || ke < ks || ke > p.total_k ||
+        ke - ks > p.Nkv) {
+      if (threadIdx.x == 0) atomicOr(p.err, kErrBadIndex);
+      return;
+    }
+    q_base = qs;
+    k_base = ks;
+    Nq = qe - qs;
+    Nkv = ke - ks;
+    bc = 0;
+    if (q0 >= Nq) return;
+    if (Nkv == 0) {
+      // No keys: O = 0 and LSE = -inf for this pair's rows.
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      for (int r = threadIdx.x; r < 2 * kBM; r += kThreads) {
+        if (q0 + r >= Nq) break;
+        T *orow = reinterpret_cast<T *>(p.o) + static_cast<int64_t>(h) * p.o_sh +
+                  static_cast<int64_t>(q_base + q0 + r) * p.o_sn;
+        for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4 *>(orow + d) = make_uint4(0, 0, 0, 0);
+        if (p.lse != nullptr) p.lse[static_cast<int64_t>(h) * p.total_q + q_base + q0 + r] = -INFINITY;
+      }
+      return;
+    }
+  }
+  const int nkv_all = (Nkv + kBN - 1) / kBN;
   // KV tiles needed by each query tile (causal: up to and including its diagonal tile)
   const int n_kv0 = CAUSAL ? min(nkv_all, (q0 + kBM + kBN - 1) / kBN) : nkv_all;
   const int n_kv1 = CAUSAL ? min(nkv_all, (q0 + 2 * kBM + kBN - 1) / kBN) : nkv_all;
+  // Variable length: the last KV tile runs past the sequence and is used here.
+  const int j_tail = nkv_all - 1;
+  const bool zero_v = VARLEN && (Nkv % kBN) != 0 && n_kv1 == nkv_all;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_Q), 1);
@@ -157,6 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::B_OD + i), 1);
     }
     mbar_init(BAR(C::B_DONE), 1);
+    mbar_init(BAR(C::B_VZ), 1);
+    mbar_init(BAR(C::B_VT), 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -187,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c)
-            tma_tile(sQ + t * C::QT_BYTES + c * C::CHUNK_Q, &tmQ, c * 64, q0 + t * kBM, h, b, p.slots_q,
+            tma_tile(sQ + t * C::QT_BYTES + c * C::CHUNK_Q, &tmQ, c * 64, q_base + q0 + t * kBM, h, bc, p.slots_q,
                      BAR(C::B_Q));
         for (int j = 0; j < n_kv1; ++j) {
           const int st = j % ST;
@@ -196,14 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(BAR(C::B_KF + st), C::KV_BYTES);
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c)
-            tma_tile(sK + st * C::KV_BYTES + c * C::CHUNK_KV, &tmK, c * 64, j * kBN, hk, b, p.slots_k,
+            tma_tile(sK + st * C::KV_BYTES + c * C::CHUNK_KV, &tmK, c * 64, k_base + j * kBN, hk, bc, p.slots_k,
                      BAR(C::B_KF + st));
           ++issued_k;
           if (j >= ST && !(ok = mbar_wait(BAR(C::B_VE + st), ph ^ 1, abort_flag, p.err))) break;
           mbar_arrive_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c)
-            tma_tile(sV + st * C::KV_BYTES + c * C::CHUNK_KV, &tmV, c * 64, j * kBN, hk, b, p.slots_v,
+            tma_tile(sV + st * C::KV_BYTES + c * C::CHUNK_KV, &tmV, c * 64, k_base + j * kBN, hk, bc, p.slots_v,
                      BAR(C::B_VF + st));
           ++issued_v;
         }
@@ -241,6 +280,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, bdesc, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
         };
+        // V of tile j has landed (and, for a sequence's tail tile, been zeroed past
+        // the end: this thread, which follows the stage phases in order, tells
+        // warp 10 when the tail tile is in and waits for it to clear the rows).
+        auto wait_v = [&](int j) -> bool {
+          if (!mbar_wait(BAR(C::B_VF + j % ST), (j / ST) & 1, abort_flag, p.err)) return false;
+          if (!(zero_v && j == j_tail)) return true;
+          mbar_arrive(BAR(C::B_VT));
+          return mbar_wait(BAR(C::B_VZ), 0, abort_flag, p.err);
+        };
         bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, p.err);
         bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
         for (int j = 0; ok && j < n_kv1; ++j) {
@@ -254,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O1 += P1_{j-1} V_{j-1}
             const int sp = (j - 1) % ST;
             if (!(ok = mbar_wait(BAR(C::B_PF + 1), (j - 1) & 1, abort_flag, p.err))) break;
-            if (!v_waited && !(ok = mbar_wait(BAR(C::B_VF + sp), ((j - 1) / ST) & 1, abort_flag, p.err))) break;
+            if (!v_waited && !(ok = wait_v(j - 1))) break;
             tc_fence_after();
             issue_pv(1, j - 1, sV + sp * C::KV_BYTES);
             tc_commit(BAR(C::B_VE + sp));
@@ -265,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j < n_kv0) {
             // O0 += P0_j V_j
             if (!(ok = mbar_wait(BAR(C::B_PF + 0), j & 1, abort_flag, p.err))) break;
-            if (!(ok = mbar_wait(BAR(C::B_VF + st), ph, abort_flag, p.err))) break;
+            if (!(ok = wait_v(j))) break;
             v_waited = true;
             tc_fence_after();
             issue_pv(0, j, sV + st * C::KV_BYTES);
@@ -276,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int jl = n_kv1 - 1;
           const int sp = jl % ST;
           ok = mbar_wait(BAR(C::B_PF + 1), jl & 1, abort_flag, p.err) &&
-               (v_waited || mbar_wait(BAR(C::B_VF + sp), (jl / ST) & 1, abort_flag, p.err));
+               (v_waited || wait_v(jl));
           if (ok) {
             tc_fence_after();
             issue_pv(1, jl, sV + sp * C::KV_BYTES);
@@ -286,6 +334,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(BAR(C::B_DONE));
         mbar_wait(BAR(C::B_DONE), 0, nullptr, p.err);
+      }
+      __syncwarp();
+    } else if (warp == 10) {
+      // ---------------------------------------------------------- variable length: tail of V
+      if (zero_v) {
+        const int st = j_tail % ST;
+        const bool landed = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_VT), 0, abort_flag, p.err));
+        if (landed) {
+          const int r0 = Nkv % kBN;  // rows r0..127 of the tile lie past the sequence
+          uint8_t *vt = smem + C::OFF_V + st * C::KV_BYTES;
+          const int pieces = (kBN - r0) * 8;  // 16-byte pieces per 128-byte row chunk
+          for (int c = 0; c < C::KCH; ++c)
+            for (int i = lane; i < pieces; i += 32)
+              *reinterpret_cast<uint4 *>(vt + c * C::CHUNK_KV + (r0 + i / 8) * 128 + (i % 8) * 16) =
+                  make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();  // make the zeros visible to the tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_VZ));
+        }
       }
       __syncwarp();
     }
@@ -316,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 4; ++i) reg_fence(sr[i]);
 
       const int kv0 = j * kBN;
-      const bool need_mask = (kv0 + kBN > p.Nkv) || (CAUSAL && kv0 + kBN - 1 > q_tile0);
+      const bool need_mask = (kv0 + kBN > Nkv) || (CAUSAL && kv0 + kBN - 1 > q_tile0);
       if (need_mask) {
-        const int lim = (CAUSAL ? min(p.Nkv, q_row + 1) : p.Nkv) - kv0;  // columns c < lim are kept
+        const int lim = (CAUSAL ? min(Nkv, q_row + 1) : Nkv) - kv0;  // columns c < lim are kept
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -387,10 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -------------------------------------------------------- epilogue: O / l, LSE
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const bool row_ok = q_row < p.Nq;
+      const bool row_ok = q_row < Nq;
       using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      T *orow = reinterpret_cast<T *>(p.o) + static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
-                static_cast<int64_t>(q_row) * p.o_sn;
+      T *orow = reinterpret_cast<T *>(p.o) + static_cast<int64_t>(bc) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
+                static_cast<int64_t>(q_base + q_row) * p.o_sn;
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) {
         uint32_t ov[32];
@@ -409,7 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (p.lse != nullptr && row_ok)
-        p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + q_row] = (m + __log2f(l)) * kLn2;
+        p.lse[VARLEN ? static_cast<int64_t>(h) * p.total_q + q_base + q_row
+                     : (static_cast<int64_t>(b) * p.Hq + h) * p.Nq + q_row] = (m + __log2f(l)) * kLn2;
     }
   }
 
@@ -421,10 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool VARLEN>
 cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p,
                        int B, cudaStream_t stream) {
-  auto kern = prefill_fwd_kernel<D, CAUSAL, BF16>;
+  auto kern = prefill_fwd_kernel<D, CAUSAL, BF16, VARLEN>;
   constexpr uint32_t smem = Cfg<D>::SMEM_BYTES;
   // setmaxnreg redistributes the registers the CTA was launched with; a split
   // larger than that pool would never be granted, so refuse to launch then.
@@ -441,10 +509,12 @@ cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 
 }  // namespace
 
-cudaError_t launch_prefill(int D, bool causal, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk,
+cudaError_t launch_prefill(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq, const CUtensorMap &tk,
                            const CUtensorMap &tv, const PrefillParams &p, int B, cudaStream_t stream) {
-#define ATTN_PREFILL_CASE(DD, CC, BB) \
-  if (D == DD && causal == CC && bf16 == BB) return launch_one<DD, CC, BB>(tq, tk, tv, p, B, stream);
+#define ATTN_PREFILL_CASE(DD, CC, BB)                                                   \
+  if (D == DD && causal == CC && bf16 == BB)                                            \
+    return varlen ? launch_one<DD, CC, BB, true>(tq, tk, tv, p, B, stream)              \
+                  : launch_one<DD, CC, BB, false>(tq, tk, tv, p, B, stream);
   ATTN_PREFILL_CASE(128, true, true)
   ATTN_PREFILL_CASE(128, false, true)
   ATTN_PREFILL_CASE(128, true, false)

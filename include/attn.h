@@ -31,8 +31,8 @@
  *   are returned synchronously; nothing is enqueued in that case.  A failed
  *   launch returns ATTN_ERR_CUDA.
  * - Device-side failures (a pipeline wait that exceeded its time limit, or an
- *   out-of-range page id, length or position read from device memory by the
- *   paged calls) are recorded in a device error word; read and clear it with
+ *   out-of-range page id, length, position or sequence offset read from device
+ *   memory by the paged and variable-length calls) are recorded in a device error word; read and clear it with
  *   attn_get_device_error().  While the word is non-zero, the library's
  *   kernels return immediately without computing.
  * - There is no CPU fallback and no other backend: every call runs the CUDA
@@ -90,6 +90,40 @@ attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void
                                attn_dtype_t dtype, int B, int H_q, int H_kv, int N_q, int N_kv, int D,
                                const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
                                const int64_t o_str[4], int causal, float scale, void *stream);
+
+/*
+ * attn_fwd_prefill_varlen -- attn_fwd_prefill over a batch of sequences of
+ * different lengths, packed without padding.
+ *
+ * Covers the variable-length batches of "Skill: Write a Triton Attention
+ * Kernel" (Inputs: a CSR-style variable-length layout; Correctness
+ * requirements: the KV loop of a sequence ends at that sequence's own length,
+ * and padding never contributes).  Sequence b owns rows
+ * [cu_seqlens_q[b], cu_seqlens_q[b+1]) of Q and O and rows
+ * [cu_seqlens_k[b], cu_seqlens_k[b+1]) of K and V; masks (causal: key j kept
+ * for query i iff j <= i) are per sequence, positions counted from the start
+ * of the sequence.
+ *
+ *   q     (total_q, H_q, D)  element strides q_str[3] in (row, head, d) order   read
+ *   k, v  (total_k, H_kv, D) strides k_str[3], v_str[3]                        read
+ *   o     (total_q, H_q, D)  strides o_str[3]                                  written
+ *   lse   (H_q, total_q) fp32 contiguous, natural log, or NULL
+ *   cu_seqlens_q, cu_seqlens_k  int32 device arrays (B + 1), non-decreasing,
+ *         starting at 0 and ending at total_q / total_k
+ *   max_seqlen_q, max_seqlen_k  host bounds of the sequence lengths (they size
+ *         the grid); a sequence with no keys gets O = 0 and LSE = -inf
+ *   Rows are 16-byte aligned as for attn_fwd_prefill; d stride 1.
+ *
+ * A cu_seqlens entry that is out of order, past total_*, or gives a length
+ * above max_seqlen_* is recorded as ATTN_ERR_DEVICE_INDEX and that sequence
+ * is left unwritten.  Returns ATTN_OK after enqueueing one kernel on `stream`.
+ */
+attn_status_t attn_fwd_prefill_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                                      attn_dtype_t dtype, int B, int H_q, int H_kv, int D, const int32_t *cu_seqlens_q,
+                                      const int32_t *cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, int total_q,
+                                      int total_k, const int64_t q_str[3], const int64_t k_str[3],
+                                      const int64_t v_str[3], const int64_t o_str[3], int causal, float scale,
+                                      void *stream);
 
 /*
  * attn_decode_workspace_size -- bytes of scratch attn_fwd_decode needs.

@@ -16,6 +16,10 @@ Definitions followed (see the header of ``attn_oracle.c`` for the steps):
 * ``kv_cache_write``: "Triton-FlashAttention", Phase 2 (the preallocated-cache
   write helper kept apart from the attention math) -- a plain copy of the new
   tokens into positions [pos, pos + n) of the cache.
+* ``prefill_varlen``: "Skill: Write a Triton Attention Kernel" (Inputs and
+  Correctness requirements on variable-length batches) -- ``attention`` of
+  each packed sequence on its own rows, masks and positions per sequence; a
+  sequence with no keys gives O = 0, LSE = -inf.
 * ``gather_pages``, ``decode_paged``, ``kv_cache_write_paged``: the paged,
   per-request-length decode that "Triton-FlashAttention" lists as deferred
   work (Deferred / explicitly out of scope).  Row t of request b's cache is row
@@ -236,3 +240,26 @@ def kv_cache_write_paged(k_pages, v_pages, k_new, v_new, block_table, positions)
             kp[page, :, pos % page_size, :] = k_new[b, :, t, :]
             vp[page, :, pos % page_size, :] = v_new[b, :, t, :]
     return kp, vp
+
+
+def prefill_varlen(q, k, v, cu_q, cu_k, causal: bool, scale: float, nthreads: int | None = None):
+    """Attention of packed sequences: sequence b is rows [cu_q[b], cu_q[b+1]) of
+    q (total_q, H_q, D) against rows [cu_k[b], cu_k[b+1]) of k, v (total_k, H_kv, D).
+
+    Returns (O (total_q, H_q, D), LSE (H_q, total_q)).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    total_q, Hq, D = q.shape
+    o = np.zeros((total_q, Hq, D))
+    lse = np.full((Hq, total_q), -np.inf)
+    for b in range(len(cu_q) - 1):
+        qs, qe, ks, ke = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        if qe == qs or ke == ks:
+            continue
+        qb = q[qs:qe].transpose(1, 0, 2)[None]
+        kb = k[ks:ke].transpose(1, 0, 2)[None]
+        vb = v[ks:ke].transpose(1, 0, 2)[None]
+        ob, lb = attention(qb, kb, vb, causal, scale, nthreads)
+        o[qs:qe] = ob[0].transpose(1, 0, 2)
+        lse[:, qs:qe] = lb[0]
+    return o, lse

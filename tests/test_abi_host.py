@@ -193,3 +193,27 @@ def cache_write_paged(**kw):
 ])
 def test_cache_write_paged_argument_errors(lib, kw, code):
     assert cache_write_paged(**kw) == code
+
+
+def prefill_varlen(**kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=None, dtype=A.ATTN_BF16, B=3, H_q=8, H_kv=2, D=128, cu_seqlens_q=P,
+             cu_seqlens_k=P, max_seqlen_q=100, max_seqlen_k=100, total_q=200, total_k=200,
+             q_str=(8 * 128, 128, 1), k_str=(2 * 128, 128, 1), v_str=(2 * 128, 128, 1), o_str=(8 * 128, 128, 1),
+             causal=1, scale=0.088, stream=None)
+    a.update(kw)
+    return A.attn_fwd_prefill_varlen(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu_seqlens_q=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(max_seqlen_q=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(max_seqlen_k=300), A.ATTN_ERR_INVALID_ARG),
+    (dict(total_q=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(H_kv=3), A.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), A.ATTN_ERR_UNSUPPORTED),
+    (dict(cu_seqlens_k=P + 2), A.ATTN_ERR_ALIGNMENT),
+    (dict(q_str=(8 * 128, 128, 2)), A.ATTN_ERR_ALIGNMENT),
+    (dict(k_str=(2 * 128 + 4, 128, 1)), A.ATTN_ERR_ALIGNMENT),
+])
+def test_prefill_varlen_argument_errors(lib, kw, code):
+    assert prefill_varlen(**kw) == code

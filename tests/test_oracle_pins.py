@@ -452,3 +452,54 @@ def test_paged_write_then_gather_roundtrip():
     touched[1, :3] = True
     touched[0, :5] = True
     assert (kp2[~touched[:, None, :, None].repeat(H, 1).repeat(D, 3)] == 0).all()
+
+
+# ----------------------------------------------------------------------------- variable length
+
+def test_varlen_golden_is_the_concatenation_of_fixtures():
+    """Two hand-derived fixtures packed back to back give their own expected values."""
+    with open(os.path.join(GOLDEN, "two_keys_d1.json")) as f:
+        g1 = json.load(f)
+    with open(os.path.join(GOLDEN, "causal_prefix_mean_d1.json")) as f:
+        g2 = json.load(f)
+    assert g1["scale"] == 1.0
+    # rescale fixture 2's queries so both use scale 1 (scores are the same: its keys are all 0)
+    q = np.array(g1["q"] + g2["q"]).reshape(-1, 1, 1)
+    k = np.array(g1["k"] + g2["k"]).reshape(-1, 1, 1)
+    v = np.array(g1["v"] + g2["v"]).reshape(-1, 1, 1)
+    cu = np.array([0, 2, 5])
+    for mode in ("noncausal", "causal"):
+        o, lse = oracle.prefill_varlen(q, k, v, cu, cu, mode == "causal", 1.0)
+        want_o = g1["expected"][mode]["o"] + g2["expected"][mode]["o"]
+        want_l = g1["expected"][mode]["lse"] + g2["expected"][mode]["lse"]
+        np.testing.assert_allclose(o.ravel(), want_o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse.ravel(), want_l, rtol=0, atol=1e-12)
+
+
+def test_varlen_equal_lengths_equal_dense_batch():
+    r = _rng("varlen")
+    B, Hq, Hkv, N, D = 3, 4, 2, 21, 8
+    q, k, v = r.normal(size=(B, Hq, N, D)), r.normal(size=(B, Hkv, N, D)), r.normal(size=(B, Hkv, N, D))
+    cu = np.arange(B + 1) * N
+    pack = lambda x: x.transpose(0, 2, 1, 3).reshape(B * N, x.shape[1], D)
+    for causal in (False, True):
+        o, lse = oracle.prefill_varlen(pack(q), pack(k), pack(v), cu, cu, causal, 0.3)
+        od, ld = oracle.attention(q, k, v, causal, 0.3)
+        np.testing.assert_array_equal(o, pack(od))
+        np.testing.assert_array_equal(lse, ld.transpose(1, 0, 2).reshape(Hq, B * N))
+
+
+def test_varlen_sequences_do_not_interact():
+    """Changing one sequence's keys and values leaves the other sequences' results unchanged."""
+    r = _rng("varlen2")
+    H, D = 2, 8
+    cu_q, cu_k = np.array([0, 5, 12, 13]), np.array([0, 9, 10, 30])
+    q, k, v = r.normal(size=(13, H, D)), r.normal(size=(30, H, D)), r.normal(size=(30, H, D))
+    o1, l1 = oracle.prefill_varlen(q, k, v, cu_q, cu_k, True, 0.5)
+    k2, v2 = k.copy(), v.copy()
+    k2[9:10] += 3.0
+    v2[9:10] -= 7.0
+    o2, l2 = oracle.prefill_varlen(q, k2, v2, cu_q, cu_k, True, 0.5)
+    np.testing.assert_array_equal(o1[:5], o2[:5])
+    np.testing.assert_array_equal(o1[12:], o2[12:])
+    assert not np.allclose(o1[5:12], o2[5:12])
