@@ -36,6 +36,7 @@ ATTN_BF16 = 1
 # Every function that include/attn.h declares.
 EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_varlen", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
            "attn_fwd_decode_noalloc", "kv_cache_write", "attn_fwd_decode_paged", "kv_cache_write_paged",
+           "attn_bwd_workspace_size", "attn_bwd",
            "attn_get_device_error", "attn_status_string", "attn_version")
 
 
@@ -93,6 +94,11 @@ def lib() -> ctypes.CDLL:
             L.kv_cache_write_paged.restype = i32
             L.kv_cache_write_paged.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, i64,
                                                vp, i64p, i64p, i64p, i64p, vp]
+            L.attn_bwd_workspace_size.restype = ctypes.c_size_t
+            L.attn_bwd_workspace_size.argtypes = [i32, i32, i32]
+            L.attn_bwd.restype = i32
+            L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                   i64p, i64p, i64p, i64p, i64p, i64p, i64p, i64p, i32, f32, vp, ctypes.c_size_t, vp]
             L.attn_get_device_error.restype = i32
             L.attn_get_device_error.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
@@ -174,6 +180,18 @@ def kv_cache_write_paged(k_pages, v_pages, k_new, v_new, dtype, B, H_kv, n_new, 
     return lib().kv_cache_write_paged(k_pages, v_pages, k_new, v_new, dtype, B, H_kv, n_new, D, num_pages,
                                       page_size, block_table, max_pages, bt_stride, positions, _strides(kp_str),
                                       _strides(vp_str), _strides(kn_str), _strides(vn_str), stream)
+
+
+def attn_bwd_workspace_size(B, H_q, N_q) -> int:
+    return int(lib().attn_bwd_workspace_size(B, H_q, N_q))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, k_str, v_str, o_str,
+             do_str, dq_str, dk_str, dv_str, causal, scale, workspace, workspace_bytes, stream) -> int:
+    return lib().attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, dtype, B, H_q, H_kv, N_q, N_kv, D, _strides(q_str),
+                          _strides(k_str), _strides(v_str), _strides(o_str), _strides(do_str), _strides(dq_str),
+                          _strides(dk_str), _strides(dv_str), int(causal), float(scale), workspace, workspace_bytes,
+                          stream)
 
 
 def attn_get_device_error(stream=None) -> int:
@@ -263,6 +281,31 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_s
                                  _stream_handle(stream))
     _check(st, "attn_fwd_prefill_varlen")
     return o, lse
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None, stream=None):
+    """Gradients (dQ, dK, dV) of attn_fwd_prefill from its output O and LSE and the incoming dO.
+
+    Shapes as for prefill; dK, dV are summed over each GQA group.  Returns new contiguous tensors.
+    """
+    import torch
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty((B, Hq, Nq, D), dtype=q.dtype, device=q.device)
+    dk = torch.empty((B, Hkv, Nkv, D), dtype=q.dtype, device=q.device)
+    dv = torch.empty((B, Hkv, Nkv, D), dtype=q.dtype, device=q.device)
+    n = attn_bwd_workspace_size(B, Hq, Nq)
+    if workspace is None:
+        workspace = torch.empty((n + 3) // 4, dtype=torch.float32, device=q.device)
+    st = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, q.stride(),
+                  k.stride(), v.stride(), o.stride(), dout.stride(), dq.stride(), dk.stride(), dv.stride(),
+                  1 if causal else 0, scale, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                  _stream_handle(stream))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def decode_workspace(B, H_q, H_kv, D, device=None):

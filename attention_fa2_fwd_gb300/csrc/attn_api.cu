@@ -282,6 +282,79 @@ attn_status_t attn_fwd_prefill_varlen(const void *q, const void *k, const void *
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+size_t attn_bwd_workspace_size(int B, int H_q, int N_q) {
+  if (B < 1 || H_q < 1 || N_q < 1) return 0;
+  return (static_cast<size_t>(B) * H_q * N_q * sizeof(float) + 15) & ~size_t(15);
+}
+
+attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                       const float *lse, void *dq, void *dk, void *dv, attn_dtype_t dtype, int B, int H_q, int H_kv,
+                       int N_q, int N_kv, int D, const int64_t q_str[4], const int64_t k_str[4],
+                       const int64_t v_str[4], const int64_t o_str[4], const int64_t do_str[4],
+                       const int64_t dq_str[4], const int64_t dk_str[4], const int64_t dv_str[4], int causal,
+                       float scale, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !q_str || !k_str || !v_str || !o_str ||
+      !do_str || !dq_str || !dk_str || !dv_str)
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H_q < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f) || B > 65535 || H_q > 65535) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3))
+    return ATTN_ERR_ALIGNMENT;
+  const int64_t qsz[4] = {B, H_q, N_q, D}, kvsz[4] = {B, H_kv, N_kv, D};
+  attn_status_t st;
+  if ((st = check_strides(q_str, qsz)) || (st = check_strides(k_str, kvsz)) || (st = check_strides(v_str, kvsz)) ||
+      (st = check_strides(o_str, qsz)) || (st = check_strides(do_str, qsz)) || (st = check_strides(dq_str, qsz)) ||
+      (st = check_strides(dk_str, kvsz)) || (st = check_strides(dv_str, kvsz)))
+    return st;
+  const size_t need = attn_bwd_workspace_size(B, H_q, N_q);
+  if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15) != 0) return ATTN_ERR_ALIGNMENT;
+  const DeviceState *dev = nullptr;
+  if ((st = device_state(&dev)) != ATTN_OK) return st;
+  const bool bf16 = dtype == ATTN_BF16;
+  BwdMaps m;
+  BwdParams p{};
+  if ((st = make_map(&m.q, q, bf16, qsz, q_str, 128, &p.slots_q)) ||
+      (st = make_map(&m.dout, dout, bf16, qsz, do_str, 128, &p.slots_do)) ||
+      (st = make_map(&m.k, k, bf16, kvsz, k_str, 128, &p.slots_k)) ||
+      (st = make_map(&m.v, v, bf16, kvsz, v_str, 128, &p.slots_v)))
+    return st;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dvec = static_cast<float *>(workspace);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.err = dev->err;
+  p.o_sb = o_str[0];
+  p.o_sh = o_str[1];
+  p.o_sn = o_str[2];
+  p.do_sb = do_str[0];
+  p.do_sh = do_str[1];
+  p.do_sn = do_str[2];
+  p.dq_sb = dq_str[0];
+  p.dq_sh = dq_str[1];
+  p.dq_sn = dq_str[2];
+  p.dk_sb = dk_str[0];
+  p.dk_sh = dk_str[1];
+  p.dk_sn = dk_str[2];
+  p.dv_sb = dv_str[0];
+  p.dv_sh = dv_str[1];
+  p.dv_sn = dv_str[2];
+  p.Nq = N_q;
+  p.Nkv = N_kv;
+  p.Hq = H_q;
+  p.group = H_q / H_kv;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  cudaError_t e = launch_bwd(D, causal != 0, bf16, m, p, B, H_kv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 size_t attn_decode_workspace_size(int B, int H_q, int H_kv, int D) {
   if (B < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || (D != 64 && D != 128)) return 0;
   const DeviceState *dev = nullptr;

@@ -83,4 +83,23 @@ cudaError_t launch_decode(int D, bool bf16, bool paged, int heads_per_cta, const
 
 cudaError_t launch_kv_cache_write(const KvWriteParams &p, bool paged, cudaStream_t stream);
 
+// Backward.
+struct BwdParams {
+  const void *o, *dout;
+  const float *lse;         // forward LSE (B, H_q, N_q), natural log
+  float *dvec;              // workspace: D_i = rowsum(dO o O), (B, H_q, N_q)
+  void *dq, *dk, *dv;
+  unsigned *err;
+  int64_t o_sb, o_sh, o_sn, do_sb, do_sh, do_sn;
+  int64_t dq_sb, dq_sh, dq_sn, dk_sb, dk_sh, dk_sn, dv_sb, dv_sh, dv_sn;
+  int Nq, Nkv, Hq, group;
+  float scale, scale_log2;
+  uint32_t slots_q, slots_do, slots_k, slots_v;
+};
+struct BwdMaps {
+  CUtensorMap q, dout, k, v;  // 4-D tiled maps, 64 x 128 boxes, 128-byte swizzle
+};
+cudaError_t launch_bwd(int D, bool causal, bool bf16, const BwdMaps &m, const BwdParams &p, int B, int Hkv,
+                       cudaStream_t stream);
+
 }  // namespace attn

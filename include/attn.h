@@ -126,6 +126,42 @@ attn_status_t attn_fwd_prefill_varlen(const void *q, const void *k, const void *
                                       void *stream);
 
 /*
+ * attn_bwd_workspace_size -- bytes of scratch attn_bwd needs: one fp32 per
+ * query row, 4 * B * H_q * N_q rounded up to 16.  Returns 0 on bad arguments.
+ */
+size_t attn_bwd_workspace_size(int B, int H_q, int N_q);
+
+/*
+ * attn_bwd -- gradients of the fused attention forward from its saved LSE.
+ *
+ * The "Skill: Write a Triton Attention Kernel" page keeps lse = m + log(l)
+ * precisely so that a backward pass can rebuild the attention weights
+ * (P = exp(scale q.k - lse)) without storing them; "Triton-FlashAttention"
+ * lists the GQA backward (dK, dV summed over the q heads of a group) among
+ * its deferred work.  With dO the gradient of O:
+ *   dV = P^T dO,  dP = dO V^T,  D_i = sum_d dO_id O_id,  dS = P o (dP - D),
+ *   dQ = scale dS K,  dK = scale dS^T Q  (dK, dV summed over each GQA group).
+ *
+ *   q, k, v, o, lse  the forward's inputs, output and LSE (attn_fwd_prefill
+ *                    layouts and conventions, same causal and scale)     read
+ *   dout             dO, (B, H_q, N_q, D) strides do_str[4]              read
+ *   dq               (B, H_q, N_q, D) strides dq_str[4]                  written
+ *   dk, dv           (B, H_kv, N_kv, D) strides dk_str[4], dv_str[4]     written
+ *   workspace        device scratch of attn_bwd_workspace_size() bytes, not
+ *                    initialised; calls sharing one workspace must not overlap
+ *
+ * Deterministic (no atomics): dQ is computed per query tile, dK and dV per key
+ * tile with every q head of the group.  Returns ATTN_OK after enqueueing three
+ * kernels on `stream`.
+ */
+attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                       const float *lse, void *dq, void *dk, void *dv, attn_dtype_t dtype, int B, int H_q, int H_kv,
+                       int N_q, int N_kv, int D, const int64_t q_str[4], const int64_t k_str[4],
+                       const int64_t v_str[4], const int64_t o_str[4], const int64_t do_str[4],
+                       const int64_t dq_str[4], const int64_t dk_str[4], const int64_t dv_str[4], int causal,
+                       float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * attn_decode_workspace_size -- bytes of scratch attn_fwd_decode needs.
  *
  * Split-KV decode writes one partial output (D fp32) and one partial LSE per

@@ -20,6 +20,12 @@ Definitions followed (see the header of ``attn_oracle.c`` for the steps):
   Correctness requirements on variable-length batches) -- ``attention`` of
   each packed sequence on its own rows, masks and positions per sequence; a
   sequence with no keys gives O = 0, LSE = -inf.
+* ``attention_bwd``: the gradients of ``attention`` for an incoming dO
+  ("Skill: Write a Triton Attention Kernel" keeps m + log(l) so that a
+  backward pass can rebuild the weights; "Triton-FlashAttention" defers the
+  GQA backward that sums dK, dV over a group): with the explicit weights P,
+  dV = P^T dO, dP = dO V^T, dS = P o (dP - rowsum(dO o O)), dQ = scale dS K,
+  dK = scale dS^T Q, dK and dV summed over the q heads of each kv head.
 * ``gather_pages``, ``decode_paged``, ``kv_cache_write_paged``: the paged,
   per-request-length decode that "Triton-FlashAttention" lists as deferred
   work (Deferred / explicitly out of scope).  Row t of request b's cache is row
@@ -263,3 +269,33 @@ def prefill_varlen(q, k, v, cu_q, cu_k, causal: bool, scale: float, nthreads: in
         o[qs:qe] = ob[0].transpose(1, 0, 2)
         lse[:, qs:qe] = lb[0]
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, causal: bool, scale: float):
+    """(dQ, dK, dV) of O = softmax(scale Q K^T + mask) V for the incoming gradient dout, in fp64.
+
+    q, dout: (B, H_q, N_q, D); k, v: (B, H_kv, N_kv, D).  Plain dense matrices per (b, q head).
+    """
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    g = Hq // Hkv
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // g
+            s = scale * (q[b, h] @ k[b, hk].T)
+            if causal:
+                s = np.where(np.arange(Nkv)[None, :] > np.arange(Nq)[:, None], -np.inf, s)
+            m = s.max(axis=1, keepdims=True)
+            p = np.exp(s - m)
+            p /= p.sum(axis=1, keepdims=True)
+            o = p @ v[b, hk]
+            dv[b, hk] += p.T @ dout[b, h]
+            dp = dout[b, h] @ v[b, hk].T
+            ds = p * (dp - (dout[b, h] * o).sum(axis=1, keepdims=True))
+            dq[b, h] = scale * (ds @ k[b, hk])
+            dk[b, hk] += scale * (ds.T @ q[b, h])
+    return dq, dk, dv

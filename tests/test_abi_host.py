@@ -217,3 +217,35 @@ def prefill_varlen(**kw):
 ])
 def test_prefill_varlen_argument_errors(lib, kw, code):
     assert prefill_varlen(**kw) == code
+
+
+def bwd(**kw):
+    s4 = contig(2, 8, 64, 128)
+    k4 = contig(2, 2, 64, 128)
+    a = dict(q=P, k=P, v=P, o=P, dout=P, lse=P, dq=P, dk=P, dv=P, dtype=A.ATTN_BF16, B=2, H_q=8, H_kv=2, N_q=64,
+             N_kv=64, D=128, q_str=s4, k_str=k4, v_str=k4, o_str=s4, do_str=s4, dq_str=s4, dk_str=k4, dv_str=k4,
+             causal=1, scale=0.088, workspace=P, workspace_bytes=1 << 20, stream=None)
+    a.update(kw)
+    return A.attn_bwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dout=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(lse=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(H_kv=3), A.ATTN_ERR_INVALID_ARG),
+    (dict(N_kv=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(D=32), A.ATTN_ERR_UNSUPPORTED),
+    (dict(dq=P + 8), A.ATTN_ERR_ALIGNMENT),
+    (dict(lse=P + 2), A.ATTN_ERR_ALIGNMENT),
+    (dict(workspace=None), A.ATTN_ERR_WORKSPACE),
+    (dict(workspace_bytes=16), A.ATTN_ERR_WORKSPACE),
+    (dict(dk_str=(2 * 64 * 128, 64 * 128, 128, 2)), A.ATTN_ERR_ALIGNMENT),
+])
+def test_bwd_argument_errors(lib, kw, code):
+    assert bwd(**kw) == code
+
+
+def test_bwd_workspace_size():
+    assert A.attn_bwd_workspace_size(2, 8, 64) == 2 * 8 * 64 * 4
+    assert A.attn_bwd_workspace_size(1, 1, 3) == 16
+    assert A.attn_bwd_workspace_size(0, 8, 64) == 0

@@ -503,3 +503,57 @@ def test_varlen_sequences_do_not_interact():
     np.testing.assert_array_equal(o1[:5], o2[:5])
     np.testing.assert_array_equal(o1[12:], o2[12:])
     assert not np.allclose(o1[5:12], o2[5:12])
+
+
+# ----------------------------------------------------------------------------- backward
+
+def _loss(q, k, v, g, causal, scale):
+    """L = sum(O * G), O from the forward oracle."""
+    o, _ = oracle.attention(q, k, v, causal, scale)
+    return float(np.sum(o * g))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_matches_central_finite_differences(causal):
+    """Every gradient entry of a small GQA case against (L(x+e) - L(x-e)) / 2e through the forward oracle."""
+    r = _rng("fd", causal)
+    B, Hq, Hkv, Nq, Nkv, D, scale = 1, 4, 2, 5, 7, 3, 0.7
+    q, k, v = r.normal(size=(B, Hq, Nq, D)), r.normal(size=(B, Hkv, Nkv, D)), r.normal(size=(B, Hkv, Nkv, D))
+    g = r.normal(size=(B, Hq, Nq, D))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, causal, scale)
+    eps = 1e-5
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            fd = (_loss(args_p["q"], args_p["k"], args_p["v"], g, causal, scale)
+                  - _loss(args_m["q"], args_m["k"], args_m["v"], g, causal, scale)) / (2 * eps)
+            assert abs(fd - grad[idx]) < 1e-7 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_bwd_gqa_equals_group_sum_of_mha():
+    """GQA dK, dV equal the MHA gradients of repeat_interleave-expanded K, V summed over each group."""
+    r = _rng("bwdgqa")
+    B, Hq, Hkv, N, D = 2, 8, 2, 9, 4
+    q, k, v = r.normal(size=(B, Hq, N, D)), r.normal(size=(B, Hkv, N, D)), r.normal(size=(B, Hkv, N, D))
+    g = r.normal(size=(B, Hq, N, D))
+    for causal in (False, True):
+        dq, dk, dv = oracle.attention_bwd(q, k, v, g, causal, 0.5)
+        dq2, dk2, dv2 = oracle.attention_bwd(q, _expand(k, 4), _expand(v, 4), g, causal, 0.5)
+        np.testing.assert_allclose(dq, dq2, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dk, dk2.reshape(B, Hkv, 4, N, D).sum(axis=2), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv, dv2.reshape(B, Hkv, 4, N, D).sum(axis=2), rtol=0, atol=1e-12)
+
+
+def test_bwd_rows_of_ds_sum_to_zero():
+    """Adding the same vector to every key leaves the weights unchanged, so dL/du = sum_j dK_j = 0."""
+    r = _rng("dssum")
+    q, k, v = r.normal(size=(1, 2, 6, 4)), r.normal(size=(1, 2, 6, 4)), r.normal(size=(1, 2, 6, 4))
+    g = r.normal(size=(1, 2, 6, 4))
+    for causal in (False, True):
+        _, dk, _ = oracle.attention_bwd(q, k, v, g, causal, 0.9)
+        np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
