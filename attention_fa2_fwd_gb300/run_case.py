@@ -3,6 +3,7 @@
     python -m attention_fa2_fwd_gb300.run_case prefill [--B 2 --Hq 32 --Hkv 8 --N 8192 --D 128 --causal 1]
     python -m attention_fa2_fwd_gb300.run_case decode  [--B 64 --Hq 32 --Hkv 8 --L 8192 --D 128]
     python -m attention_fa2_fwd_gb300.run_case decode_paged [--page-size 16 --ragged 1 ...]
+    python -m attention_fa2_fwd_gb300.run_case bwd     [prefill sizes; FLOPs counted as 2.5 x the forward]
 
 Inputs are seeded N(0,1) bf16 tensors drawn on the device.  Each iteration is
 timed with CUDA events on the launching stream (L2 flushed by a 256 MiB write
@@ -21,7 +22,7 @@ import attention_fa2_fwd_gb300 as A
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=("prefill", "decode", "decode_paged"))
+    ap.add_argument("kind", choices=("prefill", "decode", "decode_paged", "bwd"))
     ap.add_argument("--B", type=int)
     ap.add_argument("--Hq", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=8)
@@ -52,6 +53,19 @@ def main():
 
         def call():
             A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse)
+        unit, scale = "TFLOPS", 1e12
+    elif a.kind == "bwd":
+        B = a.B or 2
+        q, k, v = randn(B, a.Hq, a.N, a.D), randn(B, a.Hkv, a.N, a.D), randn(B, a.Hkv, a.N, a.D)
+        dout = randn(B, a.Hq, a.N, a.D)
+        o, lse = A.prefill(q, k, v, causal=bool(a.causal))
+        nbytes = A.attn_bwd_workspace_size(B, a.Hq, a.N)
+        ws = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=dev)
+        # five matrix products of the forward's size (S, dP, dV, dK, dQ): 2.5 x its FLOPs
+        work = 2.5 * 4.0 * B * a.Hq * a.N * a.N * a.D / (2 if a.causal else 1)
+
+        def call():
+            A.backward(q, k, v, o, lse, dout, causal=bool(a.causal), workspace=ws)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "decode_paged":
         B = a.B or 64
