@@ -34,7 +34,8 @@ ATTN_F16 = 0
 ATTN_BF16 = 1
 
 # Every function that include/attn.h declares.
-EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_varlen", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
+EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_ex", "attn_fwd_prefill_varlen", "attn_fwd_prefill_varlen_ex",
+           "attn_fwd_decode_ex", "attn_fwd_decode_paged_ex", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
            "attn_fwd_decode_noalloc", "kv_cache_write", "attn_fwd_decode_paged", "kv_cache_write_paged",
            "attn_bwd_workspace_size", "attn_bwd",
            "attn_get_device_error", "attn_status_string", "attn_version")
@@ -48,6 +49,12 @@ class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where}: {attn_status_string(status)} ({status})")
+
+
+class AttnOptions(ctypes.Structure):
+    """attn_options_t: sliding-window bounds (-1: none) and ALiBi slopes (device fp32 pointer or None)."""
+    _fields_ = [("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
+                ("alibi_slopes", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -73,6 +80,20 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_prefill_varlen.restype = i32
             L.attn_fwd_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, i32,
                                                   i32, i32, i64p, i64p, i64p, i64p, i32, f32, vp]
+            optp = ctypes.POINTER(AttnOptions)
+            L.attn_fwd_prefill_ex.restype = i32
+            L.attn_fwd_prefill_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                              i64p, i64p, i64p, i64p, i32, f32, optp, vp]
+            L.attn_fwd_prefill_varlen_ex.restype = i32
+            L.attn_fwd_prefill_varlen_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, i32, i32,
+                                                     i32, i32, i64p, i64p, i64p, i64p, i32, f32, optp, vp]
+            L.attn_fwd_decode_ex.restype = i32
+            L.attn_fwd_decode_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                             i64p, i64p, i64p, i64p, f32, vp, ctypes.c_size_t, optp, vp]
+            L.attn_fwd_decode_paged_ex.restype = i32
+            L.attn_fwd_decode_paged_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                                   vp, i32, ctypes.c_int64, vp, i32, i64p, i64p, i64p, i64p, f32, vp,
+                                                   ctypes.c_size_t, optp, vp]
             L.attn_decode_workspace_size.restype = ctypes.c_size_t
             L.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
             L.attn_decode_splits.restype = i32
@@ -120,6 +141,54 @@ def attn_fwd_prefill(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, 
     return lib().attn_fwd_prefill(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, _strides(q_str),
                                   _strides(k_str), _strides(v_str), _strides(o_str), int(causal), float(scale),
                                   stream)
+
+
+def _opts(opts):
+    return ctypes.byref(opts) if opts is not None else None
+
+
+def attn_fwd_prefill_ex(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, k_str, v_str, o_str,
+                        causal, scale, opts, stream) -> int:
+    return lib().attn_fwd_prefill_ex(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, _strides(q_str),
+                                     _strides(k_str), _strides(v_str), _strides(o_str), int(causal), float(scale),
+                                     _opts(opts), stream)
+
+
+def attn_fwd_prefill_varlen_ex(q, k, v, o, lse, dtype, B, H_q, H_kv, D, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                               max_seqlen_k, total_q, total_k, q_str, k_str, v_str, o_str, causal, scale, opts,
+                               stream) -> int:
+    s3 = ctypes.c_int64 * 3
+    return lib().attn_fwd_prefill_varlen_ex(q, k, v, o, lse, dtype, B, H_q, H_kv, D, cu_seqlens_q, cu_seqlens_k,
+                                            max_seqlen_q, max_seqlen_k, total_q, total_k, s3(*q_str), s3(*k_str),
+                                            s3(*v_str), s3(*o_str), int(causal), float(scale), _opts(opts), stream)
+
+
+def attn_fwd_decode_ex(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, q_str, kc_str, vc_str, o_str,
+                       scale, workspace, workspace_bytes, opts, stream) -> int:
+    return lib().attn_fwd_decode_ex(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D,
+                                    _strides(q_str), _strides(kc_str), _strides(vc_str), _strides(o_str),
+                                    float(scale), workspace, workspace_bytes, _opts(opts), stream)
+
+
+def attn_fwd_decode_paged_ex(q, k_pages, v_pages, o, lse, dtype, B, H_q, H_kv, D, num_pages, page_size, block_table,
+                             max_pages, bt_stride, cache_lens, max_cache_len, q_str, kp_str, vp_str, o_str, scale,
+                             workspace, workspace_bytes, opts, stream) -> int:
+    return lib().attn_fwd_decode_paged_ex(q, k_pages, v_pages, o, lse, dtype, B, H_q, H_kv, D, num_pages,
+                                          page_size, block_table, max_pages, bt_stride, cache_lens, max_cache_len,
+                                          _strides(q_str), _strides(kp_str), _strides(vp_str), _strides(o_str),
+                                          float(scale), workspace, workspace_bytes, _opts(opts), stream)
+
+
+def make_options(window_left: int = -1, window_right: int = -1, alibi_slopes=None):
+    """An AttnOptions for the *_ex calls (None when nothing is set); alibi_slopes: fp32 CUDA tensor (H_q)."""
+    if window_left == -1 and window_right == -1 and alibi_slopes is None:
+        return None
+    if alibi_slopes is not None:
+        import torch
+        if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda:
+            raise TypeError("alibi_slopes must be an fp32 CUDA tensor")
+    return AttnOptions(int(window_left), int(window_right),
+                       alibi_slopes.data_ptr() if alibi_slopes is not None else None)
 
 
 def attn_fwd_prefill_varlen(q, k, v, o, lse, dtype, B, H_q, H_kv, D, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
@@ -229,7 +298,7 @@ def _check(status: int, where: str):
 
 
 def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_lse: bool = True, out=None,
-            lse_out=None, stream=None):
+            lse_out=None, stream=None, window=(-1, -1), alibi_slopes=None):
     """Fused attention forward.  q (B,H_q,N_q,D); k, v (B,H_kv,N_kv,D) CUDA tensors.
 
     Any (b, h, n) strides are accepted (16-byte multiples, d stride 1), so a
@@ -246,17 +315,17 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_ls
     lse = None
     if return_lse:
         lse = lse_out if lse_out is not None else torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
-    st = attn_fwd_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                          lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D,
-                          q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
-                          _stream_handle(stream))
+    st = attn_fwd_prefill_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D,
+                             q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
+                             make_options(window[0], window[1], alibi_slopes), _stream_handle(stream))
     _check(st, "attn_fwd_prefill")
     return o, lse
 
 
 def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                    causal: bool = False, scale: float | None = None, return_lse: bool = True, out=None,
-                   lse_out=None, stream=None):
+                   lse_out=None, stream=None, window=(-1, -1), alibi_slopes=None):
     """Attention over packed sequences of different lengths.
 
     q (total_q, H_q, D); k, v (total_k, H_kv, D); cu_seqlens_q / cu_seqlens_k int32 CUDA tensors (B + 1).
@@ -274,11 +343,11 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_s
     lse = None
     if return_lse:
         lse = lse_out if lse_out is not None else torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
-    st = attn_fwd_prefill_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                 lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, D,
-                                 cq.data_ptr(), ck.data_ptr(), int(max_seqlen_q), int(max_seqlen_k), total_q, total_k,
-                                 q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
-                                 _stream_handle(stream))
+    st = attn_fwd_prefill_varlen_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, D,
+                                    cq.data_ptr(), ck.data_ptr(), int(max_seqlen_q), int(max_seqlen_k), total_q,
+                                    total_k, q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
+                                    make_options(window[0], window[1], alibi_slopes), _stream_handle(stream))
     _check(st, "attn_fwd_prefill_varlen")
     return o, lse
 
@@ -318,7 +387,7 @@ def decode_workspace(B, H_q, H_kv, D, device=None):
 
 
 def decode(q, k_cache, v_cache, cache_len: int, scale: float | None = None, return_lse: bool = True, out=None,
-           lse_out=None, workspace=None, stream=None):
+           lse_out=None, workspace=None, stream=None, window_left: int = -1, alibi_slopes=None):
     """One query token per (batch, q-head) over the first cache_len cache rows.
 
     q (B,H_q,D) or (B,H_q,1,D); caches (B,H_kv,max_len,D).  Returns (O (B,H_q,D), LSE (B,H_q)).
@@ -338,10 +407,10 @@ def decode(q, k_cache, v_cache, cache_len: int, scale: float | None = None, retu
         workspace = decode_workspace(B, Hq, Hkv, D, q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = attn_fwd_decode(q4.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o4.data_ptr(),
-                         lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, int(cache_len), D,
-                         q4.stride(), k_cache.stride(), v_cache.stride(), o4.stride(), scale, ws_ptr, ws_bytes,
-                         _stream_handle(stream))
+    st = attn_fwd_decode_ex(q4.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o4.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, int(cache_len), D,
+                            q4.stride(), k_cache.stride(), v_cache.stride(), o4.stride(), scale, ws_ptr, ws_bytes,
+                            make_options(window_left, -1, alibi_slopes), _stream_handle(stream))
     _check(st, "attn_fwd_decode")
     return o, lse
 
@@ -364,7 +433,8 @@ def _int32_cuda(t, name):
 
 
 def decode_paged(q, k_pages, v_pages, block_table, cache_lens, max_cache_len: int, scale: float | None = None,
-                 return_lse: bool = True, out=None, lse_out=None, workspace=None, stream=None):
+                 return_lse: bool = True, out=None, lse_out=None, workspace=None, stream=None,
+                 window_left: int = -1, alibi_slopes=None):
     """Decode over paged caches with per-request lengths.
 
     q (B,H_q,D); k_pages, v_pages (num_pages,H_kv,page_size,D); block_table int32 (B,max_pages) and
@@ -388,11 +458,12 @@ def decode_paged(q, k_pages, v_pages, block_table, cache_lens, max_cache_len: in
         workspace = decode_workspace(B, Hq, Hkv, D, q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = attn_fwd_decode_paged(q4.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o4.data_ptr(),
-                               lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, D,
-                               num_pages, page_size, bt.data_ptr(), bt.shape[1], bt.stride(0), cl.data_ptr(),
-                               int(max_cache_len), q4.stride(), k_pages.stride(), v_pages.stride(), o4.stride(),
-                               scale, ws_ptr, ws_bytes, _stream_handle(stream))
+    st = attn_fwd_decode_paged_ex(q4.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o4.data_ptr(),
+                                  lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, D,
+                                  num_pages, page_size, bt.data_ptr(), bt.shape[1], bt.stride(0), cl.data_ptr(),
+                                  int(max_cache_len), q4.stride(), k_pages.stride(), v_pages.stride(), o4.stride(),
+                                  scale, ws_ptr, ws_bytes, make_options(window_left, -1, alibi_slopes),
+                                  _stream_handle(stream))
     _check(st, "attn_fwd_decode_paged")
     return o, lse
 

@@ -177,6 +177,34 @@ size_t decode_ws_bytes(int B, int H_q, int D, int splits) {
 
 bool valid_dtype(attn_dtype_t dt) { return dt == ATTN_F16 || dt == ATTN_BF16; }
 
+// Mask and bias options (NULL: none).
+attn_status_t read_options(const attn_options_t *opts, int *wl, int *wr, const float **slopes) {
+  *wl = -1;
+  *wr = -1;
+  *slopes = nullptr;
+  if (opts == nullptr) return ATTN_OK;
+  if (opts->window_left < -1 || opts->window_right < -1) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(opts->alibi_slopes) & 3) != 0) return ATTN_ERR_ALIGNMENT;
+  *wl = opts->window_left;
+  *wr = opts->window_right;
+  *slopes = opts->alibi_slopes;
+  return ATTN_OK;
+}
+
+// Whether a prefill needs the masked kernel build: a left window, a right
+// window that the causal mask does not already imply, or ALiBi slopes.
+bool prefill_masked(const PrefillParams &p, bool causal) {
+  return p.window_left >= 0 || (!causal && p.window_right >= 0) || p.alibi_slopes != nullptr;
+}
+
+// Keys decode streams for a cache of `len` rows under a left window: the
+// window plus the rounding of its start down to a whole stage.
+int decode_span(int len, int wl) {
+  if (wl < 0) return len;
+  const int64_t span = static_cast<int64_t>(wl) + kDecodeStageTokens;
+  return static_cast<int>(span < len ? span : len);
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -188,6 +216,15 @@ attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void
                                int B, int H_q, int H_kv, int N_q, int N_kv, int D, const int64_t q_str[4],
                                const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4], int causal,
                                float scale, void *stream) {
+  return attn_fwd_prefill_ex(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, k_str, v_str, o_str, causal,
+                             scale, nullptr, stream);
+}
+
+attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  attn_dtype_t dtype, int B, int H_q, int H_kv, int N_q, int N_kv, int D,
+                                  const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                                  const int64_t o_str[4], int causal, float scale, const attn_options_t *opts,
+                                  void *stream) {
   if (!q || !k || !v || !o || !q_str || !k_str || !v_str || !o_str) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H_q < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
   if (H_q % H_kv != 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
@@ -202,11 +239,12 @@ attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void
       (st = check_strides(o_str, qsz)))
     return st;
 
+  PrefillParams p{};
+  if ((st = read_options(opts, &p.window_left, &p.window_right, &p.alibi_slopes)) != ATTN_OK) return st;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
   const bool bf16 = dtype == ATTN_BF16;
   CUtensorMap tq, tk, tv;
-  PrefillParams p{};
   if ((st = make_map(&tq, q, bf16, qsz, q_str, kPrefillBM, &p.slots_q)) ||
       (st = make_map(&tk, k, bf16, kvsz, k_str, kPrefillBN, &p.slots_k)) ||
       (st = make_map(&tv, v, bf16, kvsz, v_str, kPrefillBN, &p.slots_v)))
@@ -223,7 +261,8 @@ attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void
   p.group = H_q / H_kv;
   p.n_qtiles = (N_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  cudaError_t e = launch_prefill(D, causal != 0, bf16, false, tq, tk, tv, p, B, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_prefill(D, causal != 0, bf16, false, prefill_masked(p, causal != 0), tq, tk, tv, p, B,
+                                 static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -233,6 +272,17 @@ attn_status_t attn_fwd_prefill_varlen(const void *q, const void *k, const void *
                                       int total_k, const int64_t q_str[3], const int64_t k_str[3],
                                       const int64_t v_str[3], const int64_t o_str[3], int causal, float scale,
                                       void *stream) {
+  return attn_fwd_prefill_varlen_ex(q, k, v, o, lse, dtype, B, H_q, H_kv, D, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                                    max_seqlen_k, total_q, total_k, q_str, k_str, v_str, o_str, causal, scale, nullptr,
+                                    stream);
+}
+
+attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                                         attn_dtype_t dtype, int B, int H_q, int H_kv, int D,
+                                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int max_seqlen_q,
+                                         int max_seqlen_k, int total_q, int total_k, const int64_t q_str[3],
+                                         const int64_t k_str[3], const int64_t v_str[3], const int64_t o_str[3],
+                                         int causal, float scale, const attn_options_t *opts, void *stream) {
   if (!q || !k || !v || !o || !cu_seqlens_q || !cu_seqlens_k || !q_str || !k_str || !v_str || !o_str)
     return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H_q < 1 || H_kv < 1 || D < 1 || max_seqlen_q < 1 || max_seqlen_k < 1 || total_q < 1 || total_k < 1)
@@ -253,11 +303,12 @@ attn_status_t attn_fwd_prefill_varlen(const void *q, const void *k, const void *
   if ((st = check_strides(q4, qsz)) || (st = check_strides(k4, kvsz)) || (st = check_strides(v4, kvsz)) ||
       (st = check_strides(o4, qsz)))
     return st;
+  PrefillParams p{};
+  if ((st = read_options(opts, &p.window_left, &p.window_right, &p.alibi_slopes)) != ATTN_OK) return st;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
   const bool bf16 = dtype == ATTN_BF16;
   CUtensorMap tq, tk, tv;
-  PrefillParams p{};
   if ((st = make_map(&tq, q, bf16, qsz, q4, kPrefillBM, &p.slots_q)) ||
       (st = make_map(&tk, k, bf16, kvsz, k4, kPrefillBN, &p.slots_k)) ||
       (st = make_map(&tv, v, bf16, kvsz, v4, kPrefillBN, &p.slots_v)))
@@ -278,7 +329,8 @@ attn_status_t attn_fwd_prefill_varlen(const void *q, const void *k, const void *
   p.cu_k = cu_seqlens_k;
   p.total_q = total_q;
   p.total_k = total_k;
-  cudaError_t e = launch_prefill(D, causal != 0, bf16, true, tq, tk, tv, p, B, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_prefill(D, causal != 0, bf16, true, prefill_masked(p, causal != 0), tq, tk, tv, p, B,
+                                 static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -376,6 +428,15 @@ attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_
                               const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
                               const int64_t o_str[4], float scale, void *workspace, size_t workspace_bytes,
                               void *stream) {
+  return attn_fwd_decode_ex(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, q_str, kc_str, vc_str,
+                            o_str, scale, workspace, workspace_bytes, nullptr, stream);
+}
+
+attn_status_t attn_fwd_decode_ex(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                                 attn_dtype_t dtype, int B, int H_q, int H_kv, int cache_len, int D,
+                                 const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
+                                 const int64_t o_str[4], float scale, void *workspace, size_t workspace_bytes,
+                                 const attn_options_t *opts, void *stream) {
   if (!q || !k_cache || !v_cache || !o || !q_str || !kc_str || !vc_str || !o_str) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H_q < 1 || H_kv < 1 || cache_len < 1 || D < 1 || H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f) || B > 65535) return ATTN_ERR_INVALID_ARG;
@@ -388,6 +449,9 @@ attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_
   if ((st = check_strides(q_str, qsz)) || (st = check_strides(kc_str, csz)) || (st = check_strides(vc_str, csz)) ||
       (st = check_strides(o_str, qsz)))
     return st;
+  int wl, wr;
+  const float *slopes;
+  if ((st = read_options(opts, &wl, &wr, &slopes)) != ATTN_OK) return st;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
 
@@ -395,7 +459,7 @@ attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_
   const int gh = decode_heads_per_cta(group);
   const int nhc = (group + gh - 1) / gh;
   int nsplit = 1, chunk = cache_len;
-  decode_plan(B, H_q, H_kv, cache_len, D, dev->sm_count, &nsplit, &chunk);
+  decode_plan(B, H_q, H_kv, decode_span(cache_len, wl), D, dev->sm_count, &nsplit, &chunk);
   if (nsplit > 1) {
     const size_t need = decode_ws_bytes(B, H_q, D, nsplit);
     if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
@@ -427,6 +491,8 @@ attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_
   p.chunk = chunk;
   p.nsplit = nsplit;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.window_left = wl;
+  p.alibi_slopes = slopes;
   if (static_cast<int64_t>(H_kv) * nhc > 65535) return ATTN_ERR_INVALID_ARG;
   // Tensor maps over the valid rows only: rows >= cache_len read as zeros.
   CUtensorMap tk, tv;
@@ -498,6 +564,18 @@ attn_status_t attn_fwd_decode_paged(const void *q, const void *k_pages, const vo
                                     const int32_t *cache_lens, int max_cache_len, const int64_t q_str[4],
                                     const int64_t kp_str[4], const int64_t vp_str[4], const int64_t o_str[4],
                                     float scale, void *workspace, size_t workspace_bytes, void *stream) {
+  return attn_fwd_decode_paged_ex(q, k_pages, v_pages, o, lse, dtype, B, H_q, H_kv, D, num_pages, page_size,
+                                  block_table, max_pages, bt_stride, cache_lens, max_cache_len, q_str, kp_str, vp_str,
+                                  o_str, scale, workspace, workspace_bytes, nullptr, stream);
+}
+
+attn_status_t attn_fwd_decode_paged_ex(const void *q, const void *k_pages, const void *v_pages, void *o, float *lse,
+                                       attn_dtype_t dtype, int B, int H_q, int H_kv, int D, int num_pages,
+                                       int page_size, const int32_t *block_table, int max_pages, int64_t bt_stride,
+                                       const int32_t *cache_lens, int max_cache_len, const int64_t q_str[4],
+                                       const int64_t kp_str[4], const int64_t vp_str[4], const int64_t o_str[4],
+                                       float scale, void *workspace, size_t workspace_bytes,
+                                       const attn_options_t *opts, void *stream) {
   if (!q || !k_pages || !v_pages || !o || !cache_lens || !q_str || !kp_str || !vp_str || !o_str)
     return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H_q < 1 || H_kv < 1 || D < 1 || H_q % H_kv != 0 || max_cache_len < 1) return ATTN_ERR_INVALID_ARG;
@@ -513,6 +591,9 @@ attn_status_t attn_fwd_decode_paged(const void *q, const void *k_pages, const vo
   if ((st = check_strides(q_str, qsz)) || (st = check_strides(kp_str, psz)) || (st = check_strides(vp_str, psz)) ||
       (st = check_strides(o_str, qsz)))
     return st;
+  int wl, wr;
+  const float *slopes;
+  if ((st = read_options(opts, &wl, &wr, &slopes)) != ATTN_OK) return st;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
 
@@ -520,7 +601,7 @@ attn_status_t attn_fwd_decode_paged(const void *q, const void *k_pages, const vo
   const int gh = decode_heads_per_cta(group);
   const int nhc = (group + gh - 1) / gh;
   int nsplit = 1, chunk = max_cache_len;
-  decode_plan(B, H_q, H_kv, max_cache_len, D, dev->sm_count, &nsplit, &chunk);
+  decode_plan(B, H_q, H_kv, decode_span(max_cache_len, wl), D, dev->sm_count, &nsplit, &chunk);
   if (nsplit > 1) {
     const size_t need = decode_ws_bytes(B, H_q, D, nsplit);
     if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
@@ -553,6 +634,8 @@ attn_status_t attn_fwd_decode_paged(const void *q, const void *k_pages, const vo
   p.page_size = page_size;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
+  p.window_left = wl;
+  p.alibi_slopes = slopes;
   // Tensor maps over the page pool: (d, row in page, kv head, page).
   CUtensorMap tk, tv;
   const bool bf16 = dtype == ATTN_BF16;

@@ -33,6 +33,11 @@ struct PrefillParams {
   // then are the host's bounds on the per-sequence lengths; LSE is (H_q, total_q).
   const int32_t *cu_q, *cu_k;
   int total_q, total_k;
+  // Mask and bias options: key j is kept for query i only if
+  // i - window_left <= j <= i + window_right (-1: no bound on that side);
+  // alibi_slopes (device fp32, one per q head) adds -slope_h |i - j| to scores.
+  int window_left, window_right;
+  const float *alibi_slopes;
 };
 
 struct DecodeParams {
@@ -53,6 +58,10 @@ struct DecodeParams {
   const int32_t *cache_lens;   // (B) tokens per request
   int64_t bt_stride;
   int page_size, max_pages, num_pages;
+  // Mask and bias options: only keys j >= len - 1 - window_left are attended
+  // (window_left < 0: all); alibi_slopes adds -slope_h (len - 1 - j).
+  int window_left;
+  const float *alibi_slopes;
 };
 
 struct KvWriteParams {
@@ -72,8 +81,14 @@ struct KvWriteParams {
 };
 
 // Launchers (return cudaSuccess or the launch error).
-cudaError_t launch_prefill(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq, const CUtensorMap &tk,
-                           const CUtensorMap &tv, const PrefillParams &p, int B, cudaStream_t stream);
+// masked: a window bound or ALiBi slopes are set (a separate kernel build, so
+// that the plain kernel keeps its short softmax loop).
+cudaError_t launch_prefill(int D, bool causal, bool bf16, bool varlen, bool masked, const CUtensorMap &tq,
+                           const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
+                           cudaStream_t stream);
+cudaError_t launch_prefill_masked(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq,
+                                  const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
+                                  cudaStream_t stream);
 
 // Decode: heads served by one CTA, and launch (split kernel, plus the merge
 // kernel when nsplit > 1).

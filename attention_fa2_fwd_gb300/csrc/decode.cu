@@ -155,7 +155,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       len = len < 0 ? 0 : p.cache_len;
     }
   }
-  const int t_begin = split * p.chunk;
+  // Sliding window: only keys t >= t_lo are attended; the splits tile the
+  // range from t_lo rounded down to a whole stage (so that paged boxes stay
+  // inside their pages), and keys below t_lo are masked.
+  const int t_lo = p.window_left >= 0 ? max(0, len - 1 - p.window_left) : 0;
+  const int t_begin = (t_lo / kTok) * kTok + split * p.chunk;
   const int t_end = min(t_begin + p.chunk, len);
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTok - 1) / kTok : 0;
 
@@ -254,6 +258,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int sub = lane % C::CPR;      // 16-byte slice of D for P . V
     float m[GH];
     float lpart[GH];
+    float slope2[GH];  // ALiBi slope of each head, base-2 units (0 without ALiBi)
+#pragma unroll
+    for (int i = 0; i < GH; ++i)
+      slope2[i] = (p.alibi_slopes != nullptr && i < nh) ? p.alibi_slopes[h_first + i] * 1.4426950408889634f : 0.f;
     uint64_t acc[GH][4];
 #pragma unroll
     for (int i = 0; i < GH; ++i) {
@@ -291,14 +299,16 @@ __global__ void __launch_bounds__(kThreads, 2)
           s2[i] = ffma2(qb.y, k67, s2[i]);
         }
       }
-      const bool valid = t_begin + j * kTok + row < t_end;
+      const int tok = t_begin + j * kTok + row;
+      const bool valid = tok < t_end && tok >= t_lo;
+      const float dist = static_cast<float>(len - 1 - tok);  // query position minus key position
       float s[GH];
 #pragma unroll
       for (int i = 0; i < GH; ++i) {
         const float2 v = unf2(s2[i]);
         float x = v.x + v.y;
         x += __shfl_xor_sync(0xffffffffu, x, 16);
-        s[i] = valid ? x : -INFINITY;
+        s[i] = valid ? fmaf(-slope2[i], dist, x) : -INFINITY;
       }
       // online softmax over this warp's 16 tokens (both halves hold the same scores)
       float pr[GH];

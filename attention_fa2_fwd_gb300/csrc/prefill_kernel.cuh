@@ -1,0 +1,614 @@
+// prefill_kernel.cuh -- fused attention forward (prefill) kernel for sm_103a.
+//
+// Included by prefill.cu (plain causal / full masks) and prefill_masked.cu
+// (sliding windows and ALiBi), which instantiate it with MASKED false / true
+// in separate translation units compiled in parallel.
+//
+// One CTA computes TWO 128-row query tiles (rows q0..q0+255) of one
+// (batch, q-head), so the tensor core always has one tile's matrix products
+// to run while the other tile's softmax is computed:
+//   warps 0-3   softmax warpgroup of tile 0, one thread per query row (TMEM lane)
+//   warps 4-7   softmax warpgroup of tile 1
+//   warp 8      TMA producer: both Q tiles once, then K and V tiles of 128 keys
+//               into a ring of shared-memory stages (128-byte swizzle)
+//   warp 9      TMEM allocator and tcgen05 MMA issuer (one thread), per KV tile j:
+//                 S0_j = Q0 K_j^T;  O1 += P1_{j-1} V_{j-1};  S1_j = Q1 K_j^T;  O0 += P0_j V_j
+//               (SS form for Q K^T, TS form with P read from TMEM for P V)
+//   warps 10-11 idle (they complete the register split of their warpgroup)
+//
+// The algorithm is the online softmax of "Skill: Write a Triton Attention
+// Kernel" (Required reasoning process, steps 4-9): running max m and sum l in
+// fp32, O and l rescaled by alpha = exp(m_old - m_new) before a block is
+// added, O / l once after the loop, lse = m + ln l.  Details of this kernel:
+//   * scores are kept in base-2 units (scale * log2 e folded into one FMA), so
+//     the exponential is one ex2; the LSE is converted back on store;
+//   * the running max of a row is only raised when the block max exceeds it
+//     by more than 8 (base 2).  P = 2^(s - m) then stays below 2^8, the rescale
+//     of O (TMEM load, multiply, store) is skipped for most blocks, and O / l is
+//     unchanged because O and l always share the same m;
+//   * the causal mask (key j kept for query i iff j <= i) and the key-length
+//     mask set scores to -inf before the max; only tiles that straddle the
+//     diagonal or the end of the keys pay for it, and KV tiles past the
+//     diagonal of a query tile are never computed for it;
+//   * P (16-bit) overwrites the first half of its S columns in TMEM; in-order
+//     execution of the MMAs keeps the next S from landing before P V has read P,
+//     and makes P_i(j-1) V_{j-1} complete before S_i(j) is signalled, so the
+//     softmax warpgroup may rescale O_i as soon as it sees S_i(j).
+//
+// TMEM columns (512): S0/P0 [0,128) S1/P1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = kPrefillBM;  // rows per query tile
+constexpr int kBN = kPrefillBN;  // keys per KV tile
+constexpr int kThreads = 384;
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleThreshold = 8.0f;  // base-2 units
+constexpr int kSoftmaxRegs = 208;
+constexpr int kUnlimited = 0x3fffffff;  // "no window bound" (large, yet safe to add small offsets to)
+constexpr int kOtherRegs = 88;
+
+template <int D>
+struct Cfg {
+  static constexpr int KCH = D / 64;                  // 128-byte chunks along D
+  static constexpr int ST = (D == 128) ? 2 : 3;       // K/V pipeline stages
+  static constexpr uint32_t CHUNK_Q = kBM * 128;      // bytes of one 64-column chunk of a Q tile
+  static constexpr uint32_t CHUNK_KV = kBN * 128;
+  static constexpr uint32_t QT_BYTES = kBM * D * 2;   // one Q tile
+  static constexpr uint32_t KV_BYTES = kBN * D * 2;
+  // TMEM column of S_t / P_t and of O_t for query tile t
+  static __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(t) * 128u; }
+  static __device__ __forceinline__ uint32_t o_col(int t) { return 256u + static_cast<uint32_t>(t) * D; }
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * QT_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + ST * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + ST * KV_BYTES;
+  // barrier indices
+  static constexpr int B_Q = 0;
+  static constexpr int B_KF = 1;            // + stage
+  static constexpr int B_KE = 1 + ST;       // + stage
+  static constexpr int B_VF = 1 + 2 * ST;   // + stage
+  static constexpr int B_VE = 1 + 3 * ST;   // + stage
+  static constexpr int B_SF = 1 + 4 * ST;   // + tile (2): S_i(j) computed
+  static constexpr int B_PF = 3 + 4 * ST;   // + tile (2): P_i(j) stored (and O_i rescaled)
+  static constexpr int B_OD = 5 + 4 * ST;   // + tile (2): last P_i V done
+  static constexpr int B_DONE = 7 + 4 * ST; // every MMA completed
+  static constexpr int B_VZ = 8 + 4 * ST;   // variable length: V rows past the sequence zeroed
+  static constexpr int B_VT = 9 + 4 * ST;   // variable length: the tail V tile has landed
+  static constexpr int NBAR = 10 + 4 * ST;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+  // + slack for 1024-byte alignment; at least 116 KB so that only one CTA (which
+  // holds all 512 TMEM columns) is resident per SM.
+  static constexpr uint32_t SMEM_BYTES = (SMEM_USED + 1024 > 116u * 1024) ? SMEM_USED + 1024 : 116u * 1024;
+  static_assert(256 + 2 * D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 227u * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, int d, int n, int h, int b,
+                                         uint32_t slots, uint32_t bar) {
+  const int sn = slots & 3, sh = (slots >> 2) & 3;
+  const int c1 = (sn == 1) ? n : (sh == 1) ? h : b;
+  const int c2 = (sn == 2) ? n : (sh == 2) ? h : b;
+  const int c3 = (sn == 3) ? n : (sh == 3) ? h : b;
+  tma_load_4d(dst, map, d, c1, c2, c3, bar);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// VARLEN: the batch is packed; sequence b's rows are found through cu_q / cu_k
+// (see PrefillParams), tensor maps span the packed tensors, and the last V tile
+// of a sequence -- whose tail rows belong to the next sequence -- gets those
+// rows zeroed by warp 10 before P V reads it, so nothing from another sequence
+// (not even a non-finite value times a zero weight) reaches the result.
+template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+  using C = Cfg<D>;
+  constexpr int ST = C::ST;
+  extern __shared__ uint8_t smem_raw[];
+
+  if (load_volatile(p.err) != 0) return;  // an earlier launch failed; nothing runs until it is read
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (sbase - raw);
+  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / p.group;
+  const int q0 = pair * 2 * kBM;  // first row of tile 0; tile 1 starts at q0 + 128
+  int q_base = 0, k_base = 0, Nq = p.Nq, Nkv = p.Nkv, bc = b;  // bc: batch coordinate of the tensor maps
+  if constexpr (VARLEN) {
+    const int qs = p.cu_q[b], qe = p.cu_q[b + 1], ks = p.cu_k[b], ke = p.cu_k[b + 1];
+    if (qs < 0 || qe < qs || qe > p.total_q || qe - qs > p.Nq || ks < 0 || ke < ks || ke > p.total_k ||
+        ke - ks > p.Nkv) {
+      if (threadIdx.x == 0) atomicOr(p.err, kErrBadIndex);
+      return;
+    }
+    q_base = qs;
+    k_base = ks;
+    Nq = qe - qs;
+    Nkv = ke - ks;
+    bc = 0;
+    if (q0 >= Nq) return;
+    if (Nkv == 0) {
+      // No keys: O = 0 and LSE = -inf for this pair's rows.
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      for (int r = threadIdx.x; r < 2 * kBM; r += kThreads) {
+        if (q0 + r >= Nq) break;
+        T *orow = reinterpret_cast<T *>(p.o) + static_cast<int64_t>(h) * p.o_sh +
+                  static_cast<int64_t>(q_base + q0 + r) * p.o_sn;
+        for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4 *>(orow + d) = make_uint4(0, 0, 0, 0);
+        if (p.lse != nullptr) p.lse[static_cast<int64_t>(h) * p.total_q + q_base + q0 + r] = -INFINITY;
+      }
+      return;
+    }
+  }
+  const int nkv_all = (Nkv + kBN - 1) / kBN;
+  // Key band of a query row i: i - win_l <= j <= i + win_r (kUnlimited: no
+  // bound on that side); causal fixes win_r at 0.  Query tile t needs KV tiles
+  // [lo_t, hi_t); tiles outside the band are never loaded or computed.
+  // Without MASKED both bounds are compile-time constants and the band code
+  // folds away (the plain kernel keeps its shorter softmax loop).
+  const int win_l = (!MASKED || p.window_left < 0) ? kUnlimited : p.window_left;
+  const int win_r = CAUSAL ? 0 : ((!MASKED || p.window_right < 0) ? kUnlimited : p.window_right);
+  int lo[2], hi[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qa = q0 + t * kBM;  // first row of the tile
+    const int kmin = win_l == kUnlimited ? 0 : max(0, qa - win_l);
+    const int kmax = win_r == kUnlimited ? Nkv - 1 : min(Nkv - 1, qa + kBM - 1 + win_r);
+    lo[t] = kmin / kBN;
+    hi[t] = kmax < kmin ? lo[t] : kmax / kBN + 1;
+  }
+  const bool has_t0 = lo[0] < hi[0], has_t1 = lo[1] < hi[1];
+  const int J0 = has_t0 ? (has_t1 ? min(lo[0], lo[1]) : lo[0]) : (has_t1 ? lo[1] : 0);
+  const int J1 = has_t0 ? (has_t1 ? max(hi[0], hi[1]) : hi[0]) : (has_t1 ? hi[1] : 0);
+  // Variable length: the last KV tile runs past the sequence and is used here.
+  const int j_tail = nkv_all - 1;
+  const bool zero_v = VARLEN && (Nkv % kBN) != 0 && J1 == nkv_all && J0 <= j_tail;
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(C::B_Q), 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(BAR(C::B_KF + s), 1);
+      mbar_init(BAR(C::B_KE + s), 1);
+      mbar_init(BAR(C::B_VF + s), 1);
+      mbar_init(BAR(C::B_VE + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(C::B_SF + i), 1);
+      mbar_init(BAR(C::B_PF + i), 4);  // one arrival per softmax warp
+      mbar_init(BAR(C::B_OD + i), 1);
+    }
+    mbar_init(BAR(C::B_DONE), 1);
+    mbar_init(BAR(C::B_VZ), 1);
+    mbar_init(BAR(C::B_VT), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= 8) {
+    setmaxnreg_dec<kOtherRegs>();
+    if (warp == 8) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        int issued_k = 0, issued_v = 0;
+        bool ok = true;
+        mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QT_BYTES);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+            tma_tile(sQ + t * C::QT_BYTES + c * C::CHUNK_Q, &tmQ, c * 64, q_base + q0 + t * kBM, h, bc, p.slots_q,
+                     BAR(C::B_Q));
+        int st = 0;       // ring stage of KV tile j
+        uint32_t ph = 0;  // its phase
+        for (int j = J0; j < J1; ++j) {
+          const bool reuse = j - J0 >= ST;  // the stage held tile j - ST
+          if (reuse && !(ok = mbar_wait(BAR(C::B_KE + st), ph ^ 1, abort_flag, p.err))) break;
+          mbar_arrive_expect_tx(BAR(C::B_KF + st), C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+            tma_tile(sK + st * C::KV_BYTES + c * C::CHUNK_KV, &tmK, c * 64, k_base + j * kBN, hk, bc, p.slots_k,
+                     BAR(C::B_KF + st));
+          ++issued_k;
+          if (reuse && !(ok = mbar_wait(BAR(C::B_VE + st), ph ^ 1, abort_flag, p.err))) break;
+          mbar_arrive_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+            tma_tile(sV + st * C::KV_BYTES + c * C::CHUNK_KV, &tmV, c * 64, k_base + j * kBN, hk, bc, p.slots_v,
+                     BAR(C::B_VF + st));
+          ++issued_v;
+          if (++st == ST) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) {
+          // Let every copy already issued land before shared memory is released.
+          mbar_wait(BAR(C::B_Q), 0, nullptr, p.err);
+          for (int i = max(0, issued_k - ST); i < issued_k; ++i)
+            mbar_wait(BAR(C::B_KF + i % ST), (i / ST) & 1, nullptr, p.err);
+          for (int i = max(0, issued_v - ST); i < issued_v; ++i)
+            mbar_wait(BAR(C::B_VF + i % ST), (i / ST) & 1, nullptr, p.err);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = idesc_f16(BF16, kBM, kBN, false, false);
+        constexpr uint32_t idesc_pv = idesc_f16(BF16, kBM, D, false, true);
+        // Shared-memory descriptors are formed once; each MMA adds a compile-time
+        // offset (in 16-byte units) to the start-address field.  All operands lie
+        // below 256 KB, so the 14-bit field never carries into the next one.
+        const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024), dq1 = smem_desc_sw128(sQ + C::QT_BYTES, 16, 1024);
+        const uint64_t dk = smem_desc_sw128(sK, 16, 1024), dv = smem_desc_sw128(sV, C::CHUNK_KV, 1024);
+        constexpr uint32_t kStage16 = C::KV_BYTES >> 4;
+        auto issue_s = [&](int t, uint64_t qd, uint64_t kd) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // Q and K are K-major: 16 elements (32 B) per MMA inside a 128-byte swizzle row.
+            mma_ss(tmem + C::s_col(t), qd + (((kk / 4) * C::CHUNK_Q + (kk % 4) * 32) >> 4),
+                   kd + (((kk / 4) * C::CHUNK_KV + (kk % 4) * 32) >> 4), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(BAR(C::B_SF + t));
+        };
+        auto issue_pv = [&](int t, bool first, uint64_t vd) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            // V is MN-major: 16 keys per MMA = 16 rows of 128 B; D in 64-column blocks CHUNK_KV apart.
+            mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc_pv,
+                   (!first || kk > 0) ? 1u : 0u);
+          }
+        };
+        // V of KV tile j (ring stage st, phase ph) has landed (and, for a sequence's
+        // tail tile, been zeroed past the end: this thread, which follows the stage
+        // phases in order, tells warp 10 when the tail tile is in and waits for it
+        // to clear the rows).
+        auto wait_v = [&](int j, int st, uint32_t ph) -> bool {
+          if (!mbar_wait(BAR(C::B_VF + st), ph, abort_flag, p.err)) return false;
+          if (!(zero_v && j == j_tail)) return true;
+          mbar_arrive(BAR(C::B_VT));
+          return mbar_wait(BAR(C::B_VZ), 0, abort_flag, p.err);
+        };
+        // Bands: tile 1 lies at or after tile 0 (lo0 <= lo1, hi0 <= hi1), so the
+        // ring runs from lo0 (or lo1 when tile 0 is empty) to hi1 (or hi0).  The
+        // loop keeps ring stage, phases and first-block flags in registers: this
+        // thread's latency between a barrier and the next MMA is on the critical path.
+        const int lo0 = lo[0], hi0 = hi[0], lo1 = lo[1], hi1 = hi[1];
+        bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, p.err);
+        bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
+        bool h1p = false;       // tile 1 uses KV tile j-1
+        bool first0 = true, first1 = true;
+        uint32_t pf0 = 0, pf1 = 0;  // parities of the P-ready barriers
+        int st = 0, sp = 0;         // ring stages of j and j-1
+        uint32_t ph = 0, pph = 0;   // their phases
+        for (int j = J0; ok && j < J1; ++j) {
+          const bool h0 = j >= lo0 && j < hi0, h1 = j >= lo1 && j < hi1;
+          if (!(ok = mbar_wait(BAR(C::B_KF + st), ph, abort_flag, p.err))) break;
+          tc_fence_after();
+          const uint64_t kd = dk + st * kStage16;
+          if (h0) issue_s(0, dq0, kd);
+          if (h1p) {
+            // O1 += P1_{j-1} V_{j-1}: tile 1 is the last user of V_{j-1}, so its stage is released
+            if (!(ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err))) break;
+            pf1 ^= 1;
+            if (!v_waited && !(ok = wait_v(j - 1, sp, pph))) break;
+            tc_fence_after();
+            issue_pv(1, first1, dv + sp * kStage16);
+            first1 = false;
+            tc_commit(BAR(C::B_VE + sp));
+          }
+          if (h1) issue_s(1, dq1, kd);
+          tc_commit(BAR(C::B_KE + st));  // both S products that read K_j are issued
+          v_waited = false;
+          if (h0) {
+            // O0 += P0_j V_j
+            if (!(ok = mbar_wait(BAR(C::B_PF + 0), pf0, abort_flag, p.err))) break;
+            pf0 ^= 1;
+            if (!(ok = wait_v(j, st, ph))) break;
+            v_waited = true;
+            tc_fence_after();
+            issue_pv(0, first0, dv + st * kStage16);
+            first0 = false;
+            if (!h1) tc_commit(BAR(C::B_VE + st));  // tile 1 does not use V_j
+            if (j == hi0 - 1) tc_commit(BAR(C::B_OD + 0));
+          } else if (!h1) {
+            // A tile between the two bands: nothing reads V_j.  Its copy must land
+            // before the stage is handed back for the next one.
+            if (!(ok = wait_v(j, st, ph))) break;
+            tc_commit(BAR(C::B_VE + st));
+          }
+          h1p = h1;
+          sp = st;
+          pph = ph;
+          if (++st == ST) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (ok && h1p) {
+          // the last P1 V of tile 1 (its band ends the ring)
+          ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err) && (v_waited || wait_v(J1 - 1, sp, pph));
+          if (ok) {
+            tc_fence_after();
+            issue_pv(1, first1, dv + sp * kStage16);
+            tc_commit(BAR(C::B_VE + sp));
+            tc_commit(BAR(C::B_OD + 1));
+          }
+        }
+        // A query tile whose band holds no key: O is never written; the epilogue
+        // stores zeros for it.
+        if (!has_t0) tc_commit(BAR(C::B_OD + 0));
+        if (!has_t1) tc_commit(BAR(C::B_OD + 1));
+        tc_commit(BAR(C::B_DONE));
+        mbar_wait(BAR(C::B_DONE), 0, nullptr, p.err);
+      }
+      __syncwarp();
+    } else if (warp == 10) {
+      // ---------------------------------------------------------- variable length: tail of V
+      if (zero_v) {
+        const int st = (j_tail - J0) % ST;  // ring position of the tail tile
+        const bool landed = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_VT), 0, abort_flag, p.err));
+        if (landed) {
+          const int r0 = Nkv % kBN;  // rows r0..127 of the tile lie past the sequence
+          uint8_t *vt = smem + C::OFF_V + st * C::KV_BYTES;
+          const int pieces = (kBN - r0) * 8;  // 16-byte pieces per 128-byte row chunk
+          for (int c = 0; c < C::KCH; ++c)
+            for (int i = lane; i < pieces; i += 32)
+              *reinterpret_cast<uint4 *>(vt + c * C::CHUNK_KV + (r0 + i / 8) * 128 + (i % 8) * 16) =
+                  make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();  // make the zeros visible to the tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_VZ));
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    setmaxnreg_inc<kSoftmaxRegs>();
+    const int t = warp >> 2;                            // query tile of this warpgroup
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                  // row in the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int q_tile0 = q0 + t * kBM;
+    const int q_row = q_tile0 + r;
+    const float sl2 = p.scale_log2;
+    // ALiBi: score += -slope_h |i - j|, in base-2 units.
+    const bool alibi = MASKED && p.alibi_slopes != nullptr;
+    const float slope2 = alibi ? p.alibi_slopes[h] * 1.4426950408889634f : 0.f;
+    const uint32_t scol = tmem + lane_off + C::s_col(t);
+    const uint32_t ocol = tmem + lane_off + C::o_col(t);
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    // this warp's tile band as scalars (a runtime index into lo/hi would put them in local memory)
+    const int jlo = t == 0 ? lo[0] : lo[1], jhi = t == 0 ? hi[0] : hi[1];
+    for (int j = jlo; j < jhi; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF + t), (j - jlo) & 1, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tmem_ld_32x32b_x32(scol + i * 32, sr[i]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) reg_fence(sr[i]);
+
+      const int kv0 = j * kBN;
+      // Masked only where the tile crosses the end of the keys or a band edge.
+      const bool need_mask = (kv0 + kBN > Nkv) || (win_r != kUnlimited && kv0 + kBN - 1 > q_tile0 + win_r) ||
+                             (win_l != kUnlimited && kv0 < q_tile0 + kBM - 1 - win_l);
+      if (need_mask) {
+        // columns lo_c <= c < hi_c are kept
+        const int hi_c = (win_r == kUnlimited ? Nkv : min(Nkv, q_row + win_r + 1)) - kv0;
+        const int lo_c = win_l == kUnlimited ? 0 : q_row - win_l - kv0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (i * 32 + c >= hi_c || i * 32 + c < lo_c) sr[i][c] = __float_as_uint(-INFINITY);
+      }
+      float sl_eff = sl2;  // factor from the values in sr to base-2 scores
+      if (alibi) {
+        const float dq = static_cast<float>(q_row - kv0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            sr[i][c] = __float_as_uint(
+                fmaf(__uint_as_float(sr[i][c]), sl2, -slope2 * fabsf(dq - static_cast<float>(i * 32 + c))));
+        sl_eff = 1.f;
+      }
+      // Row max: four independent chains of 3-input maxima.
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < 32; c += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            mq[u] = fmax3(mq[u], __uint_as_float(sr[i][c + 2 * u]), __uint_as_float(sr[i][c + 2 * u + 1]));
+      const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+      // Raise the running max only when the block max exceeds it by more than
+      // the threshold; otherwise keep it (alpha = 1, no rescale of O).
+      const float mb = mx * sl_eff;
+      const bool raise = (m == -INFINITY) || (mb > m + kRescaleThreshold);
+      const float m_new = raise ? fmaxf(m, mb) : m;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = raise ? fast_exp2(m - m_use) : 1.f;
+      // P = 2^(s * scale * log2 e - m), two columns per packed FMA; row sum in
+      // four packed partial sums.
+      const uint64_t sl2x2 = pack_f2(sl_eff, sl_eff), negm2 = pack_f2(-m_use, -m_use);
+      uint64_t rs2[4] = {0, 0, 0, 0};
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const uint64_t e2 = ffma_f2(pack_f2(__uint_as_float(sr[i][c]), __uint_as_float(sr[i][c + 1])), sl2x2, negm2);
+          const float2 e = unpack_f2(e2);
+          const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+          rs2[(c >> 1) & 3] = fadd_f2(rs2[(c >> 1) & 3], pack_f2(p0, p1));
+          pk[i >> 1][(i & 1) * 16 + c / 2] = pack2<BF16>(p0, p1);
+        }
+      const float2 r01 = unpack_f2(fadd_f2(rs2[0], rs2[1])), r23 = unpack_f2(fadd_f2(rs2[2], rs2[3]));
+      const float rs = (r01.x + r01.y) + (r23.x + r23.y);
+      l = l * alpha + rs;
+      m = m_new;
+      // P_i(j) over the first 64 columns of S_i (S_i(j) is already in registers).
+      tmem_st_32x32b_x32(scol, pk[0]);
+      tmem_st_32x32b_x32(scol + 32, pk[1]);
+      // P_i(j-1) V_{j-1} completed before S_i(j) was signalled: O_i is stable.
+      if (j > jlo && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(ocol + i * 32, ov);
+          tmem_wait_ld();
+          reg_fence(ov);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st_32x32b_x32(ocol + i * 32, ov);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(C::B_PF + t));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OD + t), 0, abort_flag, p.err));
+    if (ok) {
+      // -------------------------------------------------------- epilogue: O / l, LSE
+      tc_fence_after();
+      // A row whose band holds no key (possible with windows) gets O = 0, LSE = -inf.
+      const bool any_key = l > 0.f;
+      const float inv_l = any_key ? 1.f / l : 0.f;
+      const bool row_ok = q_row < Nq;
+      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+      T *orow = reinterpret_cast<T *>(p.o) + static_cast<int64_t>(bc) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
+                static_cast<int64_t>(q_base + q_row) * p.o_sn;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(ocol + i * 32, ov);
+        tmem_wait_ld();
+        reg_fence(ov);
+        uint32_t packed[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          packed[c / 2] = pack2<BF16>(any_key ? __uint_as_float(ov[c]) * inv_l : 0.f,
+                                      any_key ? __uint_as_float(ov[c + 1]) * inv_l : 0.f);
+        if (row_ok) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + i * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        }
+      }
+      if (p.lse != nullptr && row_ok)
+        p.lse[VARLEN ? static_cast<int64_t>(h) * p.total_q + q_base + q_row
+                     : (static_cast<int64_t>(b) * p.Hq + h) * p.Nq + q_row] =
+            any_key ? (m + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED>
+cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p,
+                       int B, cudaStream_t stream) {
+  auto kern = prefill_fwd_kernel<D, CAUSAL, BF16, VARLEN, MASKED>;
+  constexpr uint32_t smem = Cfg<D>::SMEM_BYTES;
+  // setmaxnreg redistributes the registers the CTA was launched with; a split
+  // larger than that pool would never be granted, so refuse to launch then.
+  cudaFuncAttributes attr{};
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * kThreads < 256 * kSoftmaxRegs + 128 * kOtherRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.n_qtiles, p.Hq, B);
+  kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+// Dispatch over D, causal, dtype and varlen for one value of MASKED.
+template <bool MASKED>
+cudaError_t launch_prefill_variant(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq,
+                                   const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
+                                   cudaStream_t stream) {
+#define ATTN_PREFILL_CASE(DD, CC, BB)                                                           \
+  if (D == DD && causal == CC && bf16 == BB)                                                    \
+    return varlen ? launch_one<DD, CC, BB, true, MASKED>(tq, tk, tv, p, B, stream)              \
+                  : launch_one<DD, CC, BB, false, MASKED>(tq, tk, tv, p, B, stream);
+  ATTN_PREFILL_CASE(128, true, true)
+  ATTN_PREFILL_CASE(128, false, true)
+  ATTN_PREFILL_CASE(128, true, false)
+  ATTN_PREFILL_CASE(128, false, false)
+  ATTN_PREFILL_CASE(64, true, true)
+  ATTN_PREFILL_CASE(64, false, true)
+  ATTN_PREFILL_CASE(64, true, false)
+  ATTN_PREFILL_CASE(64, false, false)
+#undef ATTN_PREFILL_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace attn

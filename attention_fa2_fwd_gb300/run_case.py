@@ -4,6 +4,7 @@
     python -m attention_fa2_fwd_gb300.run_case decode  [--B 64 --Hq 32 --Hkv 8 --L 8192 --D 128]
     python -m attention_fa2_fwd_gb300.run_case decode_paged [--page-size 16 --ragged 1 ...]
     python -m attention_fa2_fwd_gb300.run_case bwd     [prefill sizes; FLOPs counted as 2.5 x the forward]
+    prefill / decode / decode_paged also take --window-left W and --alibi 1 (sliding window, ALiBi slopes)
 
 Inputs are seeded N(0,1) bf16 tensors drawn on the device.  Each iteration is
 timed with CUDA events on the launching stream (L2 flushed by a 256 MiB write
@@ -34,6 +35,8 @@ def main():
     ap.add_argument("--dtype", choices=("bf16", "f16"), default="bf16")
     ap.add_argument("--page-size", type=int, default=16)
     ap.add_argument("--ragged", type=int, default=0, help="decode_paged: lengths uniform in [L/2, L]")
+    ap.add_argument("--window-left", type=int, default=-1, help="sliding window: keys i - W .. i (-1: none)")
+    ap.add_argument("--alibi", type=int, default=0, help="ALiBi slopes 2^(-8 (h + 1) / H_q)")
     a = ap.parse_args()
     dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
     dev = torch.device("cuda", 0)
@@ -44,15 +47,23 @@ def main():
 
     flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    wl = a.window_left
+    slopes = (torch.tensor([2.0 ** (-8.0 * (h + 1) / a.Hq) for h in range(a.Hq)], dtype=torch.float32, device=dev)
+              if a.alibi else None)
     if a.kind == "prefill":
         B = a.B or 2
         q, k, v = randn(B, a.Hq, a.N, a.D), randn(B, a.Hkv, a.N, a.D), randn(B, a.Hkv, a.N, a.D)
         o = torch.empty_like(q)
         lse = torch.empty((B, a.Hq, a.N), dtype=torch.float32, device=dev)
-        work = 4.0 * B * a.Hq * a.N * a.N * a.D / (2 if a.causal else 1)
+        # FLOPs of the visible (query, key) pairs: 4 D per pair (Q K^T and P V)
+        i = torch.arange(a.N, dtype=torch.float64)
+        hi = i if a.causal else torch.full_like(i, a.N - 1)
+        lo = torch.clamp(i - wl, min=0) if wl >= 0 else torch.zeros_like(i)
+        pairs = float((hi - lo + 1).sum()) if (a.causal or wl >= 0) else float(a.N) * a.N
+        work = 4.0 * B * a.Hq * a.D * pairs if (a.causal or wl >= 0) else 4.0 * B * a.Hq * a.N * a.N * a.D
 
         def call():
-            A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse)
+            A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse, window=(wl, -1), alibi_slopes=slopes)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "bwd":
         B = a.B or 2
@@ -84,10 +95,12 @@ def main():
         od = torch.empty_like(qd)
         lsed = torch.empty((B, a.Hq), dtype=torch.float32, device=dev)
         ws = A.decode_workspace(B, a.Hq, a.Hkv, a.D, dev)
-        work = 2.0 * a.Hkv * a.D * 2 * float(lens.sum())
+        span = lens.clamp(max=wl + 1) if wl >= 0 else lens
+        work = 2.0 * a.Hkv * a.D * 2 * float(span.sum())
 
         def call():
-            A.decode_paged(qd, kp, vp, table, lens, a.L, out=od, lse_out=lsed, workspace=ws)
+            A.decode_paged(qd, kp, vp, table, lens, a.L, out=od, lse_out=lsed, workspace=ws, window_left=wl,
+                           alibi_slopes=slopes)
         unit, scale = "GB/s", 1e9
     else:
         B = a.B or 64
@@ -96,10 +109,10 @@ def main():
         od = torch.empty_like(qd)
         lsed = torch.empty((B, a.Hq), dtype=torch.float32, device=dev)
         ws = A.decode_workspace(B, a.Hq, a.Hkv, a.D, dev)
-        work = 2.0 * B * a.Hkv * a.L * a.D * 2
+        work = 2.0 * B * a.Hkv * (min(a.L, wl + 1) if wl >= 0 else a.L) * a.D * 2
 
         def call():
-            A.decode(qd, kc, vc, a.L, out=od, lse_out=lsed, workspace=ws)
+            A.decode(qd, kc, vc, a.L, out=od, lse_out=lsed, workspace=ws, window_left=wl, alibi_slopes=slopes)
         unit, scale = "GB/s", 1e9
     times = []
     for _ in range(a.iters):

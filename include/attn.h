@@ -65,6 +65,34 @@ typedef enum {
 } attn_dtype_t;
 
 /*
+ * Mask and bias variants ("Skill: Write a Triton Attention Kernel", Use this
+ * when: windowed attention, ALiBi and custom masks; "Triton-FlashAttention"
+ * lists sliding-window attention and ALiBi among deferred features).  Passed
+ * to the *_ex entry points; a NULL pointer means none of them.
+ *
+ *   window_left   -1, or W >= 0: query i attends only to keys j >= i - W
+ *   window_right  -1, or W >= 0: query i attends only to keys j <= i + W
+ *                 (prefill only; with causal = 1 the bound is j <= i anyway)
+ *   alibi_slopes  NULL, or a device fp32 array of H_q slopes: the score of
+ *                 (i, j) gets -slopes[h] * |i - j| added before the softmax
+ *
+ * Positions are those of the causal mask (top-left, per sequence for the
+ * variable-length call); for decode the query sits at position cache_len - 1
+ * (per request for the paged call) and window_right is ignored.  A query row
+ * left with no key gets O = 0 and LSE = -inf.
+ *
+ * Errors: a window below -1 gives ATTN_ERR_INVALID_ARG; slopes not 4-byte
+ * aligned give ATTN_ERR_ALIGNMENT.  The struct is read during the call; the
+ * slope array is read by the kernel, so it must stay valid until the work
+ * enqueued on the stream has finished.  The caller owns both.
+ */
+typedef struct {
+    int32_t window_left;
+    int32_t window_right;
+    const float *alibi_slopes;
+} attn_options_t;
+
+/*
  * attn_fwd_prefill -- fused attention forward over a whole sequence.
  *
  * Follows "Skill: Write a Triton Attention Kernel", Required reasoning process
@@ -90,6 +118,13 @@ attn_status_t attn_fwd_prefill(const void *q, const void *k, const void *v, void
                                attn_dtype_t dtype, int B, int H_q, int H_kv, int N_q, int N_kv, int D,
                                const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
                                const int64_t o_str[4], int causal, float scale, void *stream);
+
+/* attn_fwd_prefill with mask and bias options (see attn_options_t). */
+attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  attn_dtype_t dtype, int B, int H_q, int H_kv, int N_q, int N_kv, int D,
+                                  const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                                  const int64_t o_str[4], int causal, float scale, const attn_options_t *opts,
+                                  void *stream);
 
 /*
  * attn_fwd_prefill_varlen -- attn_fwd_prefill over a batch of sequences of
@@ -124,6 +159,14 @@ attn_status_t attn_fwd_prefill_varlen(const void *q, const void *k, const void *
                                       int total_k, const int64_t q_str[3], const int64_t k_str[3],
                                       const int64_t v_str[3], const int64_t o_str[3], int causal, float scale,
                                       void *stream);
+
+/* attn_fwd_prefill_varlen with mask and bias options (see attn_options_t). */
+attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                                         attn_dtype_t dtype, int B, int H_q, int H_kv, int D,
+                                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int max_seqlen_q,
+                                         int max_seqlen_k, int total_q, int total_k, const int64_t q_str[3],
+                                         const int64_t k_str[3], const int64_t v_str[3], const int64_t o_str[3],
+                                         int causal, float scale, const attn_options_t *opts, void *stream);
 
 /*
  * attn_bwd_workspace_size -- bytes of scratch attn_bwd needs: one fp32 per
@@ -208,6 +251,14 @@ attn_status_t attn_fwd_decode(const void *q, const void *k_cache, const void *v_
                               const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
                               const int64_t o_str[4], float scale, void *workspace, size_t workspace_bytes,
                               void *stream);
+
+/* attn_fwd_decode with mask and bias options (see attn_options_t); a left window
+ * W limits the keys read from the cache to the last W + 1 positions. */
+attn_status_t attn_fwd_decode_ex(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                                 attn_dtype_t dtype, int B, int H_q, int H_kv, int cache_len, int D,
+                                 const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
+                                 const int64_t o_str[4], float scale, void *workspace, size_t workspace_bytes,
+                                 const attn_options_t *opts, void *stream);
 
 /*
  * kv_cache_write -- copy n_new tokens of K and V into a preallocated cache at
@@ -297,6 +348,15 @@ attn_status_t attn_fwd_decode_paged(const void *q, const void *k_pages, const vo
                                     const int32_t *cache_lens, int max_cache_len, const int64_t q_str[4],
                                     const int64_t kp_str[4], const int64_t vp_str[4], const int64_t o_str[4],
                                     float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* attn_fwd_decode_paged with mask and bias options (see attn_options_t). */
+attn_status_t attn_fwd_decode_paged_ex(const void *q, const void *k_pages, const void *v_pages, void *o, float *lse,
+                                       attn_dtype_t dtype, int B, int H_q, int H_kv, int D, int num_pages,
+                                       int page_size, const int32_t *block_table, int max_pages, int64_t bt_stride,
+                                       const int32_t *cache_lens, int max_cache_len, const int64_t q_str[4],
+                                       const int64_t kp_str[4], const int64_t vp_str[4], const int64_t o_str[4],
+                                       float scale, void *workspace, size_t workspace_bytes,
+                                       const attn_options_t *opts, void *stream);
 
 /*
  * kv_cache_write_paged -- write n_new tokens per request into a paged cache.

@@ -249,3 +249,47 @@ def test_bwd_workspace_size():
     assert A.attn_bwd_workspace_size(2, 8, 64) == 2 * 8 * 64 * 4
     assert A.attn_bwd_workspace_size(1, 1, 3) == 16
     assert A.attn_bwd_workspace_size(0, 8, 64) == 0
+
+
+OPTION_CALLS = {
+    "prefill": lambda o: A.attn_fwd_prefill_ex(
+        P, P, P, P, None, A.ATTN_BF16, 2, 8, 2, 64, 64, 128, contig(2, 8, 64, 128), contig(2, 2, 64, 128),
+        contig(2, 2, 64, 128), contig(2, 8, 64, 128), 1, 0.088, o, None),
+    "prefill_varlen": lambda o: A.attn_fwd_prefill_varlen_ex(
+        P, P, P, P, None, A.ATTN_BF16, 3, 8, 2, 128, P, P, 100, 100, 200, 200, (8 * 128, 128, 1),
+        (2 * 128, 128, 1), (2 * 128, 128, 1), (8 * 128, 128, 1), 1, 0.088, o, None),
+    "decode": lambda o: A.attn_fwd_decode_ex(
+        P, P, P, P, None, A.ATTN_BF16, 2, 32, 8, 100, 128, contig(2, 32, 1, 128), contig(2, 8, 256, 128),
+        contig(2, 8, 256, 128), contig(2, 32, 1, 128), 0.088, P, 1 << 30, o, None),
+    "decode_paged": lambda o: A.attn_fwd_decode_paged_ex(
+        P, P, P, P, None, A.ATTN_BF16, 2, 32, 8, 128, 100, 16, P, 64, 64, P, 1000, contig(2, 32, 1, 128),
+        contig(100, 8, 16, 128), contig(100, 8, 16, 128), contig(2, 32, 1, 128), 0.088, P, 1 << 30, o, None),
+}
+
+
+@pytest.mark.parametrize("call", sorted(OPTION_CALLS))
+@pytest.mark.parametrize("opts,code", [
+    ((-2, -1, None), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -5, None), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, P + 2), A.ATTN_ERR_ALIGNMENT),
+    ((3, 4, P + 1), A.ATTN_ERR_ALIGNMENT),
+])
+def test_option_errors(lib, call, opts, code):
+    """Options are validated with the other arguments, before any CUDA call."""
+    assert OPTION_CALLS[call](A.AttnOptions(*opts)) == code
+
+
+def test_option_argument_errors_still_checked_first(lib):
+    """With valid options the ordinary argument checks still apply."""
+    assert A.attn_fwd_prefill_ex(None, P, P, P, None, A.ATTN_BF16, 2, 8, 2, 64, 64, 128, contig(2, 8, 64, 128),
+                                 contig(2, 2, 64, 128), contig(2, 2, 64, 128), contig(2, 8, 64, 128), 1, 0.088,
+                                 A.AttnOptions(16, -1, None), None) == A.ATTN_ERR_INVALID_ARG
+
+
+def test_make_options():
+    assert A.make_options() is None
+    o = A.make_options(5, 7)
+    assert (o.window_left, o.window_right, o.alibi_slopes) == (5, 7, None)
+    import torch
+    with pytest.raises(TypeError):
+        A.make_options(alibi_slopes=torch.zeros(4))  # a CPU tensor is not a device pointer

@@ -1,0 +1,175 @@
+"""GPU parity of the sliding-window and ALiBi options (the *_ex entry points)
+through the C ABI, against the fp64 windowed / ALiBi oracle.
+
+Readings (the pages name these variants without defining them): row i and key
+j sit at positions i and j; key j is visible iff
+i - window_left <= j <= i + window_right (-1: unbounded side, causal adds
+j <= i); ALiBi adds -slope_h |i - j| to the scaled score; decode's query sits at
+position cache_len - 1.  Rows whose band holds no key give O = 0, LSE = -inf.
+ALiBi slopes are the usual geometric ones, 2^(-8 (h + 1) / H_q).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attention_fa2_fwd_gb300 import inputs as I
+from oracle import masked as M
+from tests.helpers import assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_fa2_fwd_gb300 as A
+    A.lib()
+    yield
+    A.check_device_error()
+
+
+def _slopes(H):
+    return np.array([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=np.float32)
+
+
+def _dev_slopes(s):
+    return None if s is None else torch.tensor(s, dtype=torch.float32, device="cuda")
+
+
+def _assert_masked(o, lse, o_ref, lse_ref, what):
+    """Rows with keys compare within tolerance; rows without keys must be exactly O = 0, LSE = -inf."""
+    o, lse = np64(o), np64(lse)
+    empty = np.isneginf(lse_ref)
+    assert (np.isneginf(lse) == empty).all(), f"{what}: empty-row pattern differs"
+    assert (o[empty] == 0).all(), f"{what}: empty rows not zero"
+    full = ~empty
+    assert_close(o[full], o_ref[full], lse[full], lse_ref[full], what)
+
+
+PREFILL_CASES = [
+    # (name, Nq, Nkv, causal, window_left, window_right, alibi)
+    ("causal-w100", 700, 700, True, 100, -1, False),
+    ("causal-w0", 700, 700, True, 0, -1, False),
+    ("causal-w300-alibi", 700, 700, True, 300, -1, True),
+    ("causal-alibi", 700, 700, True, -1, -1, True),
+    ("band-37-300", 700, 700, False, 37, 300, False),
+    ("right0-is-causal", 700, 700, False, -1, 0, False),
+    ("full-alibi", 700, 700, False, -1, -1, True),
+    ("band-200-5-alibi", 700, 700, False, 200, 5, True),
+    ("band-128-127", 700, 700, False, 128, 127, False),
+    ("wide-window", 700, 700, True, 5000, -1, False),
+    ("cross-short-q", 300, 900, False, 50, 600, True),
+    ("cross-tall-q-empty-rows", 900, 300, False, 10, 10, False),
+    ("cross-tall-q-causal", 900, 300, True, 20, -1, True),
+]
+
+
+@pytest.mark.parametrize("name,Nq,Nkv,causal,wl,wr,alibi", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "f16")])
+def test_prefill_window_alibi(name, Nq, Nkv, causal, wl, wr, alibi, D, dtype):
+    import attention_fa2_fwd_gb300 as A
+    B, Hq, Hkv = 2, 8, 2
+    q, k, v = I.prefill_inputs(B, Hq, Hkv, Nq, Nkv, D, dtype, seed=Nq + 3 * Nkv + D)
+    sl = _slopes(Hq) if alibi else None
+    o, lse = A.prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, window=(wl, wr), alibi_slopes=_dev_slopes(sl))
+    torch.cuda.synchronize()
+    o_ref, lse_ref = M.attention_masked(np64(q), np64(k), np64(v), causal, 1 / math.sqrt(D), wl, wr, sl)
+    _assert_masked(o, lse, o_ref, lse_ref, name)
+
+
+def test_prefill_window_bhnd_and_bnhd_layouts_agree():
+    """The options do not depend on the memory layout of Q, K, V, O."""
+    import attention_fa2_fwd_gb300 as A
+    B, Hq, Hkv, N, D = 2, 8, 4, 513, 128
+    sl = _dev_slopes(_slopes(Hq))
+    outs = []
+    for layout in ("bhnd", "bnhd"):
+        q, k, v = (t.cuda() for t in I.prefill_inputs(B, Hq, Hkv, N, N, D, "bf16", layout, seed=9))
+        assert layout == "bhnd" or q.stride(1) == D  # the (B,N,H,D) memory order survived the copy
+        outs.append(A.prefill(q, k, v, causal=True, window=(70, -1), alibi_slopes=sl))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("causal,wl,wr", [(True, 64, -1), (False, 100, 50), (False, 0, 0)])
+def test_varlen_window_alibi(causal, wl, wr):
+    import attention_fa2_fwd_gb300 as A
+    lens = [1, 33, 300, 127, 1000, 256]
+    Hq, Hkv, D = 16, 4, 128
+    g = torch.Generator().manual_seed(sum(lens) + wl)
+    tq = sum(lens)
+    q = torch.randn((tq, Hq, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((tq, Hkv, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((tq, Hkv, D), generator=g).to(torch.bfloat16)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    sl = _slopes(Hq)
+    o, lse = A.prefill_varlen(q.cuda(), k.cuda(), v.cuda(), cu.cuda(), cu.cuda(), max(lens), max(lens),
+                              causal=causal, window=(wl, wr), alibi_slopes=_dev_slopes(sl))
+    torch.cuda.synchronize()
+    o_ref, lse_ref = M.prefill_varlen_masked(np64(q), np64(k), np64(v), cu.numpy(), cu.numpy(), causal,
+                                             1 / math.sqrt(D), wl, wr, sl)
+    # LSE is (H_q, total_q): compare it row-major with O's (total_q, H_q) rows
+    _assert_masked(o, lse.t(), o_ref, lse_ref.T, f"varlen causal={causal} window=({wl},{wr})")
+
+
+@pytest.mark.parametrize("B,L", [(4, 4097), (2, 8192), (64, 1000)])
+@pytest.mark.parametrize("wl", [0, 63, 64, 1000, 9000])
+@pytest.mark.parametrize("alibi", [False, True])
+def test_decode_window_alibi(B, L, wl, alibi):
+    import attention_fa2_fwd_gb300 as A
+    Hq, Hkv, D = 32, 8, 128
+    k, v = I.decode_stream(B, Hkv, L, D, "bf16", seed=L + wl)
+    q = I.decode_queries(B, Hq, D, [L - 1], "bf16", seed=L)[:, :, 0]
+    sl = _slopes(Hq) if alibi else None
+    o, lse = A.decode(q.cuda(), k.cuda(), v.cuda(), L, window_left=wl, alibi_slopes=_dev_slopes(sl))
+    torch.cuda.synchronize()
+    rows = slice(None) if B <= 4 else [0, 17, 63]
+    o_ref, lse_ref = M.decode_masked(np64(q)[rows], np64(k)[rows], np64(v)[rows], L, 1 / math.sqrt(D), wl, sl)
+    assert_close(np64(o)[rows], o_ref, np64(lse)[rows], lse_ref, f"decode B={B} L={L} wl={wl} alibi={alibi}")
+
+
+def test_decode_window_is_last_row_of_windowed_prefill():
+    """Decode at cache_len n with window w equals row n - 1 of the causal prefill with window (w, -1)."""
+    import attention_fa2_fwd_gb300 as A
+    B, Hq, Hkv, N, D, w = 2, 8, 2, 777, 128, 200
+    q, k, v = I.prefill_inputs(B, Hq, Hkv, N, N, D, "bf16", seed=77)
+    sl = _dev_slopes(_slopes(Hq))
+    o_p, l_p = A.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, window=(w, -1), alibi_slopes=sl)
+    o_d, l_d = A.decode(q[:, :, -1].contiguous().cuda(), k.cuda(), v.cuda(), N, window_left=w, alibi_slopes=sl)
+    torch.cuda.synchronize()
+    assert_close(o_d, np64(o_p[:, :, -1]), l_d, np64(l_p[:, :, -1]), "decode vs prefill last row")
+
+
+def _pool(B, Hkv, max_len, D, page_size, seed):
+    max_pages = (max_len + page_size - 1) // page_size
+    num_pages = B * max_pages + 2
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)[:B * max_pages]
+    table = perm.view(B, max_pages).to(torch.int32)
+    kp = torch.randn((num_pages, Hkv, page_size, D), generator=g).to(torch.bfloat16)
+    vp = torch.randn((num_pages, Hkv, page_size, D), generator=g).to(torch.bfloat16)
+    return kp, vp, table
+
+
+@pytest.mark.parametrize("page_size", [16, 64, 128])
+@pytest.mark.parametrize("wl,alibi", [(0, False), (100, True), (-1, True), (700, False)])
+def test_paged_decode_window_alibi(page_size, wl, alibi):
+    import attention_fa2_fwd_gb300 as A
+    Hq, Hkv, D = 32, 8, 128
+    lens = [1, 33, 257, 1000, 0, 64, 129]
+    B, max_len = len(lens), max(lens)
+    kp, vp, table = _pool(B, Hkv, max_len, D, page_size, seed=page_size + wl)
+    q = I.decode_queries(B, Hq, D, [0], "bf16", seed=page_size)[:, :, 0]
+    cl = torch.tensor(lens, dtype=torch.int32)
+    sl = _slopes(Hq) if alibi else None
+    o, lse = A.decode_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), cl.cuda(), max_len, window_left=wl,
+                            alibi_slopes=_dev_slopes(sl))
+    torch.cuda.synchronize()
+    o_ref, lse_ref = M.decode_paged_masked(np64(q), np64(kp), np64(vp), table.numpy(), cl.numpy(),
+                                           1 / math.sqrt(D), wl, sl)
+    _assert_masked(o, lse, o_ref, lse_ref, f"paged ps={page_size} wl={wl} alibi={alibi}")
