@@ -52,8 +52,35 @@ constexpr int kThreads = 384;
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 constexpr int kSoftmaxRegs = 208;
+// Of every 4 column pairs of a score row, how many take 2^x on the FMA pipe
+// (exp2_poly_f2) instead of the ex2 unit, which both softmax warpgroups share.
+constexpr int kPolyPairsOf4 = 0;
 constexpr int kUnlimited = 0x3fffffff;  // "no window bound" (large, yet safe to add small offsets to)
 constexpr int kOtherRegs = 88;
+
+// 2^x for a pair of fp32 values on the FMA pipe.  Range reduction in the
+// manner of Cody and Waite: x = j + f with j = round(x) (by adding 1.5 * 2^23,
+// which leaves j in the low mantissa bits) and f in [-1/2, 1/2]; 2^f by a
+// degree-3 polynomial fitted to minimise the relative error on that interval
+// with the Remez exchange algorithm (max relative error 7.5e-5, far below the
+// 16-bit rounding of P); 2^j by adding j to the exponent field.  x is clamped
+// at -126 so that -inf (masked scores) gives a negligible ~1e-38 instead of 0.
+__device__ __forceinline__ uint64_t exp2_poly_f2(uint64_t x2) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f, c2 = 0.2426111251115799f,
+                  c3 = 0.0551716685295105f;
+  const float2 x = unpack_f2(x2);
+  const uint64_t xc = pack_f2(fmaxf(x.x, -126.f), fmaxf(x.y, -126.f));
+  const uint64_t t = fadd_f2(xc, pack_f2(kRound, kRound));
+  const uint64_t r = fadd_f2(t, pack_f2(-kRound, -kRound));  // j as a float
+  const uint64_t f = ffma_f2(r, pack_f2(-1.f, -1.f), xc);     // x - j, exact
+  uint64_t q = ffma_f2(pack_f2(c3, c3), f, pack_f2(c2, c2));
+  q = ffma_f2(q, f, pack_f2(c1, c1));
+  q = ffma_f2(q, f, pack_f2(c0, c0));
+  const uint32_t lo = static_cast<uint32_t>(q) + (static_cast<uint32_t>(t) << 23);
+  const uint32_t hi = static_cast<uint32_t>(q >> 32) + (static_cast<uint32_t>(t >> 32) << 23);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
 
 template <int D>
 struct Cfg {
@@ -333,12 +360,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pf0 = 0, pf1 = 0;  // parities of the P-ready barriers
         int st = 0, sp = 0;         // ring stages of j and j-1
         uint32_t ph = 0, pph = 0;   // their phases
+        // S0_j is issued at the end of step j-1, right behind P0_{j-1} V_{j-1} (K_j
+        // having been waited for before P0_{j-1}): the thread's next tcgen05
+        // instruction after a P V product is the following S product, so the
+        // tensor pipe gets no gap there.
+        if (J0 < J1) {
+          ok = ok && mbar_wait(BAR(C::B_KF + 0), 0, abort_flag, p.err);
+          if (ok && J0 >= lo0 && J0 < hi0) {
+            tc_fence_after();
+            issue_s(0, dq0, dk);
+          }
+        }
         for (int j = J0; ok && j < J1; ++j) {
           const bool h0 = j >= lo0 && j < hi0, h1 = j >= lo1 && j < hi1;
-          if (!(ok = mbar_wait(BAR(C::B_KF + st), ph, abort_flag, p.err))) break;
-          tc_fence_after();
-          const uint64_t kd = dk + st * kStage16;
-          if (h0) issue_s(0, dq0, kd);
+          const int st1 = st + 1 == ST ? 0 : st + 1;          // ring stage of j + 1
+          const uint32_t ph1 = st1 == 0 ? ph ^ 1 : ph;        // and its phase
+          const bool h0n = j + 1 >= lo0 && j + 1 < hi0;       // tile 0 uses KV tile j + 1
           if (h1p) {
             // O1 += P1_{j-1} V_{j-1}: tile 1 is the last user of V_{j-1}, so its stage is released
             if (!(ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err))) break;
@@ -349,9 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             first1 = false;
             tc_commit(BAR(C::B_VE + sp));
           }
-          if (h1) issue_s(1, dq1, kd);
+          if (h1) {
+            tc_fence_after();
+            issue_s(1, dq1, dk + st * kStage16);
+          }
           tc_commit(BAR(C::B_KE + st));  // both S products that read K_j are issued
           v_waited = false;
+          if (j + 1 < J1 && !(ok = mbar_wait(BAR(C::B_KF + st1), ph1, abort_flag, p.err))) break;
           if (h0) {
             // O0 += P0_j V_j
             if (!(ok = mbar_wait(BAR(C::B_PF + 0), pf0, abort_flag, p.err))) break;
@@ -369,13 +410,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_v(j, st, ph))) break;
             tc_commit(BAR(C::B_VE + st));
           }
+          if (j + 1 < J1 && h0n) {
+            tc_fence_after();
+            issue_s(0, dq0, dk + st1 * kStage16);  // S0_{j+1}
+          }
           h1p = h1;
           sp = st;
           pph = ph;
-          if (++st == ST) {
-            st = 0;
-            ph ^= 1;
-          }
+          st = st1;
+          ph = ph1;
         }
         if (ok && h1p) {
           // the last P1 V of tile 1 (its band ends the ring)
@@ -497,8 +540,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const uint64_t e2 = ffma_f2(pack_f2(__uint_as_float(sr[i][c]), __uint_as_float(sr[i][c + 1])), sl2x2, negm2);
-          const float2 e = unpack_f2(e2);
-          const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+          float p0, p1;
+          if (((c >> 1) & 3) < kPolyPairsOf4) {
+            const float2 e = unpack_f2(exp2_poly_f2(e2));
+            p0 = e.x;
+            p1 = e.y;
+          } else {
+            const float2 e = unpack_f2(e2);
+            p0 = fast_exp2(e.x);
+            p1 = fast_exp2(e.y);
+          }
           rs2[(c >> 1) & 3] = fadd_f2(rs2[(c >> 1) & 3], pack_f2(p0, p1));
           pk[i >> 1][(i & 1) * 16 + c / 2] = pack2<BF16>(p0, p1);
         }
