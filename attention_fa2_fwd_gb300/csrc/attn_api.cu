@@ -260,6 +260,7 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
   p.Hq = H_q;
   p.group = H_q / H_kv;
   p.n_qtiles = (N_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
+  if (p.n_qtiles > 65535) return ATTN_ERR_INVALID_ARG;  // grid z
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   cudaError_t e = launch_prefill(D, causal != 0, bf16, false, prefill_masked(p, causal != 0), tq, tk, tv, p, B,
                                  static_cast<cudaStream_t>(stream));
@@ -324,6 +325,7 @@ attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const voi
   p.Hq = H_q;
   p.group = H_q / H_kv;
   p.n_qtiles = (max_seqlen_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
+  if (p.n_qtiles > 65535) return ATTN_ERR_INVALID_ARG;  // grid z
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;

@@ -174,8 +174,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int h = blockIdx.y, b = blockIdx.z;
+  // Grid (H_q, B, pairs): the block scheduler walks heads and batches first, so
+  // with the causal mask every CTA of the heaviest pair (the last rows, the most
+  // keys) starts before any lighter one -- longest-first over the whole grid,
+  // which keeps the last wave short.
+  const int pair = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.z)) : static_cast<int>(blockIdx.z);
+  const int h = blockIdx.x, b = blockIdx.y;
   const int hk = h / p.group;
   const int q0 = pair * 2 * kBM;  // first row of tile 0; tile 1 starts at q0 + 128
   int q_base = 0, k_base = 0, Nq = p.Nq, Nkv = p.Nkv, bc = b;  // bc: batch coordinate of the tensor maps
@@ -635,7 +639,7 @@ cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   if (attr.numRegs * kThreads < 256 * kSoftmaxRegs + 128 * kOtherRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(p.n_qtiles, p.Hq, B);
+  dim3 grid(p.Hq, B, p.n_qtiles);
   kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
