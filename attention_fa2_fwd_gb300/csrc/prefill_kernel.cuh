@@ -128,6 +128,16 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, i
   const int c3 = (sn == 3) ? n : (sh == 3) ? h : b;
   tma_load_4d(dst, map, d, c1, c2, c3, bar);
 }
+// tma_tile for data read once (Q): evicted from L2 first, so that the K and V
+// tiles every query tile of a head group re-reads stay resident.
+__device__ __forceinline__ void tma_tile_once(uint32_t dst, const CUtensorMap *map, int d, int n, int h, int b,
+                                              uint32_t slots, uint32_t bar) {
+  const int sn = slots & 3, sh = (slots >> 2) & 3;
+  const int c1 = (sn == 1) ? n : (sh == 1) ? h : b;
+  const int c2 = (sn == 2) ? n : (sh == 2) ? h : b;
+  const int c3 = (sn == 3) ? n : (sh == 3) ? h : b;
+  tma_load_4d_hint(dst, map, d, c1, c2, c3, bar, l2_policy_evict_first());
+}
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -279,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c)
-            tma_tile(sQ + t * C::QT_BYTES + c * C::CHUNK_Q, &tmQ, c * 64, q_base + q0 + t * kBM, h, bc, p.slots_q,
-                     BAR(C::B_Q));
+            tma_tile_once(sQ + t * C::QT_BYTES + c * C::CHUNK_Q, &tmQ, c * 64, q_base + q0 + t * kBM, h, bc,
+                          p.slots_q, BAR(C::B_Q));
         int st = 0;       // ring stage of KV tile j
         uint32_t ph = 0;  // its phase
         for (int j = J0; j < J1; ++j) {
