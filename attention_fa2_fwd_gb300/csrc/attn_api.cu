@@ -191,6 +191,17 @@ attn_status_t read_options(const attn_options_t *opts, int *wl, int *wr, const f
   return ATTN_OK;
 }
 
+// Persistent prefill schedule: units = query-tile pairs x heads x batches,
+// one CTA per SM at most.
+attn_status_t prefill_schedule(PrefillParams *p, int B, int H_q, int sm_count) {
+  const int64_t units = static_cast<int64_t>(H_q) * B * p->n_qtiles;
+  if (units > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
+  p->B = B;
+  p->n_units = static_cast<int>(units);
+  p->n_ctas = static_cast<int>(units < sm_count ? units : sm_count);
+  return ATTN_OK;
+}
+
 // Whether a prefill needs the masked kernel build: a left window, a right
 // window that the causal mask does not already imply, or ALiBi slopes.
 bool prefill_masked(const PrefillParams &p, bool causal) {
@@ -260,7 +271,7 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
   p.Hq = H_q;
   p.group = H_q / H_kv;
   p.n_qtiles = (N_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
-  if (p.n_qtiles > 65535) return ATTN_ERR_INVALID_ARG;  // grid z
+  if ((st = prefill_schedule(&p, B, H_q, dev->sm_count)) != ATTN_OK) return st;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   cudaError_t e = launch_prefill(D, causal != 0, bf16, false, prefill_masked(p, causal != 0), tq, tk, tv, p, B,
                                  static_cast<cudaStream_t>(stream));
@@ -325,7 +336,7 @@ attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const voi
   p.Hq = H_q;
   p.group = H_q / H_kv;
   p.n_qtiles = (max_seqlen_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
-  if (p.n_qtiles > 65535) return ATTN_ERR_INVALID_ARG;  // grid z
+  if ((st = prefill_schedule(&p, B, H_q, dev->sm_count)) != ATTN_OK) return st;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;

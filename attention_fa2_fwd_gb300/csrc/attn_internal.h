@@ -23,7 +23,11 @@ struct PrefillParams {
   float *lse;               // may be null
   unsigned *err;            // device error word
   int64_t o_sb, o_sh, o_sn; // output element strides (d stride is 1)
-  int Nq, Nkv, Hq, group, n_qtiles;  // n_qtiles: CTAs along N_q (each covers 2 x 128 rows)
+  int Nq, Nkv, Hq, group, n_qtiles;  // n_qtiles: query-tile pairs along N_q (2 x 128 rows each)
+  // Persistent schedule: n_units = H_q * B * n_qtiles pairs, numbered heads
+  // fastest, then batches, then pairs (longest first under the causal mask);
+  // n_ctas CTAs take them in rounds, dealt alternately forwards and backwards.
+  int B, n_units, n_ctas;
   float scale_log2;         // scale * log2(e): scores are kept in base-2 units
   // Tensor-map coordinate slot (1..3) of the n, h and b coordinates for the
   // Q, K and V maps, packed as n | h << 2 | b << 4 (slot 0 is always d).

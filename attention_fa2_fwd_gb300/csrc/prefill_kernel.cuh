@@ -51,36 +51,9 @@ constexpr int kBN = kPrefillBN;  // keys per KV tile
 constexpr int kThreads = 384;
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
-constexpr int kSoftmaxRegs = 208;
-// Of every 4 column pairs of a score row, how many take 2^x on the FMA pipe
-// (exp2_poly_f2) instead of the ex2 unit, which both softmax warpgroups share.
-constexpr int kPolyPairsOf4 = 0;
+constexpr int kSoftmaxRegs = 200;
 constexpr int kUnlimited = 0x3fffffff;  // "no window bound" (large, yet safe to add small offsets to)
-constexpr int kOtherRegs = 88;
-
-// 2^x for a pair of fp32 values on the FMA pipe.  Range reduction in the
-// manner of Cody and Waite: x = j + f with j = round(x) (by adding 1.5 * 2^23,
-// which leaves j in the low mantissa bits) and f in [-1/2, 1/2]; 2^f by a
-// degree-3 polynomial fitted to minimise the relative error on that interval
-// with the Remez exchange algorithm (max relative error 7.5e-5, far below the
-// 16-bit rounding of P); 2^j by adding j to the exponent field.  x is clamped
-// at -126 so that -inf (masked scores) gives a negligible ~1e-38 instead of 0.
-__device__ __forceinline__ uint64_t exp2_poly_f2(uint64_t x2) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f, c2 = 0.2426111251115799f,
-                  c3 = 0.0551716685295105f;
-  const float2 x = unpack_f2(x2);
-  const uint64_t xc = pack_f2(fmaxf(x.x, -126.f), fmaxf(x.y, -126.f));
-  const uint64_t t = fadd_f2(xc, pack_f2(kRound, kRound));
-  const uint64_t r = fadd_f2(t, pack_f2(-kRound, -kRound));  // j as a float
-  const uint64_t f = ffma_f2(r, pack_f2(-1.f, -1.f), xc);     // x - j, exact
-  uint64_t q = ffma_f2(pack_f2(c3, c3), f, pack_f2(c2, c2));
-  q = ffma_f2(q, f, pack_f2(c1, c1));
-  q = ffma_f2(q, f, pack_f2(c0, c0));
-  const uint32_t lo = static_cast<uint32_t>(q) + (static_cast<uint32_t>(t) << 23);
-  const uint32_t hi = static_cast<uint32_t>(q >> 32) + (static_cast<uint32_t>(t >> 32) << 23);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
+constexpr int kOtherRegs = 96;
 
 template <int D>
 struct Cfg {
@@ -159,6 +132,93 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// One unit of work: a pair of 128-row query tiles of one (batch, q head), with
+// the KV tiles each tile needs.
+struct Unit {
+  int h, b, hk, q0, q_base, k_base, Nq, Nkv, bc;  // bc: batch coordinate of the tensor maps
+  int lo0, hi0, lo1, hi1, J0, J1, j_tail;         // KV tile bands [lo_t, hi_t) and their hull [J0, J1)
+  bool zero_v;                                    // variable length: tail V tile to be zeroed
+  int kind;
+};
+constexpr int kRun = 0;    // compute the unit
+constexpr int kSkip = 1;   // nothing to do (variable length: pair past the sequence, or bad offsets)
+constexpr int kEmpty = 2;  // variable length, no keys: O = 0 and LSE = -inf
+constexpr int kBadIndex = 4;  // with kSkip: the sequence offsets were out of range
+
+// Every role of the CTA derives the same units in the same order, so the
+// pipelines (TMA ring, S/P/O barriers) stay in step across units.
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ Unit make_unit(int u, const PrefillParams &p, int win_l, int win_r) {
+  Unit U;
+  const int hb = p.Hq * p.B;
+  const int z = u / hb, rem = u - z * hb;
+  U.h = rem % p.Hq;
+  U.b = rem / p.Hq;
+  const int pair = CAUSAL ? (p.n_qtiles - 1 - z) : z;
+  U.hk = U.h / p.group;
+  U.q0 = pair * 2 * kBM;
+  U.q_base = 0;
+  U.k_base = 0;
+  U.Nq = p.Nq;
+  U.Nkv = p.Nkv;
+  U.bc = U.b;
+  U.kind = kRun;
+  if constexpr (VARLEN) {
+    const int qs = p.cu_q[U.b], qe = p.cu_q[U.b + 1], ks = p.cu_k[U.b], ke = p.cu_k[U.b + 1];
+    if (qs < 0 || qe < qs || qe > p.total_q || qe - qs > p.Nq || ks < 0 || ke < ks || ke > p.total_k ||
+        ke - ks > p.Nkv) {
+      U.kind = kSkip | kBadIndex;
+      U.Nq = U.Nkv = 0;
+    } else {
+      U.q_base = qs;
+      U.k_base = ks;
+      U.Nq = qe - qs;
+      U.Nkv = ke - ks;
+      U.bc = 0;
+      if (U.q0 >= U.Nq) U.kind = kSkip;
+      else if (U.Nkv == 0) U.kind = kEmpty;
+    }
+  }
+  // Key band of a query row i: i - win_l <= j <= i + win_r (kUnlimited: no
+  // bound on that side); causal fixes win_r at 0.  Query tile t needs KV tiles
+  // [lo_t, hi_t); tiles outside the band are never loaded or computed.  Tile 1
+  // lies at or after tile 0 (lo0 <= lo1, hi0 <= hi1).
+  int lo[2] = {0, 0}, hi[2] = {0, 0};
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qa = U.q0 + t * kBM;  // first row of the tile
+    const int kmin = win_l == kUnlimited ? 0 : max(0, qa - win_l);
+    const int kmax = win_r == kUnlimited ? U.Nkv - 1 : min(U.Nkv - 1, qa + kBM - 1 + win_r);
+    lo[t] = kmin / kBN;
+    hi[t] = kmax < kmin ? lo[t] : kmax / kBN + 1;
+  }
+  U.lo0 = lo[0];
+  U.hi0 = hi[0];
+  U.lo1 = lo[1];
+  U.hi1 = hi[1];
+  const bool has_t0 = lo[0] < hi[0], has_t1 = lo[1] < hi[1];
+  U.J0 = has_t0 ? (has_t1 ? min(lo[0], lo[1]) : lo[0]) : (has_t1 ? lo[1] : 0);
+  U.J1 = has_t0 ? (has_t1 ? max(hi[0], hi[1]) : hi[0]) : (has_t1 ? hi[1] : 0);
+  if (U.kind != kRun) U.J1 = U.J0;
+  const int nkv_all = (U.Nkv + kBN - 1) / kBN;
+  // Variable length: the last KV tile runs past the sequence and is used here.
+  U.j_tail = nkv_all - 1;
+  U.zero_v = VARLEN && U.kind == kRun && (U.Nkv % kBN) != 0 && U.J1 == nkv_all && U.J0 <= U.j_tail;
+  return U;
+}
+
+// The unit a CTA runs in round k: rounds of gridDim.x units in longest-first
+// order, dealt alternately forwards and backwards over the CTAs, which evens
+// out the CTAs' total work (the sum of the causal lengths).
+__device__ __forceinline__ int unit_index(int k, int c, int g) { return k * g + ((k & 1) ? g - 1 - c : c); }
+
+// Persistent: one CTA per SM walks rounds of units (longest first).
+// While the softmax warps store one unit's O, the next unit's Q is already
+// loaded and its first Q K^T product runs: Q is reloaded as soon as the last
+// S product of a unit completed, and a tile's O columns are only
+// overwritten by the next unit's first P V, which waits for that tile's
+// softmax warps -- the same warps that ran the epilogue.
+//
 // VARLEN: the batch is packed; sequence b's rows are found through cu_q / cu_k
 // (see PrefillParams), tensor maps span the packed tensors, and the last V tile
 // of a sequence -- whose tail rows belong to the next sequence -- gets those
@@ -184,64 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Grid (H_q, B, pairs): the block scheduler walks heads and batches first, so
-  // with the causal mask every CTA of the heaviest pair (the last rows, the most
-  // keys) starts before any lighter one -- longest-first over the whole grid,
-  // which keeps the last wave short.
-  const int pair = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.z)) : static_cast<int>(blockIdx.z);
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int hk = h / p.group;
-  const int q0 = pair * 2 * kBM;  // first row of tile 0; tile 1 starts at q0 + 128
-  int q_base = 0, k_base = 0, Nq = p.Nq, Nkv = p.Nkv, bc = b;  // bc: batch coordinate of the tensor maps
-  if constexpr (VARLEN) {
-    const int qs = p.cu_q[b], qe = p.cu_q[b + 1], ks = p.cu_k[b], ke = p.cu_k[b + 1];
-    if (qs < 0 || qe < qs || qe > p.total_q || qe - qs > p.Nq || ks < 0 || ke < ks || ke > p.total_k ||
-        ke - ks > p.Nkv) {
-      if (threadIdx.x == 0) atomicOr(p.err, kErrBadIndex);
-      return;
-    }
-    q_base = qs;
-    k_base = ks;
-    Nq = qe - qs;
-    Nkv = ke - ks;
-    bc = 0;
-    if (q0 >= Nq) return;
-    if (Nkv == 0) {
-      // No keys: O = 0 and LSE = -inf for this pair's rows.
-      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      for (int r = threadIdx.x; r < 2 * kBM; r += kThreads) {
-        if (q0 + r >= Nq) break;
-        T *orow = reinterpret_cast<T *>(p.o) + static_cast<int64_t>(h) * p.o_sh +
-                  static_cast<int64_t>(q_base + q0 + r) * p.o_sn;
-        for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4 *>(orow + d) = make_uint4(0, 0, 0, 0);
-        if (p.lse != nullptr) p.lse[static_cast<int64_t>(h) * p.total_q + q_base + q0 + r] = -INFINITY;
-      }
-      return;
-    }
-  }
-  const int nkv_all = (Nkv + kBN - 1) / kBN;
-  // Key band of a query row i: i - win_l <= j <= i + win_r (kUnlimited: no
-  // bound on that side); causal fixes win_r at 0.  Query tile t needs KV tiles
-  // [lo_t, hi_t); tiles outside the band are never loaded or computed.
   // Without MASKED both bounds are compile-time constants and the band code
   // folds away (the plain kernel keeps its shorter softmax loop).
   const int win_l = (!MASKED || p.window_left < 0) ? kUnlimited : p.window_left;
   const int win_r = CAUSAL ? 0 : ((!MASKED || p.window_right < 0) ? kUnlimited : p.window_right);
-  int lo[2], hi[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qa = q0 + t * kBM;  // first row of the tile
-    const int kmin = win_l == kUnlimited ? 0 : max(0, qa - win_l);
-    const int kmax = win_r == kUnlimited ? Nkv - 1 : min(Nkv - 1, qa + kBM - 1 + win_r);
-    lo[t] = kmin / kBN;
-    hi[t] = kmax < kmin ? lo[t] : kmax / kBN + 1;
-  }
-  const bool has_t0 = lo[0] < hi[0], has_t1 = lo[1] < hi[1];
-  const int J0 = has_t0 ? (has_t1 ? min(lo[0], lo[1]) : lo[0]) : (has_t1 ? lo[1] : 0);
-  const int J1 = has_t0 ? (has_t1 ? max(hi[0], hi[1]) : hi[0]) : (has_t1 ? hi[1] : 0);
-  // Variable length: the last KV tile runs past the sequence and is used here.
-  const int j_tail = nkv_all - 1;
-  const bool zero_v = VARLEN && (Nkv % kBN) != 0 && J1 == nkv_all && J0 <= j_tail;
+  const int u_first = blockIdx.x, u_step = gridDim.x, n_units = p.n_units;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_Q), 1);
@@ -282,41 +289,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 8) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
-        int issued_k = 0, issued_v = 0;
+        int issued_k = 0, issued_v = 0, nq = 0;  // K, V tiles and Q pairs issued so far
+        int st = 0;                              // ring stage of the next KV tile
+        uint32_t ph = 0;                         // its phase
+        int q_wait = -1;                         // what frees Q: -1 nothing, -2 the last Q load, else KE stage
+        uint32_t q_phase = 0;
         bool ok = true;
-        mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QT_BYTES);
+        for (int k = 0; ok && k * u_step < n_units; ++k) {
+          const int u = unit_index(k, u_first, u_step);
+          if (u >= n_units) continue;
+          const Unit U = make_unit<CAUSAL, VARLEN>(u, p, win_l, win_r);
+          if (U.kind != kRun) continue;
+          // The previous unit's Q is free once its last S product completed: the
+          // release of its last K stage (in-order MMAs: every S product before it
+          // is complete too), or -- for a unit without KV tiles -- once its Q landed.
+          if (q_wait >= 0) ok = mbar_wait(BAR(C::B_KE + q_wait), q_phase, abort_flag, p.err);
+          else if (q_wait == -2) ok = mbar_wait(BAR(C::B_Q), (nq - 1) & 1, abort_flag, p.err);
+          if (!ok) break;
+          mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QT_BYTES);
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
-            tma_tile_once(sQ + t * C::QT_BYTES + c * C::CHUNK_Q, &tmQ, c * 64, q_base + q0 + t * kBM, h, bc,
-                          p.slots_q, BAR(C::B_Q));
-        int st = 0;       // ring stage of KV tile j
-        uint32_t ph = 0;  // its phase
-        for (int j = J0; j < J1; ++j) {
-          const bool reuse = j - J0 >= ST;  // the stage held tile j - ST
-          if (reuse && !(ok = mbar_wait(BAR(C::B_KE + st), ph ^ 1, abort_flag, p.err))) break;
-          mbar_arrive_expect_tx(BAR(C::B_KF + st), C::KV_BYTES);
+            for (int c = 0; c < C::KCH; ++c)
+              tma_tile_once(sQ + t * C::QT_BYTES + c * C::CHUNK_Q, &tmQ, c * 64, U.q_base + U.q0 + t * kBM, U.h,
+                            U.bc, p.slots_q, BAR(C::B_Q));
+          ++nq;
+          for (int j = U.J0; j < U.J1; ++j) {
+            const bool reuse = issued_k >= ST;  // the stage held the tile ST positions back
+            if (reuse && !(ok = mbar_wait(BAR(C::B_KE + st), ph ^ 1, abort_flag, p.err))) break;
+            mbar_arrive_expect_tx(BAR(C::B_KF + st), C::KV_BYTES);
 #pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
-            tma_tile(sK + st * C::KV_BYTES + c * C::CHUNK_KV, &tmK, c * 64, k_base + j * kBN, hk, bc, p.slots_k,
-                     BAR(C::B_KF + st));
-          ++issued_k;
-          if (reuse && !(ok = mbar_wait(BAR(C::B_VE + st), ph ^ 1, abort_flag, p.err))) break;
-          mbar_arrive_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
+            for (int c = 0; c < C::KCH; ++c)
+              tma_tile(sK + st * C::KV_BYTES + c * C::CHUNK_KV, &tmK, c * 64, U.k_base + j * kBN, U.hk, U.bc,
+                       p.slots_k, BAR(C::B_KF + st));
+            ++issued_k;
+            if (reuse && !(ok = mbar_wait(BAR(C::B_VE + st), ph ^ 1, abort_flag, p.err))) break;
+            mbar_arrive_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
 #pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
-            tma_tile(sV + st * C::KV_BYTES + c * C::CHUNK_KV, &tmV, c * 64, k_base + j * kBN, hk, bc, p.slots_v,
-                     BAR(C::B_VF + st));
-          ++issued_v;
-          if (++st == ST) {
-            st = 0;
-            ph ^= 1;
+            for (int c = 0; c < C::KCH; ++c)
+              tma_tile(sV + st * C::KV_BYTES + c * C::CHUNK_KV, &tmV, c * 64, U.k_base + j * kBN, U.hk, U.bc,
+                       p.slots_v, BAR(C::B_VF + st));
+            ++issued_v;
+            q_wait = st;
+            q_phase = ph;
+            if (++st == ST) {
+              st = 0;
+              ph ^= 1;
+            }
           }
+          if (U.J0 == U.J1) q_wait = -2;
         }
         if (!ok) {
           // Let every copy already issued land before shared memory is released.
-          mbar_wait(BAR(C::B_Q), 0, nullptr, p.err);
+          if (nq > 0) mbar_wait(BAR(C::B_Q), (nq - 1) & 1, nullptr, p.err);
           for (int i = max(0, issued_k - ST); i < issued_k; ++i)
             mbar_wait(BAR(C::B_KF + i % ST), (i / ST) & 1, nullptr, p.err);
           for (int i = max(0, issued_v - ST); i < issued_v; ++i)
@@ -352,122 +377,143 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (!first || kk > 0) ? 1u : 0u);
           }
         };
-        // V of KV tile j (ring stage st, phase ph) has landed (and, for a sequence's
-        // tail tile, been zeroed past the end: this thread, which follows the stage
-        // phases in order, tells warp 10 when the tail tile is in and waits for it
-        // to clear the rows).
-        auto wait_v = [&](int j, int st, uint32_t ph) -> bool {
-          if (!mbar_wait(BAR(C::B_VF + st), ph, abort_flag, p.err)) return false;
-          if (!(zero_v && j == j_tail)) return true;
-          mbar_arrive(BAR(C::B_VT));
-          return mbar_wait(BAR(C::B_VZ), 0, abort_flag, p.err);
-        };
-        // Bands: tile 1 lies at or after tile 0 (lo0 <= lo1, hi0 <= hi1), so the
-        // ring runs from lo0 (or lo1 when tile 0 is empty) to hi1 (or hi0).  The
-        // loop keeps ring stage, phases and first-block flags in registers: this
-        // thread's latency between a barrier and the next MMA is on the critical path.
-        const int lo0 = lo[0], hi0 = hi[0], lo1 = lo[1], hi1 = hi[1];
-        bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, p.err);
-        bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
-        bool h1p = false;       // tile 1 uses KV tile j-1
-        bool first0 = true, first1 = true;
+        bool ok = true;
+        int st = 0;                 // ring stage of the next KV tile
+        uint32_t ph = 0;            // its phase
         uint32_t pf0 = 0, pf1 = 0;  // parities of the P-ready barriers
-        int st = 0, sp = 0;         // ring stages of j and j-1
-        uint32_t ph = 0, pph = 0;   // their phases
-        // S0_j is issued at the end of step j-1, right behind P0_{j-1} V_{j-1} (K_j
-        // having been waited for before P0_{j-1}): the thread's next tcgen05
-        // instruction after a P V product is the following S product, so the
-        // tensor pipe gets no gap there.
-        if (J0 < J1) {
-          ok = ok && mbar_wait(BAR(C::B_KF + 0), 0, abort_flag, p.err);
-          if (ok && J0 >= lo0 && J0 < hi0) {
-            tc_fence_after();
-            issue_s(0, dq0, dk);
+        int nq = 0, nvz = 0;        // units started; tail V tiles zeroed
+        for (int k = 0; ok && k * u_step < n_units; ++k) {
+          const int u = unit_index(k, u_first, u_step);
+          if (u >= n_units) continue;
+          const Unit U = make_unit<CAUSAL, VARLEN>(u, p, win_l, win_r);
+          if (U.kind != kRun) continue;
+          const int lo0 = U.lo0, hi0 = U.hi0, lo1 = U.lo1, hi1 = U.hi1, J0 = U.J0, J1 = U.J1;
+          // V of KV tile j (ring stage s, phase f) has landed (and, for a sequence's
+          // tail tile, been zeroed past the end: this thread, which follows the stage
+          // phases in order, tells warp 10 when the tail tile is in and waits for it
+          // to clear the rows).
+          auto wait_v = [&](int j, int s, uint32_t f) -> bool {
+            if (!mbar_wait(BAR(C::B_VF + s), f, abort_flag, p.err)) return false;
+            if (!(U.zero_v && j == U.j_tail)) return true;
+            mbar_arrive(BAR(C::B_VT));
+            const bool zeroed = mbar_wait(BAR(C::B_VZ), nvz & 1, abort_flag, p.err);
+            ++nvz;
+            return zeroed;
+          };
+          if (!(ok = mbar_wait(BAR(C::B_Q), nq & 1, abort_flag, p.err))) break;
+          ++nq;
+          bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
+          bool h1p = false;       // tile 1 uses KV tile j-1
+          bool first0 = true, first1 = true;
+          int sp = 0;             // ring stage of j-1
+          uint32_t pph = 0;       // and its phase
+          // S0_j is issued at the end of step j-1, right behind P0_{j-1} V_{j-1} (K_j
+          // having been waited for before P0_{j-1}): the thread's next tcgen05
+          // instruction after a P V product is the following S product, so the
+          // tensor pipe gets no gap there.
+          if (J0 < J1) {
+            ok = mbar_wait(BAR(C::B_KF + st), ph, abort_flag, p.err);
+            if (ok && J0 >= lo0 && J0 < hi0) {
+              tc_fence_after();
+              issue_s(0, dq0, dk + st * kStage16);
+            }
           }
+          for (int j = J0; ok && j < J1; ++j) {
+            const bool h0 = j >= lo0 && j < hi0, h1 = j >= lo1 && j < hi1;
+            const int st1 = st + 1 == ST ? 0 : st + 1;    // ring stage of j + 1
+            const uint32_t ph1 = st1 == 0 ? ph ^ 1 : ph;  // and its phase
+            const bool h0n = j + 1 >= lo0 && j + 1 < hi0;  // tile 0 uses KV tile j + 1
+            if (h1p) {
+              // O1 += P1_{j-1} V_{j-1}: tile 1 is the last user of V_{j-1}, so its stage is released
+              if (!(ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err))) break;
+              pf1 ^= 1;
+              if (!v_waited && !(ok = wait_v(j - 1, sp, pph))) break;
+              tc_fence_after();
+              issue_pv(1, first1, dv + sp * kStage16);
+              first1 = false;
+              tc_commit(BAR(C::B_VE + sp));
+            }
+            if (h1) {
+              tc_fence_after();
+              issue_s(1, dq1, dk + st * kStage16);
+            }
+            tc_commit(BAR(C::B_KE + st));  // both S products that read K_j are issued
+            v_waited = false;
+            if (j + 1 < J1 && !(ok = mbar_wait(BAR(C::B_KF + st1), ph1, abort_flag, p.err))) break;
+            if (h0) {
+              // O0 += P0_j V_j
+              if (!(ok = mbar_wait(BAR(C::B_PF + 0), pf0, abort_flag, p.err))) break;
+              pf0 ^= 1;
+              if (!(ok = wait_v(j, st, ph))) break;
+              v_waited = true;
+              tc_fence_after();
+              issue_pv(0, first0, dv + st * kStage16);
+              first0 = false;
+              if (!h1) tc_commit(BAR(C::B_VE + st));  // tile 1 does not use V_j
+              if (j == hi0 - 1) tc_commit(BAR(C::B_OD + 0));
+            } else if (!h1) {
+              // A tile between the two bands: nothing reads V_j.  Its copy must land
+              // before the stage is handed back for the next one.
+              if (!(ok = wait_v(j, st, ph))) break;
+              tc_commit(BAR(C::B_VE + st));
+            }
+            if (j + 1 < J1 && h0n) {
+              tc_fence_after();
+              issue_s(0, dq0, dk + st1 * kStage16);  // S0_{j+1}
+            }
+            h1p = h1;
+            sp = st;
+            pph = ph;
+            st = st1;
+            ph = ph1;
+          }
+          if (ok && h1p) {
+            // the last P1 V of tile 1 (its band ends the ring)
+            ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err) && (v_waited || wait_v(J1 - 1, sp, pph));
+            if (ok) {
+              pf1 ^= 1;
+              tc_fence_after();
+              issue_pv(1, first1, dv + sp * kStage16);
+              tc_commit(BAR(C::B_VE + sp));
+              tc_commit(BAR(C::B_OD + 1));
+            }
+          }
+          if (!ok) break;
+          // A query tile whose band holds no key: O is never written; the epilogue
+          // stores zeros for it.
+          if (lo0 >= hi0) tc_commit(BAR(C::B_OD + 0));
+          if (lo1 >= hi1) tc_commit(BAR(C::B_OD + 1));
         }
-        for (int j = J0; ok && j < J1; ++j) {
-          const bool h0 = j >= lo0 && j < hi0, h1 = j >= lo1 && j < hi1;
-          const int st1 = st + 1 == ST ? 0 : st + 1;          // ring stage of j + 1
-          const uint32_t ph1 = st1 == 0 ? ph ^ 1 : ph;        // and its phase
-          const bool h0n = j + 1 >= lo0 && j + 1 < hi0;       // tile 0 uses KV tile j + 1
-          if (h1p) {
-            // O1 += P1_{j-1} V_{j-1}: tile 1 is the last user of V_{j-1}, so its stage is released
-            if (!(ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err))) break;
-            pf1 ^= 1;
-            if (!v_waited && !(ok = wait_v(j - 1, sp, pph))) break;
-            tc_fence_after();
-            issue_pv(1, first1, dv + sp * kStage16);
-            first1 = false;
-            tc_commit(BAR(C::B_VE + sp));
-          }
-          if (h1) {
-            tc_fence_after();
-            issue_s(1, dq1, dk + st * kStage16);
-          }
-          tc_commit(BAR(C::B_KE + st));  // both S products that read K_j are issued
-          v_waited = false;
-          if (j + 1 < J1 && !(ok = mbar_wait(BAR(C::B_KF + st1), ph1, abort_flag, p.err))) break;
-          if (h0) {
-            // O0 += P0_j V_j
-            if (!(ok = mbar_wait(BAR(C::B_PF + 0), pf0, abort_flag, p.err))) break;
-            pf0 ^= 1;
-            if (!(ok = wait_v(j, st, ph))) break;
-            v_waited = true;
-            tc_fence_after();
-            issue_pv(0, first0, dv + st * kStage16);
-            first0 = false;
-            if (!h1) tc_commit(BAR(C::B_VE + st));  // tile 1 does not use V_j
-            if (j == hi0 - 1) tc_commit(BAR(C::B_OD + 0));
-          } else if (!h1) {
-            // A tile between the two bands: nothing reads V_j.  Its copy must land
-            // before the stage is handed back for the next one.
-            if (!(ok = wait_v(j, st, ph))) break;
-            tc_commit(BAR(C::B_VE + st));
-          }
-          if (j + 1 < J1 && h0n) {
-            tc_fence_after();
-            issue_s(0, dq0, dk + st1 * kStage16);  // S0_{j+1}
-          }
-          h1p = h1;
-          sp = st;
-          pph = ph;
-          st = st1;
-          ph = ph1;
-        }
-        if (ok && h1p) {
-          // the last P1 V of tile 1 (its band ends the ring)
-          ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err) && (v_waited || wait_v(J1 - 1, sp, pph));
-          if (ok) {
-            tc_fence_after();
-            issue_pv(1, first1, dv + sp * kStage16);
-            tc_commit(BAR(C::B_VE + sp));
-            tc_commit(BAR(C::B_OD + 1));
-          }
-        }
-        // A query tile whose band holds no key: O is never written; the epilogue
-        // stores zeros for it.
-        if (!has_t0) tc_commit(BAR(C::B_OD + 0));
-        if (!has_t1) tc_commit(BAR(C::B_OD + 1));
         tc_commit(BAR(C::B_DONE));
         mbar_wait(BAR(C::B_DONE), 0, nullptr, p.err);
       }
       __syncwarp();
     } else if (warp == 10) {
       // ---------------------------------------------------------- variable length: tail of V
-      if (zero_v) {
-        const int st = (j_tail - J0) % ST;  // ring position of the tail tile
-        const bool landed = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_VT), 0, abort_flag, p.err));
-        if (landed) {
-          const int r0 = Nkv % kBN;  // rows r0..127 of the tile lie past the sequence
-          uint8_t *vt = smem + C::OFF_V + st * C::KV_BYTES;
-          const int pieces = (kBN - r0) * 8;  // 16-byte pieces per 128-byte row chunk
-          for (int c = 0; c < C::KCH; ++c)
-            for (int i = lane; i < pieces; i += 32)
-              *reinterpret_cast<uint4 *>(vt + c * C::CHUNK_KV + (r0 + i / 8) * 128 + (i % 8) * 16) =
-                  make_uint4(0, 0, 0, 0);
-          fence_proxy_async_smem();  // make the zeros visible to the tensor core
-          __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(C::B_VZ));
+      if constexpr (VARLEN) {
+        int pos = 0, nvz = 0;  // ring position of the unit's first KV tile; tails zeroed
+        for (int k = 0; k * u_step < n_units; ++k) {
+          const int u = unit_index(k, u_first, u_step);
+          if (u >= n_units) continue;
+          const Unit U = make_unit<CAUSAL, VARLEN>(u, p, win_l, win_r);
+          if (U.kind != kRun) continue;
+          if (U.zero_v) {
+            const int st = (pos + U.j_tail - U.J0) % ST;  // ring stage of the tail tile
+            const bool landed = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_VT), nvz & 1, abort_flag, p.err));
+            ++nvz;
+            if (!landed) break;
+            const int r0 = U.Nkv % kBN;  // rows r0..127 of the tile lie past the sequence
+            uint8_t *vt = smem + C::OFF_V + st * C::KV_BYTES;
+            const int pieces = (kBN - r0) * 8;  // 16-byte pieces per 128-byte row chunk
+            for (int c = 0; c < C::KCH; ++c)
+              for (int i = lane; i < pieces; i += 32)
+                *reinterpret_cast<uint4 *>(vt + c * C::CHUNK_KV + (r0 + i / 8) * 128 + (i % 8) * 16) =
+                    make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();  // make the zeros visible to the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C::B_VZ));
+          }
+          pos += U.J1 - U.J0;
         }
       }
       __syncwarp();
@@ -479,130 +525,151 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                  // row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int q_tile0 = q0 + t * kBM;
-    const int q_row = q_tile0 + r;
     const float sl2 = p.scale_log2;
-    // ALiBi: score += -slope_h |i - j|, in base-2 units.
-    const bool alibi = MASKED && p.alibi_slopes != nullptr;
-    const float slope2 = alibi ? p.alibi_slopes[h] * 1.4426950408889634f : 0.f;
     const uint32_t scol = tmem + lane_off + C::s_col(t);
     const uint32_t ocol = tmem + lane_off + C::o_col(t);
-    float m = -INFINITY, l = 0.f;
+    using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
     bool ok = true;
-    // this warp's tile band as scalars (a runtime index into lo/hi would put them in local memory)
-    const int jlo = t == 0 ? lo[0] : lo[1], jhi = t == 0 ? hi[0] : hi[1];
-    for (int j = jlo; j < jhi; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF + t), (j - jlo) & 1, abort_flag, p.err));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tmem_ld_32x32b_x32(scol + i * 32, sr[i]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 4; ++i) reg_fence(sr[i]);
-
-      const int kv0 = j * kBN;
-      // Masked only where the tile crosses the end of the keys or a band edge.
-      const bool need_mask = (kv0 + kBN > Nkv) || (win_r != kUnlimited && kv0 + kBN - 1 > q_tile0 + win_r) ||
-                             (win_l != kUnlimited && kv0 < q_tile0 + kBM - 1 - win_l);
-      if (need_mask) {
-        // columns lo_c <= c < hi_c are kept
-        const int hi_c = (win_r == kUnlimited ? Nkv : min(Nkv, q_row + win_r + 1)) - kv0;
-        const int lo_c = win_l == kUnlimited ? 0 : q_row - win_l - kv0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (i * 32 + c >= hi_c || i * 32 + c < lo_c) sr[i][c] = __float_as_uint(-INFINITY);
-      }
-      float sl_eff = sl2;  // factor from the values in sr to base-2 scores
-      if (alibi) {
-        const float dq = static_cast<float>(q_row - kv0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            sr[i][c] = __float_as_uint(
-                fmaf(__uint_as_float(sr[i][c]), sl2, -slope2 * fabsf(dq - static_cast<float>(i * 32 + c))));
-        sl_eff = 1.f;
-      }
-      // Row max: four independent chains of 3-input maxima.
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 32; c += 8)
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            mq[u] = fmax3(mq[u], __uint_as_float(sr[i][c + 2 * u]), __uint_as_float(sr[i][c + 2 * u + 1]));
-      const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-      // Raise the running max only when the block max exceeds it by more than
-      // the threshold; otherwise keep it (alpha = 1, no rescale of O).
-      const float mb = mx * sl_eff;
-      const bool raise = (m == -INFINITY) || (mb > m + kRescaleThreshold);
-      const float m_new = raise ? fmaxf(m, mb) : m;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = raise ? fast_exp2(m - m_use) : 1.f;
-      // P = 2^(s * scale * log2 e - m), two columns per packed FMA; row sum in
-      // four packed partial sums.
-      const uint64_t sl2x2 = pack_f2(sl_eff, sl_eff), negm2 = pack_f2(-m_use, -m_use);
-      uint64_t rs2[4] = {0, 0, 0, 0};
-      uint32_t pk[2][32];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const uint64_t e2 = ffma_f2(pack_f2(__uint_as_float(sr[i][c]), __uint_as_float(sr[i][c + 1])), sl2x2, negm2);
-          float p0, p1;
-          if (((c >> 1) & 3) < kPolyPairsOf4) {
-            const float2 e = unpack_f2(exp2_poly_f2(e2));
-            p0 = e.x;
-            p1 = e.y;
-          } else {
-            const float2 e = unpack_f2(e2);
-            p0 = fast_exp2(e.x);
-            p1 = fast_exp2(e.y);
+    uint32_t sf = 0, od = 0;  // parities of this tile's S-ready and O-done barriers
+    for (int k = 0; ok && k * u_step < n_units; ++k) {
+      const int u = unit_index(k, u_first, u_step);
+      if (u >= n_units) continue;
+      int q_tile0, Nkv, jlo, jhi;
+      float slope2;
+      {
+        // Only what the step loop needs stays live through it; the epilogue
+        // derives the unit again (cheap integer work, fewer registers held).
+        const Unit U = make_unit<CAUSAL, VARLEN>(u, p, win_l, win_r);
+        q_tile0 = U.q0 + t * kBM;
+        Nkv = U.Nkv;
+        jlo = t == 0 ? U.lo0 : U.lo1;
+        jhi = t == 0 ? U.hi0 : U.hi1;
+        // ALiBi: score += -slope_h |i - j|, in base-2 units.
+        slope2 = (MASKED && p.alibi_slopes != nullptr && U.kind == kRun)
+                     ? p.alibi_slopes[U.h] * 1.4426950408889634f : 0.f;
+        if (U.kind != kRun) {
+          const int q_row = q_tile0 + r;
+          if ((U.kind & kBadIndex) && threadIdx.x == 0) atomicOr(p.err, kErrBadIndex);
+          if (U.kind == kEmpty && q_row < U.Nq) {
+            // No keys: O = 0 and LSE = -inf for this row.
+            T *orow = reinterpret_cast<T *>(p.o) + static_cast<int64_t>(U.h) * p.o_sh +
+                      static_cast<int64_t>(U.q_base + q_row) * p.o_sn;
+            for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4 *>(orow + d) = make_uint4(0, 0, 0, 0);
+            if (p.lse != nullptr) p.lse[static_cast<int64_t>(U.h) * p.total_q + U.q_base + q_row] = -INFINITY;
           }
-          rs2[(c >> 1) & 3] = fadd_f2(rs2[(c >> 1) & 3], pack_f2(p0, p1));
-          pk[i >> 1][(i & 1) * 16 + c / 2] = pack2<BF16>(p0, p1);
-        }
-      const float2 r01 = unpack_f2(fadd_f2(rs2[0], rs2[1])), r23 = unpack_f2(fadd_f2(rs2[2], rs2[3]));
-      const float rs = (r01.x + r01.y) + (r23.x + r23.y);
-      l = l * alpha + rs;
-      m = m_new;
-      // P_i(j) over the first 64 columns of S_i (S_i(j) is already in registers).
-      tmem_st_32x32b_x32(scol, pk[0]);
-      tmem_st_32x32b_x32(scol + 32, pk[1]);
-      // P_i(j-1) V_{j-1} completed before S_i(j) was signalled: O_i is stable.
-      if (j > jlo && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-          uint32_t ov[32];
-          tmem_ld_32x32b_x32(ocol + i * 32, ov);
-          tmem_wait_ld();
-          reg_fence(ov);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-          tmem_st_32x32b_x32(ocol + i * 32, ov);
+          continue;
         }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(C::B_PF + t));
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OD + t), 0, abort_flag, p.err));
-    if (ok) {
+      const int q_row = q_tile0 + r;
+      const bool alibi = MASKED && p.alibi_slopes != nullptr;
+      float m = -INFINITY, l = 0.f;
+      for (int j = jlo; j < jhi; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF + t), sf, abort_flag, p.err));
+        sf ^= 1;
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmem_ld_32x32b_x32(scol + i * 32, sr[i]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) reg_fence(sr[i]);
+
+        const int kv0 = j * kBN;
+        // Masked only where the tile crosses the end of the keys or a band edge.
+        const bool need_mask = (kv0 + kBN > Nkv) || (win_r != kUnlimited && kv0 + kBN - 1 > q_tile0 + win_r) ||
+                               (win_l != kUnlimited && kv0 < q_tile0 + kBM - 1 - win_l);
+        if (need_mask) {
+          // columns lo_c <= c < hi_c are kept
+          const int hi_c = (win_r == kUnlimited ? Nkv : min(Nkv, q_row + win_r + 1)) - kv0;
+          const int lo_c = win_l == kUnlimited ? 0 : q_row - win_l - kv0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (i * 32 + c >= hi_c || i * 32 + c < lo_c) sr[i][c] = __float_as_uint(-INFINITY);
+        }
+        float sl_eff = sl2;  // factor from the values in sr to base-2 scores
+        if (alibi) {
+          const float dq = static_cast<float>(q_row - kv0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              sr[i][c] = __float_as_uint(
+                  fmaf(__uint_as_float(sr[i][c]), sl2, -slope2 * fabsf(dq - static_cast<float>(i * 32 + c))));
+          sl_eff = 1.f;
+        }
+        // Row max: four independent chains of 3-input maxima.
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int c = 0; c < 32; c += 8)
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              mq[w] = fmax3(mq[w], __uint_as_float(sr[i][c + 2 * w]), __uint_as_float(sr[i][c + 2 * w + 1]));
+        const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+        // Raise the running max only when the block max exceeds it by more than
+        // the threshold; otherwise keep it (alpha = 1, no rescale of O).
+        const float mb = mx * sl_eff;
+        const bool raise = (m == -INFINITY) || (mb > m + kRescaleThreshold);
+        const float m_new = raise ? fmaxf(m, mb) : m;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = raise ? fast_exp2(m - m_use) : 1.f;
+        // P = 2^(s * scale * log2 e - m), two columns per packed FMA; row sum in
+        // four packed partial sums.
+        const uint64_t sl2x2 = pack_f2(sl_eff, sl_eff), negm2 = pack_f2(-m_use, -m_use);
+        uint64_t rs2[4] = {0, 0, 0, 0};
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const uint64_t e2 =
+                ffma_f2(pack_f2(__uint_as_float(sr[i][c]), __uint_as_float(sr[i][c + 1])), sl2x2, negm2);
+            const float2 e = unpack_f2(e2);
+            const float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+            rs2[(c >> 1) & 3] = fadd_f2(rs2[(c >> 1) & 3], pack_f2(p0, p1));
+            pk[i >> 1][(i & 1) * 16 + c / 2] = pack2<BF16>(p0, p1);
+          }
+        const float2 r01 = unpack_f2(fadd_f2(rs2[0], rs2[1])), r23 = unpack_f2(fadd_f2(rs2[2], rs2[3]));
+        const float rs = (r01.x + r01.y) + (r23.x + r23.y);
+        l = l * alpha + rs;
+        m = m_new;
+        // P_i(j) over the first 64 columns of S_i (S_i(j) is already in registers).
+        tmem_st_32x32b_x32(scol, pk[0]);
+        tmem_st_32x32b_x32(scol + 32, pk[1]);
+        // P_i(j-1) V_{j-1} completed before S_i(j) was signalled: O_i is stable.
+        if (j > jlo && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) {
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(ocol + i * 32, ov);
+            tmem_wait_ld();
+            reg_fence(ov);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+            tmem_st_32x32b_x32(ocol + i * 32, ov);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::B_PF + t));
+      }
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OD + t), od, abort_flag, p.err));
+      od ^= 1;
+      if (!ok) break;
       // -------------------------------------------------------- epilogue: O / l, LSE
       tc_fence_after();
+      const Unit U = make_unit<CAUSAL, VARLEN>(u, p, win_l, win_r);
       // A row whose band holds no key (possible with windows) gets O = 0, LSE = -inf.
       const bool any_key = l > 0.f;
       const float inv_l = any_key ? 1.f / l : 0.f;
-      const bool row_ok = q_row < Nq;
-      using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-      T *orow = reinterpret_cast<T *>(p.o) + static_cast<int64_t>(bc) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
-                static_cast<int64_t>(q_base + q_row) * p.o_sn;
+      const bool row_ok = q_row < U.Nq;
+      T *orow = reinterpret_cast<T *>(p.o) + static_cast<int64_t>(U.bc) * p.o_sb +
+                static_cast<int64_t>(U.h) * p.o_sh + static_cast<int64_t>(U.q_base + q_row) * p.o_sn;
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) {
         uint32_t ov[32];
@@ -622,9 +689,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (p.lse != nullptr && row_ok)
-        p.lse[VARLEN ? static_cast<int64_t>(h) * p.total_q + q_base + q_row
-                     : (static_cast<int64_t>(b) * p.Hq + h) * p.Nq + q_row] =
+        p.lse[VARLEN ? static_cast<int64_t>(U.h) * p.total_q + U.q_base + q_row
+                     : (static_cast<int64_t>(U.b) * p.Hq + U.h) * p.Nq + q_row] =
             any_key ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      // The O columns are read: the next unit's first P V may overwrite them once
+      // this warp's next P-ready arrival (after tc_fence_before) says so.
     }
   }
 
@@ -649,7 +718,7 @@ cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   if (attr.numRegs * kThreads < 256 * kSoftmaxRegs + 128 * kOtherRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(p.Hq, B, p.n_qtiles);
+  dim3 grid(p.n_ctas);  // persistent: at most one CTA per SM (n_ctas <= number of SMs)
   kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -4,6 +4,8 @@
     python -m attention_fa2_fwd_gb300.run_case decode  [--B 64 --Hq 32 --Hkv 8 --L 8192 --D 128]
     python -m attention_fa2_fwd_gb300.run_case decode_paged [--page-size 16 --ragged 1 ...]
     python -m attention_fa2_fwd_gb300.run_case bwd     [prefill sizes; FLOPs counted as 2.5 x the forward]
+    python -m attention_fa2_fwd_gb300.run_case cross   [--D 64|128: the cross-attention workload, B=4 H_q=16
+                                                        H_kv=4 N_q=1024 N_kv=4096, (B,N,H,D) memory, non-causal]
     prefill / decode / decode_paged also take --window-left W and --alibi 1 (sliding window, ALiBi slopes)
 
 Inputs are seeded N(0,1) bf16 tensors drawn on the device.  Each iteration is
@@ -23,7 +25,7 @@ import attention_fa2_fwd_gb300 as A
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=("prefill", "decode", "decode_paged", "bwd"))
+    ap.add_argument("kind", choices=("prefill", "decode", "decode_paged", "bwd", "cross"))
     ap.add_argument("--B", type=int)
     ap.add_argument("--Hq", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=8)
@@ -64,6 +66,21 @@ def main():
 
         def call():
             A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse, window=(wl, -1), alibi_slopes=slopes)
+        unit, scale = "TFLOPS", 1e12
+    elif a.kind == "cross":
+        import attention_fa2_fwd_gb300.inputs as I
+        w = I.CROSS[a.D]
+        g2 = torch.Generator(device=dev).manual_seed(42)
+        # the workload's distributions (Q ~ N(0,1), K ~ N(0,2), V ~ U(-1,1)), drawn on the device, in its layout
+        q = I.to_layout(torch.randn((w.B, w.Hq, w.Nq, w.D), generator=g2, device=dev).to(dt), w.layout)
+        k = I.to_layout((torch.randn((w.B, w.Hkv, w.Nkv, w.D), generator=g2, device=dev) * 2 ** 0.5).to(dt), w.layout)
+        v = I.to_layout((torch.rand((w.B, w.Hkv, w.Nkv, w.D), generator=g2, device=dev) * 2 - 1).to(dt), w.layout)
+        o = I.to_layout(torch.empty_like(q), w.layout)
+        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        work = w.flops
+
+        def call():
+            A.prefill(q, k, v, causal=False, out=o, lse_out=lse)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "bwd":
         B = a.B or 2
