@@ -364,6 +364,7 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
   if (B < 1 || H_q < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
   if (H_q % H_kv != 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f) || B > 65535 || H_q > 65535) return ATTN_ERR_INVALID_ARG;
+  if ((N_q + 127) / 128 > 65535 || (N_kv + 127) / 128 > 65535) return ATTN_ERR_INVALID_ARG;  // grid z
   if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3))

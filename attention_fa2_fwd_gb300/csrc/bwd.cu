@@ -131,8 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = (p.Nq + kT - 1) / kT;
-  const int qt = CAUSAL ? (n_qt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int h = blockIdx.y, b = blockIdx.z;
+  // Grid (H_q, B, query tiles), heads first: under the causal mask every CTA
+  // of the longest query tile starts before any shorter one.
+  const int qt = CAUSAL ? (n_qt - 1 - static_cast<int>(blockIdx.z)) : static_cast<int>(blockIdx.z);
+  const int h = blockIdx.x, b = blockIdx.y;
   const int hk = h / p.group;
   const int q0 = qt * kT;
   const int nkv_all = (p.Nkv + kT - 1) / kT;
@@ -328,8 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_kt = (p.Nkv + kT - 1) / kT;
-  const int kt = CAUSAL ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int hk = blockIdx.y, b = blockIdx.z;
+  // Grid (H_kv, B, key tiles), heads first: under the causal mask key tile 0
+  // sees every query tile, so the longest CTAs all start first.
+  const int kt = static_cast<int>(blockIdx.z);
+  const int hk = blockIdx.x, b = blockIdx.y;
   const int kv0 = kt * kT;
   const int n_qt = (p.Nq + kT - 1) / kT;
   // Query tiles that see this key tile: causal (top-left) keeps key j for query i iff j <= i.
@@ -543,7 +547,7 @@ cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv,
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
         cudaSuccess)
       return e;
-    kern<<<dim3((p.Nq + kT - 1) / kT, p.Hq, B), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
+    kern<<<dim3(p.Hq, B, (p.Nq + kT - 1) / kT), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
@@ -552,7 +556,7 @@ cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv,
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
         cudaSuccess)
       return e;
-    kern<<<dim3((p.Nkv + kT - 1) / kT, Hkv, B), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
+    kern<<<dim3(Hkv, B, (p.Nkv + kT - 1) / kT), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
     e = cudaGetLastError();
   }
   return e;
