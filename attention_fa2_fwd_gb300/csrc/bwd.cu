@@ -13,15 +13,25 @@
 //   bwd_preprocess  D_i = rowsum(dO o O), fp32, into the workspace;
 //   bwd_dq          one CTA per (128-row query tile, q head, b): for each KV
 //                   tile, S = Q K^T and dP = dO V^T (tcgen05, SS), then
-//                   dS in a softmax-like warpgroup, then dQ += dS K (TS form,
-//                   dS read from TMEM, K as an MN-major operand);
+//                   dS elementwise, then dQ += dS K (TS form, dS read from
+//                   TMEM, K as an MN-major operand);
 //   bwd_dkdv        one CTA per (128-row key tile, kv head, b): for each q head
 //                   of the group and each query tile, S^T = K Q^T and
 //                   dP^T = V dO^T, then P^T and dS^T per key row, then
 //                   dV += P^T dO and dK += dS^T Q (TS form), with dK and dV
 //                   accumulated in TMEM over the whole group.
+// Each 128-wide tile of the loop (KV tile for dQ, query tile for dK/dV) is
+// computed as two 64-column halves a and b with their own TMEM columns,
+// barriers and elementwise warpgroup, issued in the order
+//   Sa_j dPa_j | Sb_j dPb_j | acc_a_j | Sa_{j+1} dPa_{j+1} | acc_b_j | Sb_{j+1} ...
+// so that the elementwise work on one half runs while the tensor core
+// computes the other half's products (the elementwise work has no row
+// reduction, so the halves are independent).
 // Warp roles in both tiled kernels: warp 0 TMA producer, warp 1 TMEM allocator
-// and MMA issuer, warps 2-5 elementwise warpgroup (one thread per TMEM lane).
+// and MMA issuer, warps 2-5 the elementwise warpgroup of half a, warps 6-9 the
+// one of half b (one thread per TMEM lane in each).  A half writes its 16-bit
+// results over the first 32 of its 64 score columns, where the following
+// TS-form MMA reads them.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -32,7 +42,7 @@ namespace attn {
 namespace {
 
 constexpr int kT = 128;  // rows per tile (queries or keys)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, int d, int n, int h, int b,
@@ -55,14 +65,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-template <bool BF16>
-__device__ __forceinline__ float to_f(const void *p, int64_t i) {
-  if constexpr (BF16)
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p)[i]);
-  else
-    return __half2float(reinterpret_cast<const __half *>(p)[i]);
-}
-
 // Stores 32 fp32 accumulator columns (times s) of one row as 16-bit values.
 template <bool BF16>
 __device__ __forceinline__ void store_row32(void *base, int64_t off, const uint32_t (&v)[32], float s) {
@@ -76,22 +78,51 @@ __device__ __forceinline__ void store_row32(void *base, int64_t off, const uint3
 }
 
 // ---------------------------------------------------------------- preprocess
+// 8 values of two 16-byte vectors (16-bit elements) multiplied and summed in fp32.
+template <bool BF16>
+__device__ __forceinline__ float dot8(const uint4 &a, const uint4 &b) {
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 x, y;
+    if constexpr (BF16) {
+      x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&av[i]));
+      y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&bv[i]));
+    } else {
+      x = __half22float2(*reinterpret_cast<const __half2 *>(&av[i]));
+      y = __half22float2(*reinterpret_cast<const __half2 *>(&bv[i]));
+    }
+    acc = fmaf(x.x, y.x, acc);
+    acc = fmaf(x.y, y.y, acc);
+  }
+  return acc;
+}
+
+// D_i = sum_d dO[i, d] * O[i, d] in fp32.  D / 8 lanes per row, one 16-byte
+// load of each tensor per lane, so a warp reads 32 / (D / 8) whole rows at once.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
-  // One warp per row: D_i = sum_d dO[i, d] * O[i, d] in fp32.
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   if (load_volatile(p.err) != 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y, b = blockIdx.z;
-  const int row = blockIdx.x * 8 + warp;
-  if (row >= p.Nq) return;
-  const int64_t oo = static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(h) * p.o_sh + static_cast<int64_t>(row) * p.o_sn;
-  const int64_t od = static_cast<int64_t>(b) * p.do_sb + static_cast<int64_t>(h) * p.do_sh + static_cast<int64_t>(row) * p.do_sn;
+  const int row = (blockIdx.x * 8 + warp) * kRowsPerWarp + lane / kLanesPerRow;
+  const int part = lane % kLanesPerRow;
   float acc = 0.f;
+  if (row < p.Nq) {
+    const int64_t oo = static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
+                       static_cast<int64_t>(row) * p.o_sn + part * 8;
+    const int64_t od = static_cast<int64_t>(b) * p.do_sb + static_cast<int64_t>(h) * p.do_sh +
+                       static_cast<int64_t>(row) * p.do_sn + part * 8;
+    const uint4 o = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.o) + oo);
+    const uint4 g = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.dout) + od);
+    acc = dot8<BF16>(o, g);
+  }
 #pragma unroll
-  for (int d = lane; d < D; d += 32) acc = fmaf(to_f<BF16>(p.o, oo + d), to_f<BF16>(p.dout, od + d), acc);
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) p.dvec[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row] = acc;
+  for (int off = kLanesPerRow / 2; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (part == 0 && row < p.Nq) p.dvec[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row] = acc;
 }
 
 // ---------------------------------------------------------------- dQ
@@ -103,12 +134,17 @@ struct DqCfg {
   static constexpr uint32_t TILE = kT * D * 2;
   static constexpr uint32_t OFF_Q = 0, OFF_DO = TILE, OFF_KV = 2 * TILE;  // stage s: K at OFF_KV + 2s TILE, V after
   static constexpr uint32_t OFF_BAR = OFF_KV + ST * 2 * TILE;
-  static constexpr int B_QF = 0, B_KF = 1, B_KE = 1 + ST, B_SF = 1 + 2 * ST, B_DS = 2 + 2 * ST, B_DONE = 3 + 2 * ST,
-                       B_MMA = 4 + 2 * ST, NBAR = 5 + 2 * ST;
+  // B_SF, B_DS: + half (2)
+  static constexpr int B_QF = 0, B_KF = 1, B_KE = 1 + ST, B_SF = 1 + 2 * ST, B_DS = 3 + 2 * ST, B_DONE = 5 + 2 * ST,
+                       B_MMA = 6 + 2 * ST, NBAR = 7 + 2 * ST;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
   static constexpr uint32_t SMEM_BYTES = (SMEM_USED + 1024 > 116u * 1024) ? SMEM_USED + 1024 : 116u * 1024;
-  static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256, TMEM_COLS = 512;
+  // TMEM: half h's S at 128 h, its dP at 128 h + 64; dQ after both halves.
+  static constexpr uint32_t DQ_COL = 256, TMEM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t s_col(int h) { return 128u * h; }
+  __host__ __device__ static constexpr uint32_t dp_col(int h) { return 128u * h + 64; }
+  static constexpr uint32_t HALF_ROWS = 64 * 128;  // bytes of 64 rows in one 64-column chunk of a K or V tile
   static_assert(SMEM_BYTES <= 227u * 1024, "shared memory budget");
 };
 
@@ -146,8 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::B_KF + s), 1);
       mbar_init(BAR(C::B_KE + s), 1);
     }
-    mbar_init(BAR(C::B_SF), 1);
-    mbar_init(BAR(C::B_DS), 4);
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(BAR(C::B_SF + hf), 1);
+      mbar_init(BAR(C::B_DS + hf), 4);  // one arrival per warp of the half's warpgroup
+    }
     mbar_init(BAR(C::B_DONE), 1);
     mbar_init(BAR(C::B_MMA), 1);
     *abort_flag = 0;
@@ -196,30 +234,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(BF16, kT, kT, false, false);
+      constexpr uint32_t idesc_s = idesc_f16(BF16, kT, 64, false, false);  // N = 64 keys (one half)
       constexpr uint32_t idesc_dq = idesc_f16(BF16, kT, D, false, true);
-      bool ok = mbar_wait(BAR(C::B_QF), 0, abort_flag, p.err);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % ST;
-        if (!(ok = mbar_wait(BAR(C::B_KF + st), (j / ST) & 1, abort_flag, p.err))) break;
+      // S_h = Q K_h^T and dP_h = dO V_h^T for keys 64 h .. 64 h + 63 of the tile in stage st.
+      auto issue_sdp = [&](int hf, int st) {
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss(tmem + C::S_COL, smem_desc_sw128(sQ + ko, 16, 1024), smem_desc_sw128(sK(st) + ko, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
-          mma_ss(tmem + C::DP_COL, smem_desc_sw128(sDO + ko, 16, 1024), smem_desc_sw128(sV(st) + ko, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::s_col(hf), smem_desc_sw128(sQ + ko, 16, 1024),
+                 smem_desc_sw128(sK(st) + hf * C::HALF_ROWS + ko, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::dp_col(hf), smem_desc_sw128(sDO + ko, 16, 1024),
+                 smem_desc_sw128(sV(st) + hf * C::HALF_ROWS + ko, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
-        tc_commit(BAR(C::B_SF));
-        if (!(ok = mbar_wait(BAR(C::B_DS), j & 1, abort_flag, p.err))) break;
+        tc_commit(BAR(C::B_SF + hf));
+      };
+      // dQ += dS_h K_h: dS_h (16-bit) over the first 32 columns of S_h; K as MN-major B.
+      auto issue_dq = [&](int hf, int st, bool first) {
         tc_fence_after();
-        // dQ += dS K_j: dS (16-bit) over the first 64 columns of S; K as MN-major B.
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts(tmem + C::DQ_COL, tmem + C::S_COL + kk * 8, smem_desc_sw128(sK(st) + kk * 16 * 128, C::CHUNK, 1024),
-                 idesc_dq, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(BAR(C::B_KE + st));
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + C::DQ_COL, tmem + C::s_col(hf) + kk * 8,
+                 smem_desc_sw128(sK(st) + (hf * 4 + kk) * 16 * 128, C::CHUNK, 1024), idesc_dq,
+                 (!first || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(BAR(C::B_QF), 0, abort_flag, p.err);
+      if (ok && n_kv > 0) {
+        ok = mbar_wait(BAR(C::B_KF + 0), 0, abort_flag, p.err);
+        if (ok) issue_sdp(0, 0);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % ST, sp = (j + ST - 1) % ST;
+        if (j > 0) {
+          // dQ += dS_b K_b of tile j-1, which then releases its stage
+          if (!(ok = mbar_wait(BAR(C::B_DS + 1), (j - 1) & 1, abort_flag, p.err))) break;
+          issue_dq(1, sp, false);
+          tc_commit(BAR(C::B_KE + sp));
+        }
+        issue_sdp(1, st);
+        if (!(ok = mbar_wait(BAR(C::B_DS + 0), j & 1, abort_flag, p.err))) break;
+        issue_dq(0, st, j == 0);
+        if (j + 1 < n_kv) {
+          const int sn = (j + 1) % ST;
+          if (!(ok = mbar_wait(BAR(C::B_KF + sn), ((j + 1) / ST) & 1, abort_flag, p.err))) break;
+          issue_sdp(0, sn);
+        }
+      }
+      if (ok && n_kv > 0) {
+        const int sl = (n_kv - 1) % ST;
+        ok = mbar_wait(BAR(C::B_DS + 1), (n_kv - 1) & 1, abort_flag, p.err);
+        if (ok) {
+          issue_dq(1, sl, false);
+          tc_commit(BAR(C::B_KE + sl));
+        }
       }
       if (ok) tc_commit(BAR(C::B_DONE));
       tc_commit(BAR(C::B_MMA));
@@ -228,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // columns half * 64 .. + 63 of each tile
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int q_row = q0 + r;
@@ -238,42 +306,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF), j & 1, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF + half), j & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      const int kv0 = j * kT;
+      const int kv0 = j * kT + half * 64;  // this half's first key
       const int lim = row_ok ? ((CAUSAL ? min(p.Nkv, q_row + 1) : p.Nkv) - kv0) : 0;  // columns c < lim count
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = ch * 32;
         uint32_t sv[32], pv[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + C::S_COL + ch * 32, sv);
-        tmem_ld_32x32b_x32(tmem + lane_off + C::DP_COL + ch * 32, pv);
+        tmem_ld_32x32b_x32(tmem + lane_off + C::s_col(half) + c0, sv);
+        tmem_ld_32x32b_x32(tmem + lane_off + C::dp_col(half) + c0, pv);
         tmem_wait_ld();
         reg_fence(sv);
         reg_fence(pv);
         uint32_t ds[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const int cc = ch * 32 + c;
+          const int cc = c0 + c;
           const float p0 = (cc < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -lse2)) : 0.f;
           const float p1 = (cc + 1 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse2)) : 0.f;
           ds[c / 2] = pack2<BF16>(p0 * (__uint_as_float(pv[c]) - dv), p1 * (__uint_as_float(pv[c + 1]) - dv));
         }
-        // dS over S's first 64 columns; chunk ch only overwrites columns already read.
-        tmem_st_32x32b_x16(tmem + lane_off + C::S_COL + ch * 16, ds);
+        // dS over the first 32 of this half's S columns; chunk ch only overwrites columns already read.
+        tmem_st_32x32b_x16(tmem + lane_off + C::s_col(half) + ch * 16, ds);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(C::B_DS));
+      if (lane == 0) mbar_arrive(BAR(C::B_DS + half));
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_DONE), 0, abort_flag, p.err));
     if (ok) {
       tc_fence_after();
       const int64_t orow = static_cast<int64_t>(b) * p.dq_sb + static_cast<int64_t>(h) * p.dq_sh +
                            static_cast<int64_t>(q_row) * p.dq_sn;
+      // each half stores half of dQ's columns
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
+      for (int i = half * (D / 64); i < (half + 1) * (D / 64); ++i) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem + lane_off + C::DQ_COL + i * 32, v);
         tmem_wait_ld();
@@ -298,14 +368,20 @@ struct DkvCfg {
   static constexpr uint32_t CHUNK = kT * 128;
   static constexpr uint32_t TILE = kT * D * 2;
   static constexpr uint32_t OFF_K = 0, OFF_V = TILE, OFF_QD = 2 * TILE;  // stage s: Q at OFF_QD + 2s TILE, dO after
-  static constexpr uint32_t OFF_LD = OFF_QD + ST * 2 * TILE;              // fp32 [2][2][128]: (lse2, D) per step parity
-  static constexpr uint32_t OFF_BAR = OFF_LD + 2 * 2 * kT * 4;
-  static constexpr int B_KVF = 0, B_QF = 1, B_QE = 1 + ST, B_SF = 1 + 2 * ST, B_DS = 2 + 2 * ST,
-                       B_LD = 3 + 2 * ST /* +2 */, B_DONE = 5 + 2 * ST, B_MMA = 6 + 2 * ST, NBAR = 7 + 2 * ST;
+  // fp32 [half][step parity][lse2 | D][64]: the 64 queries of each half
+  static constexpr uint32_t OFF_LD = OFF_QD + ST * 2 * TILE;
+  static constexpr uint32_t OFF_BAR = OFF_LD + 2 * 2 * 2 * 64 * 4;
+  // B_SF, B_DS: + half (2); B_LD: + 2 half + step parity (4)
+  static constexpr int B_KVF = 0, B_QF = 1, B_QE = 1 + ST, B_SF = 1 + 2 * ST, B_DS = 3 + 2 * ST,
+                       B_LD = 5 + 2 * ST, B_DONE = 9 + 2 * ST, B_MMA = 10 + 2 * ST, NBAR = 11 + 2 * ST;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
   static constexpr uint32_t SMEM_BYTES = (SMEM_USED + 1024 > 116u * 1024) ? SMEM_USED + 1024 : 116u * 1024;
-  static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D, TMEM_COLS = 512;
+  // TMEM: half h's S^T at 128 h, its dP^T at 128 h + 64; dV and dK after both halves.
+  static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D, TMEM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t s_col(int h) { return 128u * h; }
+  __host__ __device__ static constexpr uint32_t dp_col(int h) { return 128u * h + 64; }
+  static constexpr uint32_t HALF_ROWS = 64 * 128;  // bytes of 64 rows in one 64-column chunk of a Q or dO tile
   static_assert(SMEM_BYTES <= 227u * 1024, "shared memory budget");
   static_assert(256 + 2 * D <= TMEM_COLS, "TMEM budget");
 };
@@ -326,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
-  float *sld = reinterpret_cast<float *>(smem + C::OFF_LD);  // [parity][lse2 | D][128]
+  float *sld = reinterpret_cast<float *>(smem + C::OFF_LD);  // [half][parity][lse2 | D][64]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_kt = (p.Nkv + kT - 1) / kT;
@@ -348,10 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::B_QF + s), 1);
       mbar_init(BAR(C::B_QE + s), 1);
     }
-    mbar_init(BAR(C::B_SF), 1);
-    mbar_init(BAR(C::B_DS), 4);
-    mbar_init(BAR(C::B_LD + 0), 128);
-    mbar_init(BAR(C::B_LD + 1), 128);
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(BAR(C::B_SF + hf), 1);
+      mbar_init(BAR(C::B_DS + hf), 4);  // one arrival per warp of the half's warpgroup
+      mbar_init(BAR(C::B_LD + 2 * hf + 0), 128);
+      mbar_init(BAR(C::B_LD + 2 * hf + 1), 128);
+    }
     mbar_init(BAR(C::B_DONE), 1);
     mbar_init(BAR(C::B_MMA), 1);
     *abort_flag = 0;
@@ -401,35 +479,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(BF16, kT, kT, false, false);
+      constexpr uint32_t idesc_s = idesc_f16(BF16, kT, 64, false, false);  // N = 64 queries (one half)
       constexpr uint32_t idesc_acc = idesc_f16(BF16, kT, D, false, true);
-      bool ok = mbar_wait(BAR(C::B_KVF), 0, abort_flag, p.err);
-      for (int s = 0; ok && s < n_steps; ++s) {
-        const int st = s % ST;
-        if (!(ok = mbar_wait(BAR(C::B_QF + st), (s / ST) & 1, abort_flag, p.err))) break;
+      // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for queries 64 h .. 64 h + 63 of the tile in stage st:
+      // keys on the TMEM lanes, queries on the columns.
+      auto issue_sdp = [&](int hf, int st) {
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          // S^T = K Q^T and dP^T = V dO^T: keys on the TMEM lanes, queries on the columns.
-          mma_ss(tmem + C::S_COL, smem_desc_sw128(sK + ko, 16, 1024), smem_desc_sw128(sQ(st) + ko, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
-          mma_ss(tmem + C::DP_COL, smem_desc_sw128(sV + ko, 16, 1024), smem_desc_sw128(sDO(st) + ko, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::s_col(hf), smem_desc_sw128(sK + ko, 16, 1024),
+                 smem_desc_sw128(sQ(st) + hf * C::HALF_ROWS + ko, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::dp_col(hf), smem_desc_sw128(sV + ko, 16, 1024),
+                 smem_desc_sw128(sDO(st) + hf * C::HALF_ROWS + ko, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
-        tc_commit(BAR(C::B_SF));
-        if (!(ok = mbar_wait(BAR(C::B_DS), s & 1, abort_flag, p.err))) break;
+        tc_commit(BAR(C::B_SF + hf));
+      };
+      // dV += P^T_h dO_h and dK += dS^T_h Q_h: P^T_h / dS^T_h (16-bit) over the first 32
+      // columns of S^T_h / dP^T_h, dO / Q as MN-major B (queries 64 h .. of the tile).
+      auto issue_acc = [&](int hf, int st, bool first) {
         tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q: P^T / dS^T (16-bit) from TMEM, dO / Q as MN-major B.
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk) {
-          const uint32_t bo = kk * 16 * 128;
-          mma_ts(tmem + C::DV_COL, tmem + C::S_COL + kk * 8, smem_desc_sw128(sDO(st) + bo, C::CHUNK, 1024),
-                 idesc_acc, (s > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + kk * 8, smem_desc_sw128(sQ(st) + bo, C::CHUNK, 1024),
-                 idesc_acc, (s > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t bo = (hf * 4 + kk) * 16 * 128;
+          mma_ts(tmem + C::DV_COL, tmem + C::s_col(hf) + kk * 8, smem_desc_sw128(sDO(st) + bo, C::CHUNK, 1024),
+                 idesc_acc, (!first || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DK_COL, tmem + C::dp_col(hf) + kk * 8, smem_desc_sw128(sQ(st) + bo, C::CHUNK, 1024),
+                 idesc_acc, (!first || kk > 0) ? 1u : 0u);
         }
-        tc_commit(BAR(C::B_QE + st));
+      };
+      bool ok = mbar_wait(BAR(C::B_KVF), 0, abort_flag, p.err);
+      if (ok && n_steps > 0) {
+        ok = mbar_wait(BAR(C::B_QF + 0), 0, abort_flag, p.err);
+        if (ok) issue_sdp(0, 0);
+      }
+      for (int s = 0; ok && s < n_steps; ++s) {
+        const int st = s % ST, sp = (s + ST - 1) % ST;
+        if (s > 0) {
+          // the second half of step s-1, which then releases its Q / dO stage
+          if (!(ok = mbar_wait(BAR(C::B_DS + 1), (s - 1) & 1, abort_flag, p.err))) break;
+          issue_acc(1, sp, false);
+          tc_commit(BAR(C::B_QE + sp));
+        }
+        issue_sdp(1, st);
+        if (!(ok = mbar_wait(BAR(C::B_DS + 0), s & 1, abort_flag, p.err))) break;
+        issue_acc(0, st, s == 0);
+        if (s + 1 < n_steps) {
+          const int sn = (s + 1) % ST;
+          if (!(ok = mbar_wait(BAR(C::B_QF + sn), ((s + 1) / ST) & 1, abort_flag, p.err))) break;
+          issue_sdp(0, sn);
+        }
+      }
+      if (ok && n_steps > 0) {
+        const int sl = (n_steps - 1) % ST;
+        ok = mbar_wait(BAR(C::B_DS + 1), (n_steps - 1) & 1, abort_flag, p.err);
+        if (ok) {
+          issue_acc(1, sl, false);
+          tc_commit(BAR(C::B_QE + sl));
+        }
       }
       if (ok) tc_commit(BAR(C::B_DONE));
       tc_commit(BAR(C::B_MMA));
@@ -438,8 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;   // query columns half * 64 .. + 63 of each tile
     const int r = quarter * 32 + lane;  // key row in the tile == TMEM lane
-    const int tid = (warp - 2) * 32 + lane;
+    const int tid = ((warp - 2) & 3) * 32 + lane;  // thread index within the warpgroup
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int kv = kv0 + r;
     const bool kv_ok = kv < p.Nkv;
@@ -447,84 +555,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int s = 0; s < n_steps; ++s) {
       const int h = hk * p.group + s / n_i, i0 = (i_first + s % n_i) * kT;
-      // This step's per-query log-sum-exp (base 2) and D, one value per thread, into shared memory.
-      float *buf = sld + (s & 1) * 2 * kT;
+      // This step's log-sum-exp (base 2) and D of the half's 64 queries, one value
+      // per thread of the warpgroup, into shared memory.
+      const int q_half = i0 + half * 64;  // this half's first query
+      float *buf = sld + (half * 2 + (s & 1)) * 2 * 64;
       {
-        const int qi = i0 + tid;
+        const int qi = q_half + (tid & 63);
         const int64_t ri = (static_cast<int64_t>(b) * p.Hq + h) * p.Nq + qi;
-        buf[tid] = qi < p.Nq ? p.lse[ri] * kLog2e : 0.f;
-        buf[kT + tid] = qi < p.Nq ? p.dvec[ri] : 0.f;
-        mbar_arrive(BAR(C::B_LD + (s & 1)));
+        buf[tid] = qi < p.Nq ? ((tid < 64) ? p.lse[ri] * kLog2e : p.dvec[ri]) : 0.f;
+        mbar_arrive(BAR(C::B_LD + half * 2 + (s & 1)));
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_LD + (s & 1)), (s >> 1) & 1, abort_flag, p.err));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF), s & 1, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_LD + half * 2 + (s & 1)), (s >> 1) & 1, abort_flag, p.err));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF + half), s & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      // Query columns c < hi are real queries; causal keeps query i0+c iff kv <= i0+c.
-      const int hi = min(kT, p.Nq - i0);
-      const int lo = CAUSAL ? max(0, kv - i0) : 0;
+      // Query columns c < hi are real queries; causal keeps query q_half+c iff kv <= q_half+c.
+      const int hi = min(64, p.Nq - q_half);
+      const int lo = CAUSAL ? max(0, kv - q_half) : 0;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = ch * 32;
         uint32_t sv[32], pv[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + C::S_COL + ch * 32, sv);
-        tmem_ld_32x32b_x32(tmem + lane_off + C::DP_COL + ch * 32, pv);
+        tmem_ld_32x32b_x32(tmem + lane_off + C::s_col(half) + c0, sv);
+        tmem_ld_32x32b_x32(tmem + lane_off + C::dp_col(half) + c0, pv);
         tmem_wait_ld();
         reg_fence(sv);
         reg_fence(pv);
         uint32_t pp[16], ds[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const int cc = ch * 32 + c;
+          const int cc = c0 + c;
           const bool k0 = kv_ok && cc >= lo && cc < hi, k1 = kv_ok && cc + 1 >= lo && cc + 1 < hi;
           const float p0 = k0 ? fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -buf[cc])) : 0.f;
           const float p1 = k1 ? fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -buf[cc + 1])) : 0.f;
           pp[c / 2] = pack2<BF16>(p0, p1);
-          ds[c / 2] = pack2<BF16>(p0 * (__uint_as_float(pv[c]) - buf[kT + cc]),
-                                  p1 * (__uint_as_float(pv[c + 1]) - buf[kT + cc + 1]));
+          ds[c / 2] = pack2<BF16>(p0 * (__uint_as_float(pv[c]) - buf[64 + cc]),
+                                  p1 * (__uint_as_float(pv[c + 1]) - buf[64 + cc + 1]));
         }
-        // P^T over S^T's first 64 columns, dS^T over dP^T's; only columns already read are overwritten.
-        tmem_st_32x32b_x16(tmem + lane_off + C::S_COL + ch * 16, pp);
-        tmem_st_32x32b_x16(tmem + lane_off + C::DP_COL + ch * 16, ds);
+        // P^T and dS^T over the first 32 of this half's S^T and dP^T columns;
+        // only columns already read are overwritten.
+        tmem_st_32x32b_x16(tmem + lane_off + C::s_col(half) + ch * 16, pp);
+        tmem_st_32x32b_x16(tmem + lane_off + C::dp_col(half) + ch * 16, ds);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(C::B_DS));
+      if (lane == 0) mbar_arrive(BAR(C::B_DS + half));
     }
     if (ok && n_steps > 0) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_DONE), 0, abort_flag, p.err));
     if (ok) {
       // The TMEM loads are warp-wide (.sync.aligned): every lane executes them;
-      // only rows of real keys are stored.
+      // only rows of real keys are stored.  The first warpgroup stores dV, the
+      // second dK.
       tc_fence_after();
-      const int64_t vrow = static_cast<int64_t>(b) * p.dv_sb + static_cast<int64_t>(hk) * p.dv_sh +
-                           static_cast<int64_t>(kv) * p.dv_sn;
-      const int64_t krow = static_cast<int64_t>(b) * p.dk_sb + static_cast<int64_t>(hk) * p.dk_sh +
-                           static_cast<int64_t>(kv) * p.dk_sn;
+      const bool is_dk = half == 1;
+      void *dst = is_dk ? p.dk : p.dv;
+      const int64_t row = is_dk ? static_cast<int64_t>(b) * p.dk_sb + static_cast<int64_t>(hk) * p.dk_sh +
+                                      static_cast<int64_t>(kv) * p.dk_sn
+                                : static_cast<int64_t>(b) * p.dv_sb + static_cast<int64_t>(hk) * p.dv_sh +
+                                      static_cast<int64_t>(kv) * p.dv_sn;
+      const uint32_t col = is_dk ? C::DK_COL : C::DV_COL;
+      const float mul = is_dk ? p.scale : 1.f;
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) {
         uint32_t v[32];
         if (n_steps > 0) {
-          tmem_ld_32x32b_x32(tmem + lane_off + C::DV_COL + i * 32, v);
+          tmem_ld_32x32b_x32(tmem + lane_off + col + i * 32, v);
           tmem_wait_ld();
           reg_fence(v);
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] = 0u;  // no query attends to this key
         }
-        if (kv_ok) store_row32<BF16>(p.dv, vrow + i * 32, v, 1.f);
-      }
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        uint32_t v[32];
-        if (n_steps > 0) {
-          tmem_ld_32x32b_x32(tmem + lane_off + C::DK_COL + i * 32, v);
-          tmem_wait_ld();
-          reg_fence(v);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = 0u;
-        }
-        if (kv_ok) store_row32<BF16>(p.dk, krow + i * 32, v, p.scale);
+        if (kv_ok) store_row32<BF16>(dst, row + i * 32, v, mul);
       }
     }
   }
@@ -538,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv, cudaStream_t stream) {
-  bwd_preprocess_kernel<D, BF16><<<dim3((p.Nq + 7) / 8, p.Hq, B), 256, 0, stream>>>(p);
+  constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
+  bwd_preprocess_kernel<D, BF16><<<dim3((p.Nq + kRowsPerBlock - 1) / kRowsPerBlock, p.Hq, B), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   {
