@@ -589,15 +589,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 32; ++c)
               if (i * 32 + c >= hi_c || i * 32 + c < lo_c) sr[i][c] = __float_as_uint(-INFINITY);
         }
-        float sl_eff = sl2;  // factor from the values in sr to base-2 scores
+        float sl_eff = sl2;     // factor from the values in sr to base-2 scores
+        float row_bias = 0.f;   // base-2 term every score of the row gets after the max
         if (alibi) {
           const float dq = static_cast<float>(q_row - kv0);
+          // A tile wholly left of every row's diagonal (or wholly right of it) has
+          // |i - j| = side * (i - j) with one sign: the bias splits into a column
+          // term, two columns per packed multiply-add, and a row term added later.
+          // Tiles that straddle a diagonal take |i - j| per element.
+          const int side = (kv0 + kBN - 1 <= q_tile0) ? 1 : (kv0 >= q_tile0 + kBM - 1) ? -1 : 0;
+          if (side != 0) {
+            const float cs = static_cast<float>(side) * slope2;
+            const uint64_t cs2 = pack_f2(cs, cs), sl2x2 = pack_f2(sl2, sl2);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              sr[i][c] = __float_as_uint(
-                  fmaf(__uint_as_float(sr[i][c]), sl2, -slope2 * fabsf(dq - static_cast<float>(i * 32 + c))));
+              for (int c = 0; c < 32; c += 2) {
+                const uint64_t col = pack_f2(static_cast<float>(i * 32 + c), static_cast<float>(i * 32 + c + 1));
+                const float2 v = unpack_f2(ffma_f2(pack_f2(__uint_as_float(sr[i][c]), __uint_as_float(sr[i][c + 1])),
+                                                   sl2x2, fmul_f2(col, cs2)));
+                sr[i][c] = __float_as_uint(v.x);
+                sr[i][c + 1] = __float_as_uint(v.y);
+              }
+            row_bias = -cs * dq;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                sr[i][c] = __float_as_uint(
+                    fmaf(__uint_as_float(sr[i][c]), sl2, -slope2 * fabsf(dq - static_cast<float>(i * 32 + c))));
+          }
           sl_eff = 1.f;
         }
         // Row max: four independent chains of 3-input maxima.
@@ -612,14 +634,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
         // Raise the running max only when the block max exceeds it by more than
         // the threshold; otherwise keep it (alpha = 1, no rescale of O).
-        const float mb = mx * sl_eff;
+        const float mb = mx * sl_eff + row_bias;
         const bool raise = (m == -INFINITY) || (mb > m + kRescaleThreshold);
         const float m_new = raise ? fmaxf(m, mb) : m;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = raise ? fast_exp2(m - m_use) : 1.f;
         // P = 2^(s * scale * log2 e - m), two columns per packed FMA; row sum in
         // four packed partial sums.
-        const uint64_t sl2x2 = pack_f2(sl_eff, sl_eff), negm2 = pack_f2(-m_use, -m_use);
+        const uint64_t sl2x2 = pack_f2(sl_eff, sl_eff), negm2 = pack_f2(row_bias - m_use, row_bias - m_use);
         uint64_t rs2[4] = {0, 0, 0, 0};
         uint32_t pk[2][32];
 #pragma unroll
