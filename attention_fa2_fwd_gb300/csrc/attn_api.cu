@@ -2,7 +2,8 @@
 //
 // Host-side work only: argument validation (before anything is launched),
 // TMA tensor-map encoding, split-count selection for decode, the device error
-// word, and dispatch to the kernels in prefill.cu and decode.cu.
+// word, and dispatch to the kernels (prefill_kernel.cuh through prefill.cu and
+// prefill_masked.cu, decode.cu, bwd.cu).
 #include <algorithm>
 #include <climits>
 #include <cmath>
