@@ -7,6 +7,8 @@
     python -m attention_fa2_fwd_gb300.run_case cross   [--D 64|128: the cross-attention workload, B=4 H_q=16
                                                         H_kv=4 N_q=1024 N_kv=4096, (B,N,H,D) memory, non-causal]
     prefill / decode / decode_paged also take --window-left W and --alibi 1 (sliding window, ALiBi slopes)
+    decode / decode_paged take --graph 1: the step (cache write of one token + decode) captured once in a
+    CUDA graph and replayed, against the same calls launched one by one
 
 Inputs are seeded N(0,1) bf16 tensors drawn on the device.  Each iteration is
 timed with CUDA events on the launching stream (L2 flushed by a 256 MiB write
@@ -39,6 +41,7 @@ def main():
     ap.add_argument("--ragged", type=int, default=0, help="decode_paged: lengths uniform in [L/2, L]")
     ap.add_argument("--window-left", type=int, default=-1, help="sliding window: keys i - W .. i (-1: none)")
     ap.add_argument("--alibi", type=int, default=0, help="ALiBi slopes 2^(-8 (h + 1) / H_q)")
+    ap.add_argument("--graph", type=int, default=0, help="decode: time a one-token serving step, eager vs CUDA graph")
     a = ap.parse_args()
     dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
     dev = torch.device("cuda", 0)
@@ -131,6 +134,47 @@ def main():
         def call():
             A.decode(qd, kc, vc, a.L, out=od, lse_out=lsed, workspace=ws, window_left=wl, alibi_slopes=slopes)
         unit, scale = "GB/s", 1e9
+    if a.graph and a.kind in ("decode", "decode_paged"):
+        # one serving step: write one new token per request, then decode
+        kn = randn(B, a.Hkv, 1, a.D)
+        vn = randn(B, a.Hkv, 1, a.D)
+        if a.kind == "decode":
+            pos = a.L - 1
+
+            def serve():
+                A.write_kv_cache(kc, vc, kn, vn, pos)
+                call()
+        else:
+            positions = (lens - 1).clamp(min=0)
+
+            def serve():
+                A.write_kv_cache_paged(kp, vp, kn, vn, table, positions)
+                call()
+        serve()
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                serve()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        reps = 50
+        for label, fn in (("eager", serve), ("graph", graph.replay)):
+            meds = []
+            for _ in range(a.iters):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                meds.append(e0.elapsed_time(e1) / reps)
+            print(f"{a.kind} step ({label}, {reps} back to back): median_ms={statistics.median(meds):.4f}")
+        A.check_device_error()
+        return
     times = []
     for _ in range(a.iters):
         flush.zero_()
