@@ -34,7 +34,8 @@ ATTN_F16 = 0
 ATTN_BF16 = 1
 
 # Every function that include/attn.h declares.
-EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_ex", "attn_fwd_prefill_varlen", "attn_fwd_prefill_varlen_ex",
+EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_ex", "attn_fwd_prefill_host", "attn_fwd_prefill_host_workspace_size",
+           "attn_fwd_prefill_varlen", "attn_fwd_prefill_varlen_ex",
            "attn_fwd_decode_ex", "attn_fwd_decode_paged_ex", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
            "attn_fwd_decode_noalloc", "kv_cache_write", "attn_fwd_decode_paged", "kv_cache_write_paged",
            "attn_bwd_workspace_size", "attn_bwd",
@@ -94,6 +95,11 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_decode_paged_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                                    vp, i32, ctypes.c_int64, vp, i32, i64p, i64p, i64p, i64p, f32, vp,
                                                    ctypes.c_size_t, optp, vp]
+            L.attn_fwd_prefill_host_workspace_size.restype = ctypes.c_size_t
+            L.attn_fwd_prefill_host_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+            L.attn_fwd_prefill_host.restype = i32
+            L.attn_fwd_prefill_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32,
+                                                optp, vp, ctypes.c_size_t, vp]
             L.attn_decode_workspace_size.restype = ctypes.c_size_t
             L.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
             L.attn_decode_splits.restype = i32
@@ -177,6 +183,16 @@ def attn_fwd_decode_paged_ex(q, k_pages, v_pages, o, lse, dtype, B, H_q, H_kv, D
                                           page_size, block_table, max_pages, bt_stride, cache_lens, max_cache_len,
                                           _strides(q_str), _strides(kp_str), _strides(vp_str), _strides(o_str),
                                           float(scale), workspace, workspace_bytes, _opts(opts), stream)
+
+
+def attn_fwd_prefill_host_workspace_size(dtype, B, H_q, H_kv, N_q, N_kv, D) -> int:
+    return lib().attn_fwd_prefill_host_workspace_size(dtype, B, H_q, H_kv, N_q, N_kv, D)
+
+
+def attn_fwd_prefill_host(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, causal, scale, opts, workspace,
+                          workspace_bytes, stream) -> int:
+    return lib().attn_fwd_prefill_host(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, int(causal), float(scale),
+                                       _opts(opts), workspace, workspace_bytes, stream)
 
 
 def make_options(window_left: int = -1, window_right: int = -1, alibi_slopes=None):
@@ -320,6 +336,36 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_ls
                              q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
                              make_options(window[0], window[1], alibi_slopes), _stream_handle(stream))
     _check(st, "attn_fwd_prefill")
+    return o, lse
+
+
+def prefill_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse_out=None,
+                 workspace=None, stream=None, window=(-1, -1), alibi_slopes=None):
+    """Prefill on host tensors (contiguous, ideally pinned) with copies pipelined against the compute.
+
+    q (B,H_q,N_q,D), k, v (B,H_kv,N_kv,D) CPU tensors; returns host (O, LSE).  The results are complete
+    once ``stream`` (default: the current CUDA stream) has finished; this helper synchronises it.
+    """
+    import torch
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = out if out is not None else torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    lse = lse_out if lse_out is not None else torch.empty((B, Hq, Nq), dtype=torch.float32, pin_memory=True)
+    code = _dtype_code(q)
+    need = attn_fwd_prefill_host_workspace_size(code, B, Hq, Hkv, Nq, Nkv, D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = attn_fwd_prefill_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), code, B, Hq,
+                               Hkv, Nq, Nkv, D, causal, scale, make_options(window[0], window[1], alibi_slopes),
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               _stream_handle(stream))
+    _check(st, "attn_fwd_prefill_host")
+    (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return o, lse
 
 

@@ -746,6 +746,169 @@ int attn_version(void) { return 100; }
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// attn_fwd_prefill_host: prefill from and to host buffers, copies pipelined
+// against the compute in chunks of (batch element, block of kv heads).
+namespace attn {
+namespace {
+
+struct CopyStreams {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+};
+std::mutex g_copy_mutex;
+CopyStreams g_copy[kMaxDevices];
+
+// Two non-blocking streams per device, created on first use and kept for the
+// life of the process: host-to-device copies and device-to-host copies.
+attn_status_t copy_streams(cudaStream_t *in, cudaStream_t *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_copy_mutex);
+  CopyStreams &c = g_copy[dev];
+  if (!c.ready) {
+    if (cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking) != cudaSuccess) return ATTN_ERR_CUDA;
+    c.ready = true;
+  }
+  *in = c.in;
+  *out = c.out;
+  return ATTN_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Device staging: Q, O (B,H_q,N_q,D), K, V (B,H_kv,N_kv,D), LSE (B,H_q,N_q).
+struct HostLayout {
+  size_t q_bytes, kv_bytes, lse_bytes;
+  size_t off_q, off_k, off_v, off_o, off_lse, total;
+};
+HostLayout host_layout(int B, int H_q, int H_kv, int N_q, int N_kv, int D) {
+  HostLayout L{};
+  L.q_bytes = static_cast<size_t>(B) * H_q * N_q * D * 2;
+  L.kv_bytes = static_cast<size_t>(B) * H_kv * N_kv * D * 2;
+  L.lse_bytes = static_cast<size_t>(B) * H_q * N_q * 4;
+  L.off_q = 0;
+  L.off_k = L.off_q + round256(L.q_bytes);
+  L.off_v = L.off_k + round256(L.kv_bytes);
+  L.off_o = L.off_v + round256(L.kv_bytes);
+  L.off_lse = L.off_o + round256(L.q_bytes);
+  L.total = L.off_lse + round256(L.lse_bytes);
+  return L;
+}
+
+bool host_sizes_ok(int B, int H_q, int H_kv, int N_q, int N_kv, int D) {
+  return B >= 1 && H_q >= 1 && H_kv >= 1 && N_q >= 1 && N_kv >= 1 && D >= 1 && H_q % H_kv == 0 && B <= 65535 &&
+         H_q <= 65535;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+size_t attn_fwd_prefill_host_workspace_size(attn_dtype_t dtype, int B, int H_q, int H_kv, int N_q, int N_kv, int D) {
+  if (!valid_dtype(dtype) || (D != 64 && D != 128) || !host_sizes_ok(B, H_q, H_kv, N_q, N_kv, D)) return 0;
+  return host_layout(B, H_q, H_kv, N_q, N_kv, D).total;
+}
+
+attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                                    attn_dtype_t dtype, int B, int H_q, int H_kv, int N_q, int N_kv, int D,
+                                    int causal, float scale, const attn_options_t *opts, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !o || !host_sizes_ok(B, H_q, H_kv, N_q, N_kv, D) || (causal != 0 && causal != 1))
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  int wl, wr;
+  const float *slopes;
+  attn_status_t st;
+  if ((st = read_options(opts, &wl, &wr, &slopes)) != ATTN_OK) return st;
+  const HostLayout L = host_layout(B, H_q, H_kv, N_q, N_kv, D);
+  if (workspace == nullptr || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return ATTN_ERR_ALIGNMENT;
+  const DeviceState *dev = nullptr;
+  if ((st = device_state(&dev)) != ATTN_OK) return st;
+  cudaStream_t s_in, s_out;
+  if ((st = copy_streams(&s_in, &s_out)) != ATTN_OK) return st;
+  const cudaStream_t s_comp = static_cast<cudaStream_t>(stream);
+
+  // Chunk = (batch element, block of kv heads) with at least ~2 units per SM,
+  // so that each chunk's launch still fills the GPU.
+  const int group = H_q / H_kv;
+  const int64_t pairs = (N_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
+  const int64_t want = 2 * static_cast<int64_t>(dev->sm_count);
+  const int64_t per_kvh = static_cast<int64_t>(group) * pairs;
+  const int kvh = static_cast<int>(std::min<int64_t>(H_kv, std::max<int64_t>(1, (want + per_kvh - 1) / per_kvh)));
+
+  char *ws = static_cast<char *>(workspace);
+  char *dq = ws + L.off_q, *dk = ws + L.off_k, *dv = ws + L.off_v, *dout = ws + L.off_o;
+  float *dl = reinterpret_cast<float *>(ws + L.off_lse);
+  const size_t qrow = static_cast<size_t>(N_q) * D * 2, kvrow = static_cast<size_t>(N_kv) * D * 2;  // one head
+
+  cudaEvent_t ev_start;
+  if (cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) != cudaSuccess) return ATTN_ERR_CUDA;
+  // Copies into the staging buffers wait for earlier work on the caller's stream.
+  bool fine = cudaEventRecord(ev_start, s_comp) == cudaSuccess && cudaStreamWaitEvent(s_in, ev_start, 0) == cudaSuccess;
+  cudaEventDestroy(ev_start);
+  for (int b = 0; fine && b < B; ++b) {
+    for (int h0 = 0; fine && h0 < H_kv; h0 += kvh) {
+      const int nh = std::min(kvh, H_kv - h0), qh0 = h0 * group, nqh = nh * group;
+      const size_t qo = (static_cast<size_t>(b) * H_q + qh0) * qrow, qn = nqh * qrow;
+      const size_t ko = (static_cast<size_t>(b) * H_kv + h0) * kvrow, kn = nh * kvrow;
+      const size_t lo = (static_cast<size_t>(b) * H_q + qh0) * N_q * 4, ln = static_cast<size_t>(nqh) * N_q * 4;
+      cudaEvent_t ev_in, ev_done;
+      if (cudaEventCreateWithFlags(&ev_in, cudaEventDisableTiming) != cudaSuccess) {
+        fine = false;
+        break;
+      }
+      if (cudaEventCreateWithFlags(&ev_done, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventDestroy(ev_in);
+        fine = false;
+        break;
+      }
+      fine = cudaMemcpyAsync(dq + qo, static_cast<const char *>(q) + qo, qn, cudaMemcpyHostToDevice, s_in) ==
+                 cudaSuccess &&
+             cudaMemcpyAsync(dk + ko, static_cast<const char *>(k) + ko, kn, cudaMemcpyHostToDevice, s_in) ==
+                 cudaSuccess &&
+             cudaMemcpyAsync(dv + ko, static_cast<const char *>(v) + ko, kn, cudaMemcpyHostToDevice, s_in) ==
+                 cudaSuccess &&
+             cudaEventRecord(ev_in, s_in) == cudaSuccess && cudaStreamWaitEvent(s_comp, ev_in, 0) == cudaSuccess;
+      if (fine) {
+        // The chunk is a contiguous (1, nqh, N_q, D) / (1, nh, N_kv, D) problem.
+        const int64_t sq[4] = {static_cast<int64_t>(nqh) * N_q * D, static_cast<int64_t>(N_q) * D, D, 1};
+        const int64_t sk[4] = {static_cast<int64_t>(nh) * N_kv * D, static_cast<int64_t>(N_kv) * D, D, 1};
+        attn_options_t oc{wl, wr, slopes ? slopes + qh0 : nullptr};
+        const attn_status_t cs = attn_fwd_prefill_ex(dq + qo, dk + ko, dv + ko, dout + qo,
+                                                     lse ? reinterpret_cast<float *>(reinterpret_cast<char *>(dl) + lo)
+                                                         : nullptr,
+                                                     dtype, 1, nqh, nh, N_q, N_kv, D, sq, sk, sk, sq, causal, scale,
+                                                     &oc, stream);
+        if (cs != ATTN_OK) {
+          cudaEventDestroy(ev_in);
+          cudaEventDestroy(ev_done);
+          return cs;
+        }
+        fine = cudaEventRecord(ev_done, s_comp) == cudaSuccess && cudaStreamWaitEvent(s_out, ev_done, 0) == cudaSuccess &&
+               cudaMemcpyAsync(static_cast<char *>(o) + qo, dout + qo, qn, cudaMemcpyDeviceToHost, s_out) ==
+                   cudaSuccess &&
+               (!lse || cudaMemcpyAsync(reinterpret_cast<char *>(lse) + lo, reinterpret_cast<char *>(dl) + lo, ln,
+                                        cudaMemcpyDeviceToHost, s_out) == cudaSuccess);
+      }
+      cudaEventDestroy(ev_in);
+      cudaEventDestroy(ev_done);
+    }
+  }
+  // The caller's stream waits for the last device-to-host copy.
+  cudaEvent_t ev_end;
+  if (cudaEventCreateWithFlags(&ev_end, cudaEventDisableTiming) != cudaSuccess) return ATTN_ERR_CUDA;
+  const bool joined = cudaEventRecord(ev_end, s_out) == cudaSuccess && cudaStreamWaitEvent(s_comp, ev_end, 0) == cudaSuccess;
+  cudaEventDestroy(ev_end);
+  return (fine && joined) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
 // attn_fwd_decode_noalloc: decode whose split scratch lives in a fixed array
 // compiled into the library instead of a caller-provided buffer.
 namespace attn {

@@ -240,28 +240,31 @@ def run_ours(args, rank, world, local_rank):
     value = aggregate_throughput(flops, world, args.steps, sum_pre) / 1e12
     decode_gbs = aggregate_throughput(kvb, world, args.steps, sum_dec) / 1e9
 
-    # End to end through the public API with host buffers (pinned), copies inside the timed region.
+    # End to end through the public API with host buffers (pinned), copies inside the timed region:
+    # attn_fwd_prefill_host pipelines the host-to-device copies, the compute and the copies back.
     if True:
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        code = A.ATTN_BF16
+        ws_bytes = A.attn_fwd_prefill_host_workspace_size(code, P["B"], P["Hq"], P["Hkv"], P["N"], P["N"], P["D"])
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        scale = 1.0 / math.sqrt(P["D"])
+
+        def host_call():
+            st = A.attn_fwd_prefill_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(), hl.data_ptr(),
+                                         code, P["B"], P["Hq"], P["Hkv"], P["N"], P["N"], P["D"], 1, scale, None,
+                                         ws.data_ptr(), ws_bytes, stream.cuda_stream)
+            if st != A.ATTN_OK:
+                raise RuntimeError(f"attn_fwd_prefill_host failed: {A.attn_status_string(st)}")
         n_e2e = max(3, min(args.steps, 10))
         for _ in range(2):
-            A.prefill(dq.copy_(hq, non_blocking=True), dk.copy_(hk, non_blocking=True),
-                      dv.copy_(hv, non_blocking=True), causal=True, out=o, lse_out=lse)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+            host_call()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(n_e2e):
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            A.prefill(dq, dk, dv, causal=True, out=o, lse_out=lse)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
+            host_call()
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = reduce_max([e0.elapsed_time(e1) / n_e2e], world, dev)[0]
@@ -269,7 +272,8 @@ def run_ours(args, rank, world, local_rank):
         d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
         e2e = {"value": round(aggregate_throughput(flops, world, 1, e2e_ms) / 1e12, 2), "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_call": round(e2e_ms, 4), "path": "pinned host Q,K,V -> attn_fwd_prefill -> host O,LSE"}
+               "ms_per_call": round(e2e_ms, 4),
+               "path": "pinned host Q,K,V -> attn_fwd_prefill_host (copies pipelined with the compute) -> host O,LSE"}
 
     if rank != 0:
         return None

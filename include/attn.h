@@ -280,6 +280,45 @@ attn_status_t kv_cache_write(void *k_cache, void *v_cache, const void *k_new, co
                              const int64_t vn_str[4], void *stream);
 
 /*
+ * attn_fwd_prefill_host -- attn_fwd_prefill_ex on host-resident tensors, with
+ * the host-to-device copies, the compute and the device-to-host copies
+ * pipelined.  (The pages time kernels on device-resident inputs; this entry
+ * point is a convenience of this library for callers whose tensors live in
+ * host memory, e.g. Grace-resident activations.)
+ *
+ * The problem is cut into chunks of (batch element, block of kv heads with all
+ * their q heads); chunk i's inputs are copied on a library-owned stream while
+ * chunk i-1 is computed on `stream` and chunk i-2's outputs are copied back on
+ * a second library-owned stream (two non-blocking streams per device, created
+ * on first use and kept until the process exits).  Each chunk is computed by
+ * the same kernel as attn_fwd_prefill_ex on its contiguous slice, so results
+ * equal those of attn_fwd_prefill_ex on the whole problem.
+ *
+ *   q, o  host (B, H_q, N_q, D) contiguous; k, v host (B, H_kv, N_kv, D)
+ *         contiguous; lse host (B, H_q, N_q) fp32 or NULL.  Page-locked
+ *         (pinned) host memory is what makes the copies asynchronous.
+ *   workspace  device memory of at least attn_fwd_prefill_host_workspace_size()
+ *         bytes, 256-byte aligned: staging copies of Q, K, V, O and LSE.
+ *   causal, scale, opts  as for attn_fwd_prefill_ex (ALiBi slopes: a device
+ *         array of H_q values).
+ *
+ * Ordering: the copies into the workspace start after the work enqueued on
+ * `stream` before the call; `stream` waits for the last copy back, so o and
+ * lse are complete once `stream` is.  The caller keeps the host buffers and
+ * the workspace alive and unmodified until then.
+ *
+ * Errors: as attn_fwd_prefill_ex; ATTN_ERR_WORKSPACE for a missing or short
+ * workspace, ATTN_ERR_ALIGNMENT for a workspace not 256-byte aligned,
+ * ATTN_ERR_CUDA if a copy or stream operation fails (copies already enqueued
+ * may still run: synchronise `stream` before reusing the buffers).
+ */
+size_t attn_fwd_prefill_host_workspace_size(attn_dtype_t dtype, int B, int H_q, int H_kv, int N_q, int N_kv, int D);
+attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                                    attn_dtype_t dtype, int B, int H_q, int H_kv, int N_q, int N_kv, int D,
+                                    int causal, float scale, const attn_options_t *opts, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/*
  * attn_fwd_decode_noalloc -- attn_fwd_decode for callers that may not allocate
  * device memory.  (The pages have no counterpart of this entry point; it is a
  * convenience of this library.)

@@ -293,3 +293,37 @@ def test_make_options():
     import torch
     with pytest.raises(TypeError):
         A.make_options(alibi_slopes=torch.zeros(4))  # a CPU tensor is not a device pointer
+
+
+def prefill_host(**kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=None, dtype=A.ATTN_BF16, B=2, H_q=8, H_kv=2, N_q=64, N_kv=64, D=128, causal=1,
+             scale=0.088, opts=None, workspace=P, workspace_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return A.attn_fwd_prefill_host(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(o=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(H_kv=3), A.ATTN_ERR_INVALID_ARG),
+    (dict(N_kv=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), A.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), A.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), A.ATTN_ERR_UNSUPPORTED),
+    (dict(workspace=None), A.ATTN_ERR_WORKSPACE),
+    (dict(workspace_bytes=1024), A.ATTN_ERR_WORKSPACE),
+    (dict(workspace=P + 16), A.ATTN_ERR_ALIGNMENT),
+    (dict(opts=A.AttnOptions(-3, -1, None)), A.ATTN_ERR_INVALID_ARG),
+])
+def test_prefill_host_argument_errors(lib, kw, code):
+    assert prefill_host(**kw) == code
+
+
+def test_prefill_host_workspace_size():
+    n = A.attn_fwd_prefill_host_workspace_size(A.ATTN_BF16, 2, 8, 2, 64, 64, 128)
+    q = 2 * 8 * 64 * 128 * 2
+    kv = 2 * 2 * 64 * 128 * 2
+    lse = 2 * 8 * 64 * 4
+    assert n == 2 * q + 2 * kv + lse  # every region a multiple of 256 bytes here
+    assert A.attn_fwd_prefill_host_workspace_size(A.ATTN_BF16, 2, 8, 3, 64, 64, 128) == 0
+    assert A.attn_fwd_prefill_host_workspace_size(A.ATTN_BF16, 2, 8, 2, 64, 64, 80) == 0
