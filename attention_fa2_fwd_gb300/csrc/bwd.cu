@@ -35,6 +35,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "attn_internal.h"
 #include "ptx.cuh"
 
@@ -304,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lse2 = row_ok ? p.lse[ri] * kLog2e : 0.f;
     const float dv = row_ok ? p.dvec[ri] : 0.f;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = pack_f2(sl2, sl2), nl2 = pack_f2(-lse2, -lse2), nd2 = pack_f2(-dv, -dv);
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_SF + half), j & 1, abort_flag, p.err));
@@ -311,26 +314,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int kv0 = j * kT + half * 64;  // this half's first key
       const int lim = row_ok ? ((CAUSAL ? min(p.Nkv, q_row + 1) : p.Nkv) - kv0) : 0;  // columns c < lim count
+      // dS = 2^(s scale log2 e - lse2) (dP - D), two columns per packed FMA / add / multiply;
+      // the per-column mask only where some row of the warp needs it.
+      auto tile = [&](auto masked) {
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = ch * 32;
-        uint32_t sv[32], pv[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + C::s_col(half) + c0, sv);
-        tmem_ld_32x32b_x32(tmem + lane_off + C::dp_col(half) + c0, pv);
-        tmem_wait_ld();
-        reg_fence(sv);
-        reg_fence(pv);
-        uint32_t ds[16];
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = ch * 32;
+          uint32_t sv[32], pv[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + C::s_col(half) + c0, sv);
+          tmem_ld_32x32b_x32(tmem + lane_off + C::dp_col(half) + c0, pv);
+          tmem_wait_ld();
+          reg_fence(sv);
+          reg_fence(pv);
+          uint32_t ds[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int cc = c0 + c;
-          const float p0 = (cc < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -lse2)) : 0.f;
-          const float p1 = (cc + 1 < lim) ? fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -lse2)) : 0.f;
-          ds[c / 2] = pack2<BF16>(p0 * (__uint_as_float(pv[c]) - dv), p1 * (__uint_as_float(pv[c + 1]) - dv));
+          for (int c = 0; c < 32; c += 2) {
+            const float2 e = unpack_f2(ffma_f2(pack_f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nl2));
+            float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+            if constexpr (decltype(masked)::value) {
+              if (c0 + c >= lim) p0 = 0.f;
+              if (c0 + c + 1 >= lim) p1 = 0.f;
+            }
+            const float2 d = unpack_f2(
+                fmul_f2(pack_f2(p0, p1), fadd_f2(pack_f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), nd2)));
+            ds[c / 2] = pack2<BF16>(d.x, d.y);
+          }
+          // dS over the first 32 of this half's S columns; chunk ch only overwrites columns already read.
+          tmem_st_32x32b_x16(tmem + lane_off + C::s_col(half) + ch * 16, ds);
         }
-        // dS over the first 32 of this half's S columns; chunk ch only overwrites columns already read.
-        tmem_st_32x32b_x16(tmem + lane_off + C::s_col(half) + ch * 16, ds);
-      }
+      };
+      if (__all_sync(0xffffffffu, lim >= 64))
+        tile(std::false_type{});
+      else
+        tile(std::true_type{});
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -552,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kv = kv0 + r;
     const bool kv_ok = kv < p.Nkv;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = pack_f2(sl2, sl2);
     bool ok = true;
     for (int s = 0; s < n_steps; ++s) {
       const int h = hk * p.group + s / n_i, i0 = (i_first + s % n_i) * kT;
@@ -562,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int qi = q_half + (tid & 63);
         const int64_t ri = (static_cast<int64_t>(b) * p.Hq + h) * p.Nq + qi;
-        buf[tid] = qi < p.Nq ? ((tid < 64) ? p.lse[ri] * kLog2e : p.dvec[ri]) : 0.f;
+        buf[tid] = qi < p.Nq ? ((tid < 64) ? -p.lse[ri] * kLog2e : -p.dvec[ri]) : 0.f;  // negated
         mbar_arrive(BAR(C::B_LD + half * 2 + (s & 1)));
       }
       ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_LD + half * 2 + (s & 1)), (s >> 1) & 1, abort_flag, p.err));
@@ -572,31 +589,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Query columns c < hi are real queries; causal keeps query q_half+c iff kv <= q_half+c.
       const int hi = min(64, p.Nq - q_half);
       const int lo = CAUSAL ? max(0, kv - q_half) : 0;
+      // P^T = 2^(s scale log2 e - lse2), dS^T = P^T (dP^T - D), two columns per packed
+      // FMA / add / multiply with the per-query values read in pairs; the mask only
+      // where some key row of the warp needs it.
+      auto tile = [&](auto masked) {
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = ch * 32;
-        uint32_t sv[32], pv[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + C::s_col(half) + c0, sv);
-        tmem_ld_32x32b_x32(tmem + lane_off + C::dp_col(half) + c0, pv);
-        tmem_wait_ld();
-        reg_fence(sv);
-        reg_fence(pv);
-        uint32_t pp[16], ds[16];
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = ch * 32;
+          uint32_t sv[32], pv[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + C::s_col(half) + c0, sv);
+          tmem_ld_32x32b_x32(tmem + lane_off + C::dp_col(half) + c0, pv);
+          tmem_wait_ld();
+          reg_fence(sv);
+          reg_fence(pv);
+          uint32_t pp[16], ds[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int cc = c0 + c;
-          const bool k0 = kv_ok && cc >= lo && cc < hi, k1 = kv_ok && cc + 1 >= lo && cc + 1 < hi;
-          const float p0 = k0 ? fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -buf[cc])) : 0.f;
-          const float p1 = k1 ? fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -buf[cc + 1])) : 0.f;
-          pp[c / 2] = pack2<BF16>(p0, p1);
-          ds[c / 2] = pack2<BF16>(p0 * (__uint_as_float(pv[c]) - buf[64 + cc]),
-                                  p1 * (__uint_as_float(pv[c + 1]) - buf[64 + cc + 1]));
+          for (int c = 0; c < 32; c += 2) {
+            const int cc = c0 + c;
+            const uint64_t nl = *reinterpret_cast<const uint64_t *>(buf + cc);       // -lse2 of the two queries
+            const uint64_t nd = *reinterpret_cast<const uint64_t *>(buf + 64 + cc);  // -D of the two queries
+            const float2 e = unpack_f2(ffma_f2(pack_f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, nl));
+            float p0 = fast_exp2(e.x), p1 = fast_exp2(e.y);
+            if constexpr (decltype(masked)::value) {
+              if (!(kv_ok && cc >= lo && cc < hi)) p0 = 0.f;
+              if (!(kv_ok && cc + 1 >= lo && cc + 1 < hi)) p1 = 0.f;
+            }
+            pp[c / 2] = pack2<BF16>(p0, p1);
+            const float2 d = unpack_f2(
+                fmul_f2(pack_f2(p0, p1), fadd_f2(pack_f2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])), nd)));
+            ds[c / 2] = pack2<BF16>(d.x, d.y);
+          }
+          // P^T and dS^T over the first 32 of this half's S^T and dP^T columns;
+          // only columns already read are overwritten.
+          tmem_st_32x32b_x16(tmem + lane_off + C::s_col(half) + ch * 16, pp);
+          tmem_st_32x32b_x16(tmem + lane_off + C::dp_col(half) + ch * 16, ds);
         }
-        // P^T and dS^T over the first 32 of this half's S^T and dP^T columns;
-        // only columns already read are overwritten.
-        tmem_st_32x32b_x16(tmem + lane_off + C::s_col(half) + ch * 16, pp);
-        tmem_st_32x32b_x16(tmem + lane_off + C::dp_col(half) + ch * 16, ds);
-      }
+      };
+      if (__all_sync(0xffffffffu, kv_ok && lo <= 0 && hi >= 64))
+        tile(std::false_type{});
+      else
+        tile(std::true_type{});
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
