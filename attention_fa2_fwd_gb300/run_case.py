@@ -4,6 +4,8 @@
     python -m attention_fa2_fwd_gb300.run_case decode  [--B 64 --Hq 32 --Hkv 8 --L 8192 --D 128]
     python -m attention_fa2_fwd_gb300.run_case decode_paged [--page-size 16 --ragged 1 ...]
     python -m attention_fa2_fwd_gb300.run_case bwd     [prefill sizes; FLOPs counted as 2.5 x the forward]
+    python -m attention_fa2_fwd_gb300.run_case varlen  [--B 16 --N 8192: B packed sequences, lengths uniform in
+                                                        [N/8, N] (seeded), H_q=32 H_kv=8, causal by default]
     python -m attention_fa2_fwd_gb300.run_case cross   [--D 64|128: the cross-attention workload, B=4 H_q=16
                                                         H_kv=4 N_q=1024 N_kv=4096, (B,N,H,D) memory, non-causal]
     prefill / decode / decode_paged also take --window-left W and --alibi 1 (sliding window, ALiBi slopes)
@@ -27,7 +29,7 @@ import attention_fa2_fwd_gb300 as A
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kind", choices=("prefill", "decode", "decode_paged", "bwd", "cross"))
+    ap.add_argument("kind", choices=("prefill", "decode", "decode_paged", "bwd", "cross", "varlen"))
     ap.add_argument("--B", type=int)
     ap.add_argument("--Hq", type=int, default=32)
     ap.add_argument("--Hkv", type=int, default=8)
@@ -69,6 +71,22 @@ def main():
 
         def call():
             A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse, window=(wl, -1), alibi_slopes=slopes)
+        unit, scale = "TFLOPS", 1e12
+    elif a.kind == "varlen":
+        B = a.B or 16
+        lens = torch.randint(a.N // 8, a.N + 1, (B,), generator=torch.Generator().manual_seed(11)).tolist()
+        tq = sum(lens)
+        q, k, v = randn(tq, a.Hq, a.D), randn(tq, a.Hkv, a.D), randn(tq, a.Hkv, a.D)
+        cu = torch.tensor([0] + list(torch.tensor(lens).cumsum(0)), dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((a.Hq, tq), dtype=torch.float32, device=dev)
+        pairs = sum(n * (n + 1) // 2 if a.causal else n * n for n in lens)
+        work = 4.0 * a.Hq * a.D * pairs
+        print(f"varlen: {B} sequences, {tq} tokens, lengths {min(lens)}..{max(lens)}")
+
+        def call():
+            A.prefill_varlen(q, k, v, cu, cu, max(lens), max(lens), causal=bool(a.causal), out=o, lse_out=lse,
+                             window=(a.window_left, -1), alibi_slopes=slopes)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "cross":
         import attention_fa2_fwd_gb300.inputs as I
