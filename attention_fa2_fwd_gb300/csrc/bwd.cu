@@ -238,26 +238,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16(BF16, kT, 64, false, false);  // N = 64 keys (one half)
       constexpr uint32_t idesc_dq = idesc_f16(BF16, kT, D, false, true);
+      // Shared-memory descriptors are formed once; each MMA adds the operand's
+      // offset (in 16-byte units) to the start-address field, which never
+      // carries (every operand lies below 256 KB).  The MMA thread's issue rate
+      // bounds the step, so no descriptor is rebuilt per MMA.
+      const uint64_t dq_k = smem_desc_sw128(sQ, 16, 1024), ddo_k = smem_desc_sw128(sDO, 16, 1024);
+      const uint64_t dkv_k = smem_desc_sw128(sK(0), 16, 1024), dkv_mn = smem_desc_sw128(sK(0), C::CHUNK, 1024);
       // S_h = Q K_h^T and dP_h = dO V_h^T for keys 64 h .. 64 h + 63 of the tile in stage st.
       auto issue_sdp = [&](int hf, int st) {
         tc_fence_after();
+        const uint64_t kd = dkv_k + ((2 * st * C::TILE + hf * C::HALF_ROWS) >> 4), vd = kd + (C::TILE >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss(tmem + C::s_col(hf), smem_desc_sw128(sQ + ko, 16, 1024),
-                 smem_desc_sw128(sK(st) + hf * C::HALF_ROWS + ko, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-          mma_ss(tmem + C::dp_col(hf), smem_desc_sw128(sDO + ko, 16, 1024),
-                 smem_desc_sw128(sV(st) + hf * C::HALF_ROWS + ko, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t ko = ((kk / 4) * C::CHUNK + (kk % 4) * 32) >> 4;
+          mma_ss(tmem + C::s_col(hf), dq_k + ko, kd + ko, idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::dp_col(hf), ddo_k + ko, vd + ko, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(BAR(C::B_SF + hf));
       };
       // dQ += dS_h K_h: dS_h (16-bit) over the first 32 columns of S_h; K as MN-major B.
       auto issue_dq = [&](int hf, int st, bool first) {
         tc_fence_after();
+        const uint64_t kd = dkv_mn + ((2 * st * C::TILE + hf * 4 * 16 * 128) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + C::DQ_COL, tmem + C::s_col(hf) + kk * 8,
-                 smem_desc_sw128(sK(st) + (hf * 4 + kk) * 16 * 128, C::CHUNK, 1024), idesc_dq,
+          mma_ts(tmem + C::DQ_COL, tmem + C::s_col(hf) + kk * 8, kd + ((kk * 16 * 128) >> 4), idesc_dq,
                  (!first || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(BAR(C::B_QF), 0, abort_flag, p.err);
@@ -499,15 +504,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_acc = idesc_f16(BF16, kT, D, false, true);
       // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for queries 64 h .. 64 h + 63 of the tile in stage st:
       // keys on the TMEM lanes, queries on the columns.
+      // Descriptors formed once, per-MMA offsets added to the start-address field
+      // (as in the dQ kernel).
+      const uint64_t dk_k = smem_desc_sw128(sK, 16, 1024), dv_k = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dqd_k = smem_desc_sw128(sQ(0), 16, 1024), dqd_mn = smem_desc_sw128(sQ(0), C::CHUNK, 1024);
       auto issue_sdp = [&](int hf, int st) {
         tc_fence_after();
+        const uint64_t qd = dqd_k + ((2 * st * C::TILE + hf * C::HALF_ROWS) >> 4), dod = qd + (C::TILE >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk / 4) * C::CHUNK + (kk % 4) * 32;
-          mma_ss(tmem + C::s_col(hf), smem_desc_sw128(sK + ko, 16, 1024),
-                 smem_desc_sw128(sQ(st) + hf * C::HALF_ROWS + ko, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-          mma_ss(tmem + C::dp_col(hf), smem_desc_sw128(sV + ko, 16, 1024),
-                 smem_desc_sw128(sDO(st) + hf * C::HALF_ROWS + ko, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t ko = ((kk / 4) * C::CHUNK + (kk % 4) * 32) >> 4;
+          mma_ss(tmem + C::s_col(hf), dk_k + ko, qd + ko, idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::dp_col(hf), dv_k + ko, dod + ko, idesc_s, kk > 0 ? 1u : 0u);
         }
         tc_commit(BAR(C::B_SF + hf));
       };
@@ -515,13 +523,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // columns of S^T_h / dP^T_h, dO / Q as MN-major B (queries 64 h .. of the tile).
       auto issue_acc = [&](int hf, int st, bool first) {
         tc_fence_after();
+        const uint64_t qd = dqd_mn + ((2 * st * C::TILE + hf * 4 * 16 * 128) >> 4), dod = qd + (C::TILE >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t bo = (hf * 4 + kk) * 16 * 128;
-          mma_ts(tmem + C::DV_COL, tmem + C::s_col(hf) + kk * 8, smem_desc_sw128(sDO(st) + bo, C::CHUNK, 1024),
-                 idesc_acc, (!first || kk > 0) ? 1u : 0u);
-          mma_ts(tmem + C::DK_COL, tmem + C::dp_col(hf) + kk * 8, smem_desc_sw128(sQ(st) + bo, C::CHUNK, 1024),
-                 idesc_acc, (!first || kk > 0) ? 1u : 0u);
+          const uint32_t bo = (kk * 16 * 128) >> 4;
+          mma_ts(tmem + C::DV_COL, tmem + C::s_col(hf) + kk * 8, dod + bo, idesc_acc, (!first || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DK_COL, tmem + C::dp_col(hf) + kk * 8, qd + bo, idesc_acc, (!first || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(BAR(C::B_KVF), 0, abort_flag, p.err);
