@@ -196,7 +196,9 @@ attn_status_t read_options(const attn_options_t *opts, int *wl, int *wr, const f
 // one CTA per SM at most.
 attn_status_t prefill_schedule(PrefillParams *p, int B, int H_q, int sm_count) {
   const int64_t units = static_cast<int64_t>(H_q) * B * p->n_qtiles;
-  if (units > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
+  // The kernel walks units in rounds of up to sm_count; every index it forms
+  // (round * CTAs + CTA) stays below units + sm_count, which must fit an int.
+  if (units + sm_count > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
   p->B = B;
   p->n_units = static_cast<int>(units);
   p->n_ctas = static_cast<int>(units < sm_count ? units : sm_count);
