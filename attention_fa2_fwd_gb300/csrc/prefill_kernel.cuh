@@ -292,19 +292,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued_k = 0, issued_v = 0, nq = 0;  // K, V tiles and Q pairs issued so far
         int st = 0;                              // ring stage of the next KV tile
         uint32_t ph = 0;                         // its phase
-        int q_wait = -1;                         // what frees Q: -1 nothing, -2 the last Q load, else KE stage
+        int q_wait = -1;                         // what frees Q: -1 nothing, else the KE stage to wait for
         uint32_t q_phase = 0;
         bool ok = true;
         for (int k = 0; ok && k * u_step < n_units; ++k) {
           const int u = unit_index(k, u_first, u_step);
           if (u >= n_units) continue;
           const Unit U = make_unit<CAUSAL, VARLEN>(u, p, win_l, win_r);
-          if (U.kind != kRun) continue;
+          // A unit without KV tiles (every row's band empty, possible with
+          // windows) has no product that reads Q, so it gets no Q load.  Each Q
+          // load is then followed by S products, and the release below implies
+          // the MMA thread has passed its wait for the previous Q: the Q barrier
+          // never runs two phases ahead of that wait.
+          if (U.kind != kRun || U.J0 == U.J1) continue;
           // The previous unit's Q is free once its last S product completed: the
           // release of its last K stage (in-order MMAs: every S product before it
-          // is complete too), or -- for a unit without KV tiles -- once its Q landed.
+          // is complete too).
           if (q_wait >= 0) ok = mbar_wait(BAR(C::B_KE + q_wait), q_phase, abort_flag, p.err);
-          else if (q_wait == -2) ok = mbar_wait(BAR(C::B_Q), (nq - 1) & 1, abort_flag, p.err);
           if (!ok) break;
           mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QT_BYTES);
 #pragma unroll
@@ -337,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               ph ^= 1;
             }
           }
-          if (U.J0 == U.J1) q_wait = -2;
         }
         if (!ok) {
           // Let every copy already issued land before shared memory is released.
@@ -400,8 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nvz;
             return zeroed;
           };
-          if (!(ok = mbar_wait(BAR(C::B_Q), nq & 1, abort_flag, p.err))) break;
-          ++nq;
+          // A unit without KV tiles gets no Q load (see the producer): its wait
+          // is for the previous, already completed phase, and passes at once.
+          const bool has_kv = J0 < J1;
+          if (!(ok = mbar_wait(BAR(C::B_Q), (nq + (has_kv ? 0 : 1)) & 1, abort_flag, p.err))) break;
+          nq += has_kv ? 1 : 0;
           bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
           bool h1p = false;       // tile 1 uses KV tile j-1
           bool first0 = true, first1 = true;
@@ -479,10 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          // A query tile whose band holds no key: O is never written; the epilogue
-          // stores zeros for it.
-          if (lo0 >= hi0) tc_commit(BAR(C::B_OD + 0));
-          if (lo1 >= hi1) tc_commit(BAR(C::B_OD + 1));
+          // A query tile whose band holds no key gets no product and no O-done
+          // signal: its softmax warps store zeros without waiting.  (Signalled
+          // here, a run of such units would let this thread complete the
+          // barrier's phases faster than the softmax warps consume them.)
         }
         tc_commit(BAR(C::B_DONE));
         mbar_wait(BAR(C::B_DONE), 0, nullptr, p.err);
@@ -680,8 +686,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(C::B_PF + t));
       }
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OD + t), od, abort_flag, p.err));
-      od ^= 1;
+      // O-done comes only for a tile with keys, one phase per such unit; the
+      // MMA thread cannot signal the next one before these warps' next P-ready
+      // arrival, so the barrier stays within one phase of this wait.
+      if (jlo < jhi) {
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OD + t), od, abort_flag, p.err));
+        od ^= 1;
+      }
       if (!ok) break;
       // -------------------------------------------------------- epilogue: O / l, LSE
       tc_fence_after();

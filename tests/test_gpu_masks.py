@@ -82,6 +82,27 @@ def test_prefill_window_alibi(name, Nq, Nkv, causal, wl, wr, alibi, D, dtype):
     _assert_masked(o, lse, o_ref, lse_ref, name)
 
 
+def test_prefill_many_keyless_units_after_one_with_keys():
+    """Window (0, 0) over 128 keys and 8192 queries: each CTA runs one unit with
+    keys and then ~31 units whose bands hold none (no Q load, no products) --
+    the MMA thread's Q waits must stay in step with the producer's loads."""
+    import attention_fa2_fwd_gb300 as A
+    B, Hq, Hkv, Nq, Nkv, D = 1, 152, 8, 8192, 128, 64
+    q, k, v = I.prefill_inputs(B, Hq, Hkv, Nq, Nkv, D, "bf16", seed=21)
+    for _ in range(3):
+        o, lse = A.prefill(q.cuda(), k.cuda(), v.cuda(), causal=False, window=(0, 0))
+    torch.cuda.synchronize()
+    o, lse = np64(o), np64(lse)
+    # row i < Nkv sees key i alone: O = V[i] exactly, LSE = the scaled score
+    g = Hq // Hkv
+    v_rows = np64(v)[:, np.arange(Hq) // g]  # (B, Hq, Nkv, D)
+    assert (o[:, :, :Nkv] == v_rows).all()
+    s = (np64(q)[:, :, :Nkv] * np64(k)[:, np.arange(Hq) // g]).sum(-1) / math.sqrt(D)
+    assert np.abs(lse[:, :, :Nkv] - s).max() <= 1e-3
+    # rows past the keys: O = 0, LSE = -inf
+    assert (o[:, :, Nkv:] == 0).all() and np.isneginf(lse[:, :, Nkv:]).all()
+
+
 def test_prefill_window_bhnd_and_bnhd_layouts_agree():
     """The options do not depend on the memory layout of Q, K, V, O."""
     import attention_fa2_fwd_gb300 as A
