@@ -53,6 +53,16 @@ def decode_bytes(B, Hkv, L, D, **_):
     return 2 * B * Hkv * L * D * 2
 
 
+def prefill_exps(B, Hq, N, causal, **_):
+    """Exponentials the softmax needs: one per attended (query, key) pair."""
+    return B * Hq * (N * (N + 1) / 2 if causal else N * N)
+
+
+# ex2.approx.f32 lanes per clock per SM on this part (a stand-alone issue-rate
+# micro-benchmark); times the SM count and the SM clock it is the exp peak.
+EX2_LANES_PER_CLK_SM = 32
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -282,6 +292,10 @@ def run_ours(args, rank, world, local_rank):
     dec_avg = sum_dec / args.steps
     ach = flops / (pre_avg * 1e-3) / 1e12
     ach_d = kvb / (dec_avg * 1e-3) / 1e9
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk_mhz = (clocks or {}).get("sm_mhz") or (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
+    exp_rate = prefill_exps(**P) / (pre_avg * 1e-3)
+    exp_peak = EX2_LANES_PER_CLK_SM * sms * clk_mhz * 1e6
     tr = profiled_traffic("prefill_fwd")
     tr_d = profiled_traffic("decode_split")
     line = {
@@ -303,6 +317,11 @@ def run_ours(args, rank, world, local_rank):
                    "decode_splits": splits},
         "prefill_ms": round(pre_avg, 4),
         "prefill_ms_median": round(statistics.median(pre_ms), 4) if world == 1 else None,
+        "prefill_ms_std": round(statistics.pstdev(pre_ms), 4) if world == 1 else None,
+        "decode_ms_std": round(statistics.pstdev(dec_ms), 4) if world == 1 else None,
+        "exp_rate": {"value": round(exp_rate / 1e12, 3), "unit": "Texp/s", "exps_per_step": prefill_exps(**P),
+                     "peak": round(exp_peak / 1e12, 3), "frac": round(exp_rate / exp_peak, 4),
+                     "peak_source": f"ex2 {EX2_LANES_PER_CLK_SM} lanes/clk/SM x {sms} SMs x {clk_mhz:.0f} MHz (secondary: the tensor pipe bounds the prefill)"},
         "decode": {"value": round(decode_gbs, 1), "unit": "GB/s", "ms_per_step": round(dec_avg, 4),
                    "kv_bytes_per_step": kvb, "kernels": "kv_cache_write + decode_split" + (" + decode_merge" if splits > 1 else "")},
         "region_ms_incl_flush": round(region_ms, 3),
