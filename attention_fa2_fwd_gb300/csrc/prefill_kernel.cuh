@@ -403,10 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nvz;
             return zeroed;
           };
-          // A unit without KV tiles gets no Q load (see the producer): its wait
-          // is for the previous, already completed phase, and passes at once.
+          // A unit without KV tiles gets no Q load (see the producer) and must not
+          // wait for one: the next unit's Q may already have landed, so not even
+          // the Q barrier's previous phase can be waited for.  It waits instead
+          // on the all-done barrier's (never incomplete) phase before its first,
+          // which passes at once.
           const bool has_kv = J0 < J1;
-          if (!(ok = mbar_wait(BAR(C::B_Q), (nq + (has_kv ? 0 : 1)) & 1, abort_flag, p.err))) break;
+          if (!(ok = mbar_wait(BAR(has_kv ? C::B_Q : C::B_DONE), has_kv ? (nq & 1) : 1u, abort_flag, p.err))) break;
           nq += has_kv ? 1 : 0;
           bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
           bool h1p = false;       // tile 1 uses KV tile j-1

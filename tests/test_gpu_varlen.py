@@ -109,3 +109,31 @@ def test_varlen_bad_offsets_are_reported():
     assert A.attn_get_device_error(torch.cuda.current_stream().cuda_stream) == A.ATTN_ERR_DEVICE_INDEX
     A.prefill_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), 32, 64)  # length above max_seqlen_q
     assert A.attn_get_device_error(torch.cuda.current_stream().cuda_stream) == A.ATTN_ERR_DEVICE_INDEX
+
+
+@pytest.mark.parametrize("causal,window", [(True, (-1, -1)), (False, (-1, -1)), (True, (32, -1)), (False, (16, 16))])
+def test_varlen_many_short_sequences(causal, window):
+    """1500 packed sequences with independent query and key lengths in 0..400
+    (zeros included): every CTA runs dozens of units that mix full, ragged,
+    key-less (windows, more queries than keys) and empty sequences."""
+    import attention_fa2_fwd_gb300 as A
+    from oracle import masked as M
+    rng = np.random.default_rng(5)
+    n = 1500
+    lens_q = rng.integers(0, 401, n)
+    lens_k = rng.integers(0, 401, n)
+    lens_q[::97] = 0
+    lens_k[::89] = 0
+    q, k, v, cq, ck = _packed(lens_q.tolist(), lens_k.tolist(), 4, 2, 64, "bf16", seed=17)
+    o, lse = A.prefill_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), int(lens_q.max()),
+                              int(lens_k.max()), causal=causal, window=window)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = M.prefill_varlen_masked(np64(q), np64(k), np64(v), cq.numpy(), ck.numpy(), causal, 1 / 8,
+                                             window[0], window[1])
+    o, lse = np64(o), np64(lse)
+    empty = np.isneginf(lse_ref)  # (H_q, total_q): rows that see no key
+    assert (np.isneginf(lse) == empty).all(), "rows without keys differ"
+    assert (o.transpose(1, 0, 2)[empty] == 0).all(), "rows without keys are not zero"
+    full = ~empty
+    assert_close(o.transpose(1, 0, 2)[full], o_ref.transpose(1, 0, 2)[full], lse[full], lse_ref[full],
+                 f"many sequences causal={causal} window={window}")
