@@ -410,6 +410,78 @@ def run_reference(args, rank, world):
     }
 
 
+def oracle_config_table():
+    """Wall time of the fp64 oracle on each parity configuration, on this host's cores.
+
+    All cores for every configuration, one core as well for the small MHA case
+    and the cross-attention; the N=8192 causal prefill on sampled rows (its
+    full run is hours), extrapolated by FLOPs.  Prints one JSON line per entry.
+    """
+    import numpy as np
+    import torch
+
+    import oracle
+    from attention_fa2_fwd_gb300 import inputs as I
+    oracle.build()
+    cores = oracle.default_threads()
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True).stdout
+        model = next((l.split(":", 1)[1].strip() for l in out.splitlines() if l.startswith("Model name")), "")
+    except OSError:
+        pass
+
+    def f64(t):
+        return t.to(torch.float64).numpy()
+
+    def emit(config, what, seconds, threads, flops=None):
+        rec = {"oracle_config": config, "what": what, "seconds": round(seconds, 4), "threads": threads,
+               "host": model, "nproc": os.cpu_count()}
+        if flops:
+            rec["tflops"] = round(flops / seconds / 1e12, 5)
+        print(json.dumps(rec), flush=True)
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    c = I.MHA_256
+    q, k, v = (f64(t) for t in c.make())
+    for th in (cores, 1):
+        emit(1, c.name, timed(lambda: oracle.attention(q, k, v, c.causal, c.scale, nthreads=th)), th, c.flops)
+    for n in (2048, 4096):
+        c = I.GQA_CAUSAL[n]
+        q, k, v = (f64(t) for t in c.make())
+        emit(2, c.name, timed(lambda: oracle.attention(q, k, v, c.causal, c.scale, nthreads=cores)), cores, c.flops)
+    c = I.GQA_CAUSAL[8192]
+    q, k, v = (f64(t) for t in c.make())
+    rng = np.random.default_rng(0)
+    sel = np.stack([rng.integers(0, c.B, 4096), rng.integers(0, c.Hq, 4096), rng.integers(0, c.Nq, 4096)], 1)
+    sec = timed(lambda: oracle.attention_rows(q, k, v, True, c.scale, sel, nthreads=cores))
+    f = float(sum(4 * c.D * (int(i) + 1) for i in sel[:, 2]))
+    emit(2, c.name + " (4096 sampled rows; full run extrapolated by FLOPs: %.0f s)" % (sec * c.flops / f), sec,
+         cores, f)
+    tot, fl = 0.0, 0.0
+    for c in I.sweep_cases():
+        q, k, v = (f64(t) for t in c.make())
+        tot += timed(lambda: oracle.attention(q, k, v, c.causal, c.scale, nthreads=cores))
+        fl += c.flops
+    emit(3, "sweep, 160 cases", tot, cores, fl)
+    for B in I.DECODE_B:
+        kk, vv = (f64(t) for t in I.decode_stream(B, 8, max(I.DECODE_LENS), 128, "bf16"))
+        qs = f64(I.decode_queries(B, 32, 128, [L - 1 for L in I.DECODE_LENS], "bf16"))
+        tot = 0.0
+        for j, L in enumerate(I.DECODE_LENS):
+            tot += timed(lambda: oracle.decode(qs[:, :, j], kk, vv, L, 1 / math.sqrt(128), nthreads=cores))
+        emit(4, f"decode B={B}, one step at each of L={list(I.DECODE_LENS)}", tot, cores)
+    for D in sorted(I.CROSS):
+        c = I.CROSS[D]
+        q, k, v = (f64(t.contiguous()) for t in c.make())
+        for th in (cores, 1):
+            emit(5, c.name, timed(lambda: oracle.attention(q, k, v, c.causal, c.scale, nthreads=th)), th, c.flops)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,6 +489,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--oracle-configs", action="store_true",
+                    help="with --impl reference: time the oracle on every parity configuration (a few minutes)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -425,6 +499,10 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.impl == "reference" and args.oracle_configs:
+        if rank == 0:
+            oracle_config_table()
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:
