@@ -29,6 +29,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <utility>
+
 #include "attn_internal.h"
 #include "ptx.cuh"
 
@@ -127,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const DecodeParams p) {
   using C = DecCfg<D, GH>;
   extern __shared__ uint8_t smem_raw[];
+  griddep_wait();  // before any global memory access (launched with programmatic serialization)
   if (load_volatile(p.err) != 0) return;
 
   const uint32_t raw = smem_u32(smem_raw);
@@ -419,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
+  griddep_wait();
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, hq = bh % p.Hq;
   const int d = threadIdx.x;
@@ -441,6 +445,7 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
 }
 
 __global__ void __launch_bounds__(256) kv_cache_write_kernel(const KvWriteParams p) {
+  griddep_wait();
   if (load_volatile(p.err) != 0) return;
   const int pieces = p.D / 8;  // 16-byte pieces per row
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < 2 * p.total_units;
@@ -470,6 +475,7 @@ __global__ void __launch_bounds__(256) kv_cache_write_kernel(const KvWriteParams
 // i.e. row (pos % page_size) of page block_table[b][pos / page_size].  A page
 // id or position out of range skips the write and records kErrBadIndex.
 __global__ void __launch_bounds__(256) kv_cache_write_paged_kernel(const KvWriteParams p) {
+  griddep_wait();
   if (load_volatile(p.err) != 0) return;
   const int pieces = p.D / 8;
   for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < 2 * p.total_units;
@@ -503,6 +509,27 @@ __global__ void __launch_bounds__(256) kv_cache_write_paged_kernel(const KvWrite
   }
 }
 
+// Launches with programmatic stream serialization: the kernel's blocks may be
+// scheduled while the preceding kernel of the stream drains, which hides the
+// launch gap between the short kernels of a decode step.  Every kernel launched
+// this way calls griddep_wait() before it touches global memory, so it reads
+// and writes nothing the preceding kernel is still using.
+template <typename... Params, typename... Args>
+cudaError_t launch_serialized(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int D, int GH, bool BF16, bool PAGED>
 cudaError_t launch_split(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int B, int Hkv,
                          cudaStream_t stream) {
@@ -512,11 +539,9 @@ cudaError_t launch_split(const CUtensorMap &tk, const CUtensorMap &tv, const Dec
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   dim3 grid(p.nsplit, Hkv * p.nhc, B);
-  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tk, tv, p);
-  e = cudaGetLastError();
+  e = launch_serialized(kern, grid, dim3(kThreads), C::SMEM_BYTES, stream, tk, tv, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
-  decode_merge_kernel<D, BF16><<<B * p.Hq, D, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_serialized(decode_merge_kernel<D, BF16>, dim3(B * p.Hq), dim3(D), 0, stream, p);
 }
 
 }  // namespace
@@ -549,11 +574,8 @@ cudaError_t launch_kv_cache_write(const KvWriteParams &p, bool paged, cudaStream
   const int64_t work = 2 * p.total_units;
   int64_t blocks = (work + 255) / 256;
   if (blocks > 65535 * 8) blocks = 65535 * 8;
-  if (paged)
-    kv_cache_write_paged_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  else
-    kv_cache_write_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_serialized(paged ? kv_cache_write_paged_kernel : kv_cache_write_kernel,
+                           dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
 
 }  // namespace attn

@@ -81,6 +81,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may be scheduled while the preceding kernel
+// of its stream is still finishing; this waits until that kernel has completed
+// and its memory writes are visible.  Without the attribute it returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 // 4-D tiled bulk tensor load global -> shared, completion counted in bytes on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
