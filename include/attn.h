@@ -27,6 +27,10 @@
  *   contiguous.  Accumulation is fp32 throughout.
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   Every call is stream-ordered and returns once its kernels are enqueued.
+ *   The decode calls and the cache writes launch their kernels with
+ *   programmatic stream serialization (each kernel may be scheduled while the
+ *   preceding kernel of the stream drains, and waits for it to complete before
+ *   it touches memory), which keeps stream order for the caller.
  * - Argument errors are detected on the host before anything is launched and
  *   are returned synchronously; nothing is enqueued in that case.  A failed
  *   launch returns ATTN_ERR_CUDA.
