@@ -292,23 +292,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued_k = 0, issued_v = 0, nq = 0;  // K, V tiles and Q pairs issued so far
         int st = 0;                              // ring stage of the next KV tile
         uint32_t ph = 0;                         // its phase
-        int q_wait = -1;                         // what frees Q: -1 nothing, else the KE stage to wait for
+        int q_wait = -1;                         // what frees Q: -1 nothing, -2 the last Q load, else KE stage
         uint32_t q_phase = 0;
         bool ok = true;
         for (int k = 0; ok && k * u_step < n_units; ++k) {
           const int u = unit_index(k, u_first, u_step);
           if (u >= n_units) continue;
           const Unit U = make_unit<CAUSAL, VARLEN>(u, p, win_l, win_r);
-          // A unit without KV tiles (every row's band empty, possible with
-          // windows) has no product that reads Q, so it gets no Q load.  Each Q
-          // load is then followed by S products, and the release below implies
-          // the MMA thread has passed its wait for the previous Q: the Q barrier
-          // never runs two phases ahead of that wait.
-          if (U.kind != kRun || U.J0 == U.J1) continue;
+          if (U.kind != kRun) continue;
+          // With windows (MASKED), a unit without KV tiles (every row's band
+          // empty) has no product that reads Q, so it gets no Q load.  Each Q load
+          // is then followed by S products, and the release below implies the MMA
+          // thread has passed its wait for the previous Q: the Q barrier never
+          // runs two phases ahead of that wait.  Without windows every unit has
+          // KV tiles.
+          if constexpr (MASKED) {
+            if (U.J0 == U.J1) continue;
+          }
           // The previous unit's Q is free once its last S product completed: the
           // release of its last K stage (in-order MMAs: every S product before it
-          // is complete too).
+          // is complete too), or -- for a unit without KV tiles -- once its Q landed.
           if (q_wait >= 0) ok = mbar_wait(BAR(C::B_KE + q_wait), q_phase, abort_flag, p.err);
+          else if (q_wait == -2) ok = mbar_wait(BAR(C::B_Q), (nq - 1) & 1, abort_flag, p.err);
           if (!ok) break;
           mbar_arrive_expect_tx(BAR(C::B_Q), 2 * C::QT_BYTES);
 #pragma unroll
@@ -341,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ph ^= 1;
             }
           }
+          if (U.J0 == U.J1) q_wait = -2;
         }
         if (!ok) {
           // Let every copy already issued land before shared memory is released.
@@ -403,14 +409,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nvz;
             return zeroed;
           };
-          // A unit without KV tiles gets no Q load (see the producer) and must not
-          // wait for one: the next unit's Q may already have landed, so not even
-          // the Q barrier's previous phase can be waited for.  It waits instead
-          // on the all-done barrier's (never incomplete) phase before its first,
-          // which passes at once.
-          const bool has_kv = J0 < J1;
-          if (!(ok = mbar_wait(BAR(has_kv ? C::B_Q : C::B_DONE), has_kv ? (nq & 1) : 1u, abort_flag, p.err))) break;
-          nq += has_kv ? 1 : 0;
+          if constexpr (MASKED) {
+            // A unit without KV tiles gets no Q load (see the producer) and must
+            // not wait for one: the next unit's Q may already have landed, so not
+            // even the Q barrier's previous phase can be waited for.  It waits
+            // instead on the all-done barrier's (never incomplete) phase before
+            // its first, which passes at once.
+            const bool has_kv = J0 < J1;
+            if (!(ok = mbar_wait(BAR(has_kv ? C::B_Q : C::B_DONE), has_kv ? (nq & 1) : 1u, abort_flag, p.err)))
+              break;
+            nq += has_kv ? 1 : 0;
+          } else {
+            if (!(ok = mbar_wait(BAR(C::B_Q), nq & 1, abort_flag, p.err))) break;
+            ++nq;
+          }
           bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
           bool h1p = false;       // tile 1 uses KV tile j-1
           bool first0 = true, first1 = true;
@@ -488,10 +500,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          // A query tile whose band holds no key gets no product and no O-done
-          // signal: its softmax warps store zeros without waiting.  (Signalled
-          // here, a run of such units would let this thread complete the
-          // barrier's phases faster than the softmax warps consume them.)
+          // With windows (MASKED), a query tile whose band holds no key gets no
+          // product and no O-done signal: its softmax warps store zeros without
+          // waiting.  (Signalled here, a run of such units would let this thread
+          // complete the barrier's phases faster than the softmax warps consume
+          // them.)  Without windows no band is empty.
+          if constexpr (!MASKED) {
+            if (lo0 >= hi0) tc_commit(BAR(C::B_OD + 0));
+            if (lo1 >= hi1) tc_commit(BAR(C::B_OD + 1));
+          }
         }
         tc_commit(BAR(C::B_DONE));
         mbar_wait(BAR(C::B_DONE), 0, nullptr, p.err);
@@ -689,10 +706,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(C::B_PF + t));
       }
-      // O-done comes only for a tile with keys, one phase per such unit; the
-      // MMA thread cannot signal the next one before these warps' next P-ready
-      // arrival, so the barrier stays within one phase of this wait.
-      if (jlo < jhi) {
+      // O-done comes only for a tile with keys (MASKED: one phase per such
+      // unit); the MMA thread cannot signal the next one before these warps'
+      // next P-ready arrival, so the barrier stays within one phase of this wait.
+      if (!MASKED || jlo < jhi) {
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OD + t), od, abort_flag, p.err));
         od ^= 1;
       }
