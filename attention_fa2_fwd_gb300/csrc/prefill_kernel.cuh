@@ -4,9 +4,10 @@
 // (sliding windows and ALiBi), which instantiate it with MASKED false / true
 // in separate translation units compiled in parallel.
 //
-// One CTA computes TWO 128-row query tiles (rows q0..q0+255) of one
-// (batch, q-head), so the tensor core always has one tile's matrix products
-// to run while the other tile's softmax is computed:
+// Persistent: one CTA per SM walks a sequence of units; a unit is TWO 128-row
+// query tiles (rows q0..q0+255) of one (batch, q-head), so the tensor core
+// always has one tile's matrix products to run while the other tile's softmax
+// is computed:
 //   warps 0-3   softmax warpgroup of tile 0, one thread per query row (TMEM lane)
 //   warps 4-7   softmax warpgroup of tile 1
 //   warp 8      TMA producer: both Q tiles once, then K and V tiles of 128 keys
@@ -14,7 +15,9 @@
 //   warp 9      TMEM allocator and tcgen05 MMA issuer (one thread), per KV tile j:
 //                 S0_j = Q0 K_j^T;  O1 += P1_{j-1} V_{j-1};  S1_j = Q1 K_j^T;  O0 += P0_j V_j
 //               (SS form for Q K^T, TS form with P read from TMEM for P V)
-//   warps 10-11 idle (they complete the register split of their warpgroup)
+//   warp 10     variable length only: zeroes the rows past a sequence's end in
+//               its last V tile before P V reads it
+//   warp 11     idle (it completes the register split of its warpgroup)
 //
 // The algorithm is the online softmax of "Skill: Write a Triton Attention
 // Kernel" (Required reasoning process, steps 4-9): running max m and sum l in
