@@ -39,7 +39,7 @@ EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_ex", "attn_fwd_prefill_host", "
            "attn_fwd_decode_ex", "attn_fwd_decode_paged_ex", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
            "attn_fwd_decode_noalloc", "kv_cache_write", "attn_fwd_decode_paged", "kv_cache_write_paged",
            "attn_bwd_workspace_size", "attn_bwd",
-           "attn_get_device_error", "attn_status_string", "attn_version")
+           "attn_get_device_error", "attn_selftest_wait_timeout", "attn_status_string", "attn_version")
 
 
 class AttnLibraryMissing(RuntimeError):
@@ -128,6 +128,8 @@ def lib() -> ctypes.CDLL:
                                    i64p, i64p, i64p, i64p, i64p, i64p, i64p, i64p, i32, f32, vp, ctypes.c_size_t, vp]
             L.attn_get_device_error.restype = i32
             L.attn_get_device_error.argtypes = [vp]
+            L.attn_selftest_wait_timeout.restype = i32
+            L.attn_selftest_wait_timeout.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
             L.attn_status_string.argtypes = [i32]
             L.attn_version.restype = i32
@@ -281,6 +283,11 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, dtype, B, H_q, H_kv, N_q, N_kv, 
 
 def attn_get_device_error(stream=None) -> int:
     return lib().attn_get_device_error(stream)
+
+
+def attn_selftest_wait_timeout(stream=None) -> int:
+    """Enqueue the bounded-wait self-test kernel (see include/attn.h); returns its launch status."""
+    return lib().attn_selftest_wait_timeout(stream)
 
 
 def attn_status_string(status: int) -> str:

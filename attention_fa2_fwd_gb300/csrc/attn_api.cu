@@ -192,6 +192,21 @@ attn_status_t read_options(const attn_options_t *opts, int *wl, int *wr, const f
   return ATTN_OK;
 }
 
+// Failure-detection self-test: one thread waits on an mbarrier that nothing
+// ever arrives on.  The bounded wait gives up after its wall-clock limit,
+// records kErrWaitTimeout in the device error word and returns.
+__global__ void selftest_wait_kernel(unsigned *err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, err);
+}
+
 // Persistent prefill schedule: units = query-tile pairs x heads x batches,
 // one CTA per SM at most.
 attn_status_t prefill_schedule(PrefillParams *p, int B, int H_q, int sm_count) {
@@ -714,6 +729,14 @@ attn_status_t kv_cache_write_paged(void *k_pages, void *v_pages, const void *k_n
   p.num_pages = num_pages;
   cudaError_t e = launch_kv_cache_write(p, true, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_selftest_wait_timeout(void *stream) {
+  const DeviceState *dev = nullptr;
+  attn_status_t st = device_state(&dev);
+  if (st != ATTN_OK) return st;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->err);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_get_device_error(void *stream) {

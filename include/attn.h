@@ -428,6 +428,19 @@ attn_status_t kv_cache_write_paged(void *k_pages, void *v_pages, const void *k_n
  */
 attn_status_t attn_get_device_error(void *stream);
 
+/*
+ * attn_selftest_wait_timeout -- failure-detection self-test.  Enqueues one
+ * small kernel on `stream` that waits on a shared-memory mbarrier nothing
+ * ever arrives on, through the same bounded wait every pipeline wait of the
+ * library uses (a wall-clock limit of 4 s, then the wait gives up, records
+ * the time-out in the device error word and the kernel returns).  The next
+ * attn_get_device_error() on the stream then returns ATTN_ERR_DEVICE_TIMEOUT
+ * and clears the word; the CUDA context stays usable.  Returns ATTN_OK after
+ * enqueueing, ATTN_ERR_UNSUPPORTED on a device other than sm_103, ATTN_ERR_CUDA
+ * if the launch failed.
+ */
+attn_status_t attn_selftest_wait_timeout(void *stream);
+
 /* attn_status_string -- static, human-readable name of a status code. */
 const char *attn_status_string(attn_status_t status);
 
