@@ -56,3 +56,34 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "TFLOPS" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_exponential_count_and_nvtx_fallback():
+    sys.path.insert(0, ROOT)
+    import bench
+    # one exponential per attended (query, key) pair
+    assert bench.prefill_exps(B=1, Hq=1, N=4, causal=True) == 10
+    assert bench.prefill_exps(B=2, Hq=3, N=4, causal=False) == 2 * 3 * 16
+    push, pop = bench.nvtx_ranges()
+    push("x")
+    pop()
+
+
+def test_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "attention_fa2_fwd_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cuh").write_text("kernel v1\n")
+    import hashlib
+    sha = hashlib.sha256(b"kernel v1\n").hexdigest()
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic.json").write_text(json.dumps({"k": {"source": "k.cuh", "source_sha256": sha,
+                                                         "dram_bytes_per_launch": 123}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "PROFILES", str(prof))
+    assert bench.profiled_traffic("k") == 123.0
+    (src / "k.cuh").write_text("kernel v2\n")  # the source changed after the capture
+    assert bench.profiled_traffic("k") is None
+    assert bench.profiled_traffic("missing") is None
