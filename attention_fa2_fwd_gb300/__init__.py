@@ -53,9 +53,11 @@ class AttnError(RuntimeError):
 
 
 class AttnOptions(ctypes.Structure):
-    """attn_options_t: sliding-window bounds (-1: none) and ALiBi slopes (device fp32 pointer or None)."""
+    """attn_options_t: sliding-window bounds (-1: none), ALiBi slopes (device fp32 pointer or None),
+    rotary embedding base (0: none) and pairing, and the decode split count (0: automatic)."""
     _fields_ = [("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
-                ("alibi_slopes", ctypes.c_void_p)]
+                ("alibi_slopes", ctypes.c_void_p), ("rope_theta", ctypes.c_float),
+                ("rope_interleaved", ctypes.c_int32), ("num_splits", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -197,16 +199,23 @@ def attn_fwd_prefill_host(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, ca
                                        _opts(opts), workspace, workspace_bytes, stream)
 
 
-def make_options(window_left: int = -1, window_right: int = -1, alibi_slopes=None):
-    """An AttnOptions for the *_ex calls (None when nothing is set); alibi_slopes: fp32 CUDA tensor (H_q)."""
-    if window_left == -1 and window_right == -1 and alibi_slopes is None:
+def make_options(window_left: int = -1, window_right: int = -1, alibi_slopes=None, rope_theta: float = 0.0,
+                 rope_interleaved: bool = False, num_splits: int = 0):
+    """An AttnOptions for the *_ex calls (None when nothing is set).
+
+    alibi_slopes: fp32 CUDA tensor (H_q); rope_theta: base of the rotary embedding (0: none);
+    rope_interleaved: pairs (2c, 2c+1) instead of (c, c+D/2); num_splits: decode split count (0: automatic).
+    """
+    if (window_left == -1 and window_right == -1 and alibi_slopes is None and not rope_theta
+            and not num_splits):
         return None
     if alibi_slopes is not None:
         import torch
         if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda:
             raise TypeError("alibi_slopes must be an fp32 CUDA tensor")
     return AttnOptions(int(window_left), int(window_right),
-                       alibi_slopes.data_ptr() if alibi_slopes is not None else None)
+                       alibi_slopes.data_ptr() if alibi_slopes is not None else None, float(rope_theta),
+                       1 if rope_interleaved else 0, int(num_splits))
 
 
 def attn_fwd_prefill_varlen(q, k, v, o, lse, dtype, B, H_q, H_kv, D, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
@@ -440,10 +449,13 @@ def decode_workspace(B, H_q, H_kv, D, device=None):
 
 
 def decode(q, k_cache, v_cache, cache_len: int, scale: float | None = None, return_lse: bool = True, out=None,
-           lse_out=None, workspace=None, stream=None, window_left: int = -1, alibi_slopes=None):
+           lse_out=None, workspace=None, stream=None, window_left: int = -1, alibi_slopes=None,
+           num_splits: int = 0):
     """One query token per (batch, q-head) over the first cache_len cache rows.
 
     q (B,H_q,D) or (B,H_q,1,D); caches (B,H_kv,max_len,D).  Returns (O (B,H_q,D), LSE (B,H_q)).
+    num_splits: 0 automatic, n >= 1 at most n KV splits (a workspace for more splits than the automatic
+    choice must be passed in).
     """
     import torch
     q4 = q if q.dim() == 4 else q.unsqueeze(2)
@@ -463,7 +475,8 @@ def decode(q, k_cache, v_cache, cache_len: int, scale: float | None = None, retu
     st = attn_fwd_decode_ex(q4.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o4.data_ptr(),
                             lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, int(cache_len), D,
                             q4.stride(), k_cache.stride(), v_cache.stride(), o4.stride(), scale, ws_ptr, ws_bytes,
-                            make_options(window_left, -1, alibi_slopes), _stream_handle(stream))
+                            make_options(window_left, -1, alibi_slopes, num_splits=num_splits),
+                            _stream_handle(stream))
     _check(st, "attn_fwd_decode")
     return o, lse
 

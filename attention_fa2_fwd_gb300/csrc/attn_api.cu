@@ -19,12 +19,17 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 __device__ unsigned g_device_error = 0;
+// Where attn_get_device_error's one-thread kernel leaves the word it took.
+__device__ unsigned g_device_error_taken = 0;
+
+__global__ void take_error_kernel(unsigned *err, unsigned *out) { *out = atomicExch(err, 0u); }
 
 struct DeviceState {
   bool ready = false;
   bool supported = false;
   int sm_count = 0;
   unsigned *err = nullptr;
+  unsigned *taken = nullptr;
 };
 
 std::mutex g_mutex;
@@ -54,6 +59,8 @@ attn_status_t device_state(const DeviceState **out) {
       void *p = nullptr;
       if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return ATTN_ERR_CUDA;
       s.err = static_cast<unsigned *>(p);
+      if (cudaGetSymbolAddress(&p, g_device_error_taken) != cudaSuccess) return ATTN_ERR_CUDA;
+      s.taken = static_cast<unsigned *>(p);
       if (g_encode == nullptr) {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -158,12 +165,20 @@ int decode_max_splits(int B, int H_q, int H_kv, int sm_count) {
 
 // Split plan of one decode call: every split holds a multiple of the stage
 // size in keys (except the last), at least kMinChunk keys, and none is empty.
-void decode_plan(int B, int H_q, int H_kv, int cache_len, int D, int sm_count, int *nsplit_out, int *chunk_out) {
+// forced > 0 (a caller's num_splits) replaces the automatic split count as
+// the upper bound and drops the minimum split length (down to one stage).
+void decode_plan(int B, int H_q, int H_kv, int cache_len, int D, int sm_count, int *nsplit_out, int *chunk_out,
+                 int forced = 0) {
   constexpr int kMinChunk = 256;
   (void)D;
-  const int max_splits = decode_max_splits(B, H_q, H_kv, sm_count);
   const int step = kDecodeStageTokens;
-  int nsplit = std::min<int>(max_splits, (cache_len + kMinChunk - 1) / kMinChunk);
+  int nsplit;
+  if (forced > 0) {
+    nsplit = std::min<int>(forced, (cache_len + step - 1) / step);
+  } else {
+    const int max_splits = decode_max_splits(B, H_q, H_kv, sm_count);
+    nsplit = std::min<int>(max_splits, (cache_len + kMinChunk - 1) / kMinChunk);
+  }
   nsplit = std::max(nsplit, 1);
   int chunk = (cache_len + nsplit - 1) / nsplit;
   chunk = (chunk + step - 1) / step * step;
@@ -178,17 +193,30 @@ size_t decode_ws_bytes(int B, int H_q, int D, int splits) {
 
 bool valid_dtype(attn_dtype_t dt) { return dt == ATTN_F16 || dt == ATTN_BF16; }
 
-// Mask and bias options (NULL: none).
-attn_status_t read_options(const attn_options_t *opts, int *wl, int *wr, const float **slopes) {
-  *wl = -1;
-  *wr = -1;
-  *slopes = nullptr;
+// Mask, bias, position and split options (NULL: none of them).
+struct Opts {
+  int wl = -1, wr = -1;          // window bounds (-1: unbounded)
+  const float *slopes = nullptr; // ALiBi slopes (device, H_q)
+  float rope_theta = 0.f;        // 0: no rotary embedding
+  int rope_interleaved = 0;      // 0: pairs (c, c + D/2); 1: pairs (2c, 2c + 1)
+  int num_splits = 0;            // decode: 0 automatic, else at most this many KV splits
+};
+constexpr int kMaxDecodeSplits = 64;
+
+attn_status_t read_opts(const attn_options_t *opts, Opts *o) {
+  *o = Opts{};
   if (opts == nullptr) return ATTN_OK;
   if (opts->window_left < -1 || opts->window_right < -1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(opts->rope_theta) || opts->rope_theta < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (opts->rope_interleaved != 0 && opts->rope_interleaved != 1) return ATTN_ERR_INVALID_ARG;
+  if (opts->num_splits < 0 || opts->num_splits > kMaxDecodeSplits) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(opts->alibi_slopes) & 3) != 0) return ATTN_ERR_ALIGNMENT;
-  *wl = opts->window_left;
-  *wr = opts->window_right;
-  *slopes = opts->alibi_slopes;
+  o->wl = opts->window_left;
+  o->wr = opts->window_right;
+  o->slopes = opts->alibi_slopes;
+  o->rope_theta = opts->rope_theta;
+  o->rope_interleaved = opts->rope_interleaved;
+  o->num_splits = opts->num_splits;
   return ATTN_OK;
 }
 
@@ -234,6 +262,28 @@ int decode_span(int len, int wl) {
   return static_cast<int>(span < len ? span : len);
 }
 
+// Argument checks of attn_fwd_decode (everything but the options and the
+// workspace), in the order that call applies them: pointers and sizes, then
+// the type and head dimension, then alignment and strides.
+attn_status_t decode_check_args(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                                attn_dtype_t dtype, int B, int H_q, int H_kv, int cache_len, int D,
+                                const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
+                                const int64_t o_str[4], float scale) {
+  if (!q || !k_cache || !v_cache || !o || !q_str || !kc_str || !vc_str || !o_str) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H_q < 1 || H_kv < 1 || cache_len < 1 || D < 1 || H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f) || B > 65535) return ATTN_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3)))
+    return ATTN_ERR_ALIGNMENT;
+  const int64_t qsz[4] = {B, H_q, 1, D}, csz[4] = {B, H_kv, cache_len, D};
+  attn_status_t st;
+  if ((st = check_strides(q_str, qsz)) || (st = check_strides(kc_str, csz)) || (st = check_strides(vc_str, csz)) ||
+      (st = check_strides(o_str, qsz)))
+    return st;
+  return ATTN_OK;
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -269,7 +319,12 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
     return st;
 
   PrefillParams p{};
-  if ((st = read_options(opts, &p.window_left, &p.window_right, &p.alibi_slopes)) != ATTN_OK) return st;
+  Opts op;
+  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
+  p.window_left = op.wl;
+  p.window_right = op.wr;
+  p.alibi_slopes = op.slopes;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
   const bool bf16 = dtype == ATTN_BF16;
@@ -334,7 +389,12 @@ attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const voi
       (st = check_strides(o4, qsz)))
     return st;
   PrefillParams p{};
-  if ((st = read_options(opts, &p.window_left, &p.window_right, &p.alibi_slopes)) != ATTN_OK) return st;
+  Opts op;
+  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
+  p.window_left = op.wl;
+  p.window_right = op.wr;
+  p.alibi_slopes = op.slopes;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
   const bool bf16 = dtype == ATTN_BF16;
@@ -469,21 +529,15 @@ attn_status_t attn_fwd_decode_ex(const void *q, const void *k_cache, const void 
                                  const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
                                  const int64_t o_str[4], float scale, void *workspace, size_t workspace_bytes,
                                  const attn_options_t *opts, void *stream) {
-  if (!q || !k_cache || !v_cache || !o || !q_str || !kc_str || !vc_str || !o_str) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || H_q < 1 || H_kv < 1 || cache_len < 1 || D < 1 || H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f) || B > 65535) return ATTN_ERR_INVALID_ARG;
-  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
-      (lse && (reinterpret_cast<uintptr_t>(lse) & 3)))
-    return ATTN_ERR_ALIGNMENT;
-  const int64_t qsz[4] = {B, H_q, 1, D}, csz[4] = {B, H_kv, cache_len, D};
-  attn_status_t st;
-  if ((st = check_strides(q_str, qsz)) || (st = check_strides(kc_str, csz)) || (st = check_strides(vc_str, csz)) ||
-      (st = check_strides(o_str, qsz)))
-    return st;
-  int wl, wr;
-  const float *slopes;
-  if ((st = read_options(opts, &wl, &wr, &slopes)) != ATTN_OK) return st;
+  attn_status_t st = decode_check_args(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, q_str, kc_str,
+                                       vc_str, o_str, scale);
+  if (st != ATTN_OK) return st;
+  const int64_t csz[4] = {B, H_kv, cache_len, D};
+  Opts op;
+  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
+  const int wl = op.wl;
+  const float *slopes = op.slopes;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
 
@@ -491,7 +545,7 @@ attn_status_t attn_fwd_decode_ex(const void *q, const void *k_cache, const void 
   const int gh = decode_heads_per_cta(group);
   const int nhc = (group + gh - 1) / gh;
   int nsplit = 1, chunk = cache_len;
-  decode_plan(B, H_q, H_kv, decode_span(cache_len, wl), D, dev->sm_count, &nsplit, &chunk);
+  decode_plan(B, H_q, H_kv, decode_span(cache_len, wl), D, dev->sm_count, &nsplit, &chunk, op.num_splits);
   if (nsplit > 1) {
     const size_t need = decode_ws_bytes(B, H_q, D, nsplit);
     if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
@@ -623,9 +677,11 @@ attn_status_t attn_fwd_decode_paged_ex(const void *q, const void *k_pages, const
   if ((st = check_strides(q_str, qsz)) || (st = check_strides(kp_str, psz)) || (st = check_strides(vp_str, psz)) ||
       (st = check_strides(o_str, qsz)))
     return st;
-  int wl, wr;
-  const float *slopes;
-  if ((st = read_options(opts, &wl, &wr, &slopes)) != ATTN_OK) return st;
+  Opts op;
+  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
+  const int wl = op.wl;
+  const float *slopes = op.slopes;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
 
@@ -633,7 +689,7 @@ attn_status_t attn_fwd_decode_paged_ex(const void *q, const void *k_pages, const
   const int gh = decode_heads_per_cta(group);
   const int nhc = (group + gh - 1) / gh;
   int nsplit = 1, chunk = max_cache_len;
-  decode_plan(B, H_q, H_kv, decode_span(max_cache_len, wl), D, dev->sm_count, &nsplit, &chunk);
+  decode_plan(B, H_q, H_kv, decode_span(max_cache_len, wl), D, dev->sm_count, &nsplit, &chunk, op.num_splits);
   if (nsplit > 1) {
     const size_t need = decode_ws_bytes(B, H_q, D, nsplit);
     if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
@@ -743,12 +799,19 @@ attn_status_t attn_get_device_error(void *stream) {
   const DeviceState *dev = nullptr;
   attn_status_t st = device_state(&dev);
   if (st != ATTN_OK) return st;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // One host thread at a time uses the per-device "taken" word.
+  static std::mutex take_mutex;
+  std::lock_guard<std::mutex> lock(take_mutex);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  // Read and clear in one atomic exchange on the device.
+  take_error_kernel<<<1, 1, 0, s>>>(dev->err, dev->taken);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   unsigned word = 0;
-  if (cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpyAsync(&word, dev->taken, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   if (word == 0) return ATTN_OK;
-  const unsigned zero = 0;
-  if (cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
   return (word & kErrWaitTimeout) ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_ERR_DEVICE_INDEX;
 }
 
@@ -844,10 +907,12 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
     return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
-  int wl, wr;
-  const float *slopes;
   attn_status_t st;
-  if ((st = read_options(opts, &wl, &wr, &slopes)) != ATTN_OK) return st;
+  Opts op;
+  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
+  const int wl = op.wl, wr = op.wr;
+  const float *slopes = op.slopes;
   const HostLayout L = host_layout(B, H_q, H_kv, N_q, N_kv, D);
   if (workspace == nullptr || workspace_bytes < L.total) return ATTN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return ATTN_ERR_ALIGNMENT;
@@ -864,6 +929,13 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
   const int64_t want = 2 * static_cast<int64_t>(dev->sm_count);
   const int64_t per_kvh = static_cast<int64_t>(group) * pairs;
   const int kvh = static_cast<int>(std::min<int64_t>(H_kv, std::max<int64_t>(1, (want + per_kvh - 1) / per_kvh)));
+  // The checks attn_fwd_prefill_ex applies to a chunk's shapes, made here for
+  // the largest chunk before anything is enqueued: the unit count of the
+  // persistent schedule and the tensor-map stride limit.
+  if (static_cast<int64_t>(kvh) * per_kvh + dev->sm_count > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<uint64_t>(kvh) * group * N_q * D * 2 >= (1ull << 40) ||
+      static_cast<uint64_t>(kvh) * N_kv * D * 2 >= (1ull << 40))
+    return ATTN_ERR_ALIGNMENT;
 
   char *ws = static_cast<char *>(workspace);
   char *dq = ws + L.off_q, *dk = ws + L.off_k, *dv = ws + L.off_v, *dout = ws + L.off_o;
@@ -909,8 +981,18 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
                                                      dtype, 1, nqh, nh, N_q, N_kv, D, sq, sk, sk, sq, causal, scale,
                                                      &oc, stream);
         if (cs != ATTN_OK) {
+          // Not expected after the checks above; the copies already enqueued on
+          // the library's streams are joined to the caller's stream first.
           cudaEventDestroy(ev_in);
           cudaEventDestroy(ev_done);
+          cudaEvent_t ev_j;
+          if (cudaEventCreateWithFlags(&ev_j, cudaEventDisableTiming) == cudaSuccess) {
+            cudaEventRecord(ev_j, s_in);
+            cudaStreamWaitEvent(s_comp, ev_j, 0);
+            cudaEventRecord(ev_j, s_out);
+            cudaStreamWaitEvent(s_comp, ev_j, 0);
+            cudaEventDestroy(ev_j);
+          }
           return cs;
         }
         fine = cudaEventRecord(ev_done, s_comp) == cudaSuccess && cudaStreamWaitEvent(s_out, ev_done, 0) == cudaSuccess &&
@@ -973,12 +1055,13 @@ attn_status_t attn_fwd_decode_noalloc(const void *q, const void *k_cache, const 
                                       attn_dtype_t dtype, int B, int H_q, int H_kv, int cache_len, int D,
                                       const int64_t q_str[4], const int64_t kc_str[4], const int64_t vc_str[4],
                                       const int64_t o_str[4], float scale, void *stream) {
-  // Sizes first: the scratch this call would need must fit the fixed array.
-  if (B < 1 || H_q < 1 || H_kv < 1 || cache_len < 1 || H_q % H_kv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
-  const DeviceState *dev = nullptr;
-  attn_status_t st = device_state(&dev);
+  // The same argument checks, in the same order, as attn_fwd_decode; then the
+  // scratch this call would need must fit the fixed array.
+  attn_status_t st = decode_check_args(q, k_cache, v_cache, o, lse, dtype, B, H_q, H_kv, cache_len, D, q_str, kc_str,
+                                       vc_str, o_str, scale);
   if (st != ATTN_OK) return st;
+  const DeviceState *dev = nullptr;
+  if ((st = device_state(&dev)) != ATTN_OK) return st;
   int nsplit = 1, chunk = cache_len;
   decode_plan(B, H_q, H_kv, cache_len, D, dev->sm_count, &nsplit, &chunk);
   if (decode_ws_bytes(B, H_q, D, nsplit) > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;

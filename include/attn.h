@@ -69,31 +69,58 @@ typedef enum {
 } attn_dtype_t;
 
 /*
- * Mask and bias variants ("Skill: Write a Triton Attention Kernel", Use this
- * when: windowed attention, ALiBi and custom masks; "Triton-FlashAttention"
- * lists sliding-window attention and ALiBi among deferred features).  Passed
- * to the *_ex entry points; a NULL pointer means none of them.
+ * Mask, bias and position variants ("Skill: Write a Triton Attention Kernel",
+ * Use this when: windowed attention, ALiBi, RoPE-fused and custom masks;
+ * "Triton-FlashAttention", Deferred / explicitly out of scope: fused rotary
+ * embeddings, sliding-window attention and attention biases such as ALiBi).
+ * Passed to the *_ex entry points; a NULL pointer means none of them.  A
+ * zero-initialised struct with window_left = window_right = -1 is the same as
+ * NULL.
  *
  *   window_left   -1, or W >= 0: query i attends only to keys j >= i - W
  *   window_right  -1, or W >= 0: query i attends only to keys j <= i + W
  *                 (prefill only; with causal = 1 the bound is j <= i anyway)
  *   alibi_slopes  NULL, or a device fp32 array of H_q slopes: the score of
  *                 (i, j) gets -slopes[h] * |i - j| added before the softmax
+ *   rope_theta    0, or the base theta > 0 of rotary position embeddings
+ *                 (RoPE): before the scores are formed, every query and key
+ *                 row at position p has each of its D/2 coordinate pairs
+ *                 (x_a, x_b) rotated by the angle p * theta^(-2c/D), c the
+ *                 pair's index:  x_a' = x_a cos - x_b sin,
+ *                 x_b' = x_b cos + x_a sin.  The kernels rotate Q and K tiles
+ *                 on chip; the caller's tensors are not modified.
+ *   rope_interleaved  which coordinates form pair c: 0 pairs (c, c + D/2)
+ *                 (the "rotate half" layout), 1 pairs (2c, 2c + 1)
+ *   num_splits    decode only: 0 lets the library choose how many parts the
+ *                 cache is split into; n in [1, 64] uses at most n (1: one
+ *                 pass, no workspace).  More splits than the automatic choice
+ *                 need a workspace of 4 * B * H_q * n * (D + 1) bytes.
  *
  * Positions are those of the causal mask (top-left, per sequence for the
  * variable-length call); for decode the query sits at position cache_len - 1
  * (per request for the paged call) and window_right is ignored.  A query row
  * left with no key gets O = 0 and LSE = -inf.
  *
- * Errors: a window below -1 gives ATTN_ERR_INVALID_ARG; slopes not 4-byte
- * aligned give ATTN_ERR_ALIGNMENT.  The struct is read during the call; the
- * slope array is read by the kernel, so it must stay valid until the work
- * enqueued on the stream has finished.  The caller owns both.
+ * RoPE and the KV cache: the decode calls rotate only the query, at its
+ * position; the cache must already hold rotated keys, which is what
+ * kv_cache_write_ex / kv_cache_write_paged_ex write when given the same
+ * rope_theta and rope_interleaved (each new key rotated at the position it is
+ * written to).  The values are never rotated.
+ *
+ * Errors: a window below -1, a rope_theta that is negative or not finite, a
+ * rope_interleaved other than 0 or 1, or a num_splits outside [0, 64] gives
+ * ATTN_ERR_INVALID_ARG; slopes not 4-byte aligned give ATTN_ERR_ALIGNMENT.
+ * The struct is read during the call; the slope array is read by the kernel,
+ * so it must stay valid until the work enqueued on the stream has finished.
+ * The caller owns both.
  */
 typedef struct {
     int32_t window_left;
     int32_t window_right;
     const float *alibi_slopes;
+    float rope_theta;
+    int32_t rope_interleaved;
+    int32_t num_splits;
 } attn_options_t;
 
 /*
@@ -175,6 +202,7 @@ attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const voi
 /*
  * attn_bwd_workspace_size -- bytes of scratch attn_bwd needs: one fp32 per
  * query row, 4 * B * H_q * N_q rounded up to 16.  Returns 0 on bad arguments.
+ * (A sizing utility of this library; the pages define no counterpart.)
  */
 size_t attn_bwd_workspace_size(int B, int H_q, int N_q);
 
@@ -215,7 +243,9 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
  * (b, q-head, split) and merges them.  The number of splits depends only on
  * B, H_q, H_kv and the current device's SM count (never on cache_len), so a
  * workspace sized once serves every cache length.  Returns 0 on bad
- * arguments.  Host-only; reads the current device's SM count.
+ * arguments.  Host-only; reads the current device's SM count.  (A sizing
+ * utility of this library; the pages define no counterpart.  The split itself
+ * is the decode design of attn_fwd_decode below.)
  */
 size_t attn_decode_workspace_size(int B, int H_q, int H_kv, int D);
 
@@ -223,7 +253,8 @@ size_t attn_decode_workspace_size(int B, int H_q, int H_kv, int D);
  * attn_decode_splits -- number of KV splits attn_fwd_decode uses for these
  * sizes on the current device (1 means one kernel and no workspace traffic;
  * more means a split kernel plus a merge kernel).  Returns 0 on bad
- * arguments.  Host-only.
+ * arguments.  Host-only.  (A query utility of this library; the pages define
+ * no counterpart.)
  */
 int attn_decode_splits(int B, int H_q, int H_kv, int cache_len, int D);
 
@@ -420,11 +451,15 @@ attn_status_t kv_cache_write_paged(void *k_pages, void *v_pages, const void *k_n
                                    const int64_t kn_str[4], const int64_t vn_str[4], void *stream);
 
 /*
- * attn_get_device_error -- synchronise `stream`, read the device error word of
- * the current device and clear it.  Returns ATTN_OK if no kernel reported a
- * failure, ATTN_ERR_DEVICE_TIMEOUT if one gave up on a wait,
- * ATTN_ERR_DEVICE_INDEX if a paged call met an out-of-range page id, length or
- * position, ATTN_ERR_CUDA if the synchronisation itself failed.
+ * attn_get_device_error -- synchronise `stream`, then read and clear the
+ * device error word of the current device in one atomic step (a one-thread
+ * kernel exchanges it with zero, so a failure recorded by a kernel still
+ * running on another stream is either returned now or kept for the next
+ * call, never lost).  Returns ATTN_OK if no kernel reported a failure,
+ * ATTN_ERR_DEVICE_TIMEOUT if one gave up on a wait, ATTN_ERR_DEVICE_INDEX if
+ * a paged or variable-length call met an out-of-range page id, length,
+ * position or offset, ATTN_ERR_CUDA if a CUDA call failed.  (Error reporting
+ * of this library; the pages define no counterpart.)
  */
 attn_status_t attn_get_device_error(void *stream);
 
@@ -441,10 +476,12 @@ attn_status_t attn_get_device_error(void *stream);
  */
 attn_status_t attn_selftest_wait_timeout(void *stream);
 
-/* attn_status_string -- static, human-readable name of a status code. */
+/* attn_status_string -- static, human-readable name of a status code.  (A
+ * utility of this library; the pages define no counterpart.) */
 const char *attn_status_string(attn_status_t status);
 
-/* attn_version -- library version as major * 10000 + minor * 100 + patch. */
+/* attn_version -- library version as major * 10000 + minor * 100 + patch.
+ * (A utility of this library; the pages define no counterpart.) */
 int attn_version(void);
 
 #ifdef __cplusplus

@@ -273,6 +273,12 @@ OPTION_CALLS = {
     ((-1, -5, None), A.ATTN_ERR_INVALID_ARG),
     ((-1, -1, P + 2), A.ATTN_ERR_ALIGNMENT),
     ((3, 4, P + 1), A.ATTN_ERR_ALIGNMENT),
+    ((-1, -1, None, -1.0, 0, 0), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, None, float("nan"), 0, 0), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, None, float("inf"), 0, 0), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, None, 10000.0, 2, 0), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, None, 0.0, 0, -1), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, None, 0.0, 0, 65), A.ATTN_ERR_INVALID_ARG),
 ])
 def test_option_errors(lib, call, opts, code):
     """Options are validated with the other arguments, before any CUDA call."""
@@ -327,3 +333,23 @@ def test_prefill_host_workspace_size():
     assert n == 2 * q + 2 * kv + lse  # every region a multiple of 256 bytes here
     assert A.attn_fwd_prefill_host_workspace_size(A.ATTN_BF16, 2, 8, 3, 64, 64, 128) == 0
     assert A.attn_fwd_prefill_host_workspace_size(A.ATTN_BF16, 2, 8, 2, 64, 64, 80) == 0
+
+
+def test_noalloc_decode_checks_arguments_before_the_scratch_size(lib):
+    """A call that is both malformed and too large for the fixed scratch array
+    reports the malformed argument, in the order attn_fwd_decode checks them;
+    nothing is launched (the pointers are never used)."""
+    B, Hq, Hkv, D, L = 64, 32, 8, 128, 8192
+    q_s, c_s = (Hq * D, D, D, 1), (Hkv * L * D, L * D, D, 1)
+    args = dict(q=P, k_cache=P, v_cache=P, o=P, lse=None, dtype=A.ATTN_BF16, B=B, H_q=Hq, H_kv=Hkv, cache_len=L,
+                D=D, q_str=q_s, kc_str=c_s, vc_str=c_s, o_str=q_s, scale=0.088, stream=None)
+    cases = [(dict(q=None), A.ATTN_ERR_INVALID_ARG), (dict(cache_len=0), A.ATTN_ERR_INVALID_ARG),
+             (dict(scale=0.0), A.ATTN_ERR_INVALID_ARG), (dict(D=96), A.ATTN_ERR_UNSUPPORTED),
+             (dict(k_cache=BAD), A.ATTN_ERR_ALIGNMENT), (dict(lse=P + 2), A.ATTN_ERR_ALIGNMENT),
+             (dict(kc_str=(Hkv * L * D, L * D, D, 2)), A.ATTN_ERR_ALIGNMENT),
+             (dict(o_str=(Hq * D, -D, D, 1)), A.ATTN_ERR_INVALID_ARG)]
+    for kw, code in cases:
+        a = {**args, **kw}
+        assert A.attn_fwd_decode_noalloc(**a) == code, kw
+        ws = {k: v for k, v in a.items()}
+        assert A.attn_fwd_decode(**ws, workspace=P, workspace_bytes=1 << 30) == code, kw
