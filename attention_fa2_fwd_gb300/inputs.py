@@ -7,7 +7,8 @@ Phase 3: fixed seed 42), in fp32, then cast to the workload's dtype, so the
 GPU path and the oracle see the same rounded values.
 
 Distributions follow the workloads' descriptions: i.i.d. N(0, 1) for Q, K, V;
-the cross-attention workload draws K with variance 2 (std sqrt(2)) and V from
+the cross-attention workload draws K with variance 2 (std sqrt(2)) -- and, as
+a second reading of its "N(0, 2)", with standard deviation 2 -- and V from
 U(-1, 1).
 """
 from __future__ import annotations
@@ -156,5 +157,9 @@ DECODE_LENS = (1, 33, 257, 1024, 4097, 8192)
 DECODE_B = (2, 64)
 
 # Workload 5: cross-attention, bf16, (B,N,H,D) memory layout, unequal lengths.
+# "K ~ N(0, 2)" is read as variance 2 (CROSS); the standard-deviation reading,
+# K = 2 * N(0, 1) (variance 4), is run as well (CROSS_STD2).
 CROSS = {D: Prefill(f"cross_b4_hq16_hkv4_nq1024_nkv4096_d{D}_bnhd_bf16", 4, 16, 4, 1024, 4096, D, False,
                     "bf16", "bnhd", ("normal", 1.0), ("normal", 2.0), ("uniform", 1.0)) for D in (64, 128)}
+CROSS_STD2 = {D: Prefill(f"cross_b4_hq16_hkv4_nq1024_nkv4096_d{D}_bnhd_bf16_kstd2", 4, 16, 4, 1024, 4096, D, False,
+                         "bf16", "bnhd", ("normal", 1.0), ("normal", 4.0), ("uniform", 1.0)) for D in (64, 128)}

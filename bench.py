@@ -216,7 +216,9 @@ def run_ours(args, rank, world, local_rank):
 
     range_push, range_pop = nvtx_ranges()
 
-    def step(evs=None):
+    R = args.passes_per_step
+
+    def one_pass(evs=None):
         flush.zero_()
         if evs:
             evs[0].record(stream)
@@ -234,6 +236,12 @@ def run_ours(args, rank, world, local_rank):
         if evs:
             evs[3].record(stream)
 
+    def step(evs=None):
+        # One step: R passes of the whole path over the same batch, the L2 cache
+        # flushed before every timed kernel group.
+        for r in range(R):
+            one_pass(evs[r] if evs else None)
+
     for _ in range(args.warmup):
         step()
     A.check_device_error()
@@ -243,7 +251,7 @@ def run_ours(args, rank, world, local_rank):
         time.sleep(0.3)
         for _ in range(max(args.warmup, 10)):  # keep the GPU busy while the sampler starts
             step()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(R)] for _ in range(args.steps)]
     r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -259,56 +267,57 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     A.check_device_error()
-    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    pre_ms = [e[0].elapsed_time(e[1]) for se in evs for e in se]
+    dec_ms = [e[2].elapsed_time(e[3]) for se in evs for e in se]
     region_ms = r0.elapsed_time(r1)
     sum_pre, sum_dec, region_ms = reduce_max([sum(pre_ms), sum(dec_ms), region_ms], world, dev)
 
     flops = prefill_flops(**P)
     kvb = decode_bytes(**Dc)
-    value = aggregate_throughput(flops, world, args.steps, sum_pre) / 1e12
-    decode_gbs = aggregate_throughput(kvb, world, args.steps, sum_dec) / 1e9
+    n_pass = args.steps * R
+    value = aggregate_throughput(flops, world, n_pass, sum_pre) / 1e12
+    decode_gbs = aggregate_throughput(kvb, world, n_pass, sum_dec) / 1e9
 
     # End to end through the public API with host buffers (pinned), copies inside the timed region:
     # attn_fwd_prefill_host pipelines the host-to-device copies, the compute and the copies back.
-    if True:
-        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        code = A.ATTN_BF16
-        ws_bytes = A.attn_fwd_prefill_host_workspace_size(code, P["B"], P["Hq"], P["Hkv"], P["N"], P["N"], P["D"])
-        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        scale = 1.0 / math.sqrt(P["D"])
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    code = A.ATTN_BF16
+    ws_bytes = A.attn_fwd_prefill_host_workspace_size(code, P["B"], P["Hq"], P["Hkv"], P["N"], P["N"], P["D"])
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(P["D"])
 
-        def host_call():
-            st = A.attn_fwd_prefill_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(), hl.data_ptr(),
-                                         code, P["B"], P["Hq"], P["Hkv"], P["N"], P["N"], P["D"], 1, scale, None,
-                                         ws.data_ptr(), ws_bytes, stream.cuda_stream)
-            if st != A.ATTN_OK:
-                raise RuntimeError(f"attn_fwd_prefill_host failed: {A.attn_status_string(st)}")
-        n_e2e = max(3, min(args.steps, 10))
-        for _ in range(2):
-            host_call()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            host_call()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = reduce_max([e0.elapsed_time(e1) / n_e2e], world, dev)[0]
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-        e2e = {"value": round(aggregate_throughput(flops, world, 1, e2e_ms) / 1e12, 2), "unit": "TFLOPS",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_call": round(e2e_ms, 4),
-               "path": "pinned host Q,K,V -> attn_fwd_prefill_host (copies pipelined with the compute) -> host O,LSE"}
+    def host_call():
+        st = A.attn_fwd_prefill_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(), hl.data_ptr(),
+                                     code, P["B"], P["Hq"], P["Hkv"], P["N"], P["N"], P["D"], 1, scale, None,
+                                     ws.data_ptr(), ws_bytes, stream.cuda_stream)
+        if st != A.ATTN_OK:
+            raise RuntimeError(f"attn_fwd_prefill_host failed: {A.attn_status_string(st)}")
+    n_e2e = max(3, min(args.steps, 10))
+    for _ in range(2):
+        host_call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        host_call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max([e0.elapsed_time(e1) / n_e2e], world, dev)[0]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    e2e = {"value": round(aggregate_throughput(flops, world, 1, e2e_ms) / 1e12, 2), "unit": "TFLOPS",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_call": round(e2e_ms, 4),
+           "path": "pinned host Q,K,V -> attn_fwd_prefill_host (copies pipelined with the compute) -> host O,LSE"}
 
     if rank != 0:
-        return None
+        return None, None
     peaks = load_peaks()
-    pre_avg = sum_pre / args.steps
-    dec_avg = sum_dec / args.steps
+    pre_avg = sum_pre / n_pass
+    dec_avg = sum_dec / n_pass
     ach = flops / (pre_avg * 1e-3) / 1e12
     ach_d = kvb / (dec_avg * 1e-3) / 1e9
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -325,6 +334,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round((sum_pre + sum_dec) / args.steps, 4),
+        "passes_per_step": R,
+        "ms_per_pass": round((sum_pre + sum_dec) / n_pass, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -332,6 +343,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) bf16, generated on device)",
         "config": {"workload": WORKLOAD, "prefill": P, "decode": Dc,
                    "l2": "flushed by a 256 MiB write before every timed kernel group (outside the event pairs)",
+                   "step": f"{R} passes of the whole path (prefill + decode step) over the same batch",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "decode_splits": splits},
         "prefill_ms": round(pre_avg, 4),
@@ -344,6 +356,9 @@ def run_ours(args, rank, world, local_rank):
         "decode": {"value": round(decode_gbs, 1), "unit": "GB/s", "ms_per_step": round(dec_avg, 4),
                    "kv_bytes_per_step": kvb, "kernels": "kv_cache_write + decode_split" + (" + decode_merge" if splits > 1 else "")},
         "region_ms_incl_flush": round(region_ms, 3),
+        # time x median SM clock under load (ms x MHz = thousands of SM cycles): comparable across clocks
+        "sm_kcycles": {"prefill": round(pre_avg * clk_mhz, 1), "decode_step": round(dec_avg * clk_mhz, 1),
+                       "per_step": round((sum_pre + sum_dec) / args.steps * clk_mhz, 1), "sm_mhz": clk_mhz},
         "roofline": {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": tr,
                      "peak_source": f"{peaks['source']} bf16 dense (burst)", "kernel": "prefill_fwd"},
@@ -351,10 +366,11 @@ def run_ours(args, rank, world, local_rank):
                             "frac": round(ach_d / peaks["hbm_gbs"], 4), "traffic": tr_d,
                             "peak_source": f"{peaks['source']} HBM copy", "kernel": "decode_split"},
         "e2e": e2e,
-        "gpu_launches": args.steps * (1 + 1 + (2 if splits > 1 else 1)),
+        "gpu_launches": n_pass * (1 + 1 + (2 if splits > 1 else 1)),
         "clocks": clocks,
     }
-    return line
+    data = {"prefill": (q, k, v, o, lse), "decode": (qd, kc, vc, od, lsed, Dc["L"])}
+    return line, data
 
 
 # --------------------------------------------------------------------------- oracle (CPU)
@@ -377,23 +393,65 @@ def oracle_sample(rows_per_step: int, seed: int):
     return q, k, v, sel, flops
 
 
-def time_oracle(target_s: float, seed=0):
-    """Time the oracle on growing samples until about target_s seconds; returns (TFLOPS, rows, secs, cores)."""
+def cpu_baseline_leg(target_s: float, data, seed=0):
+    """The CPU-baseline leg: the oracle, as it stands, timed on the host cores on
+    a bounded sample of the bench's own prefill workload -- growing batches of
+    query rows of single (b, h) heads of the very Q, K, V the GPU was timed on,
+    until about target_s seconds.  The oracle rows are then also compared with
+    the O and LSE the timed kernels wrote (and a few batch entries of the decode
+    step with its O and LSE), so the bench line says whether the outputs it
+    timed match the oracle.  Returns the cpu_baseline record."""
+    import numpy as np
+    import torch
+
     import oracle
     cores = oracle.default_threads()
-    rows = 64
-    total_f, total_t, total_rows = 0.0, 0.0, 0
+    P = PREFILL
+    q, k, v, o, lse = data["prefill"]
+    g = P["Hq"] // P["Hkv"]
+    scale = 1 / math.sqrt(P["D"])
+    rng = np.random.default_rng(seed)
+
+    def f64(t):
+        return t.detach().double().cpu().numpy()
+
+    rows, total_f, total_t, total_rows = 64, 0.0, 0.0, 0
+    o_err, l_err, o_sum, n_el, heads = 0.0, 0.0, 0.0, 0, 0
     while total_t < target_s:
-        q, k, v, sel, f = oracle_sample(rows, seed)
+        b, h = int(rng.integers(P["B"])), int(rng.integers(P["Hq"]))
+        qh, kh, vh = (f64(t[b:b + 1, x:x + 1]) for t, x in ((q, h), (k, h // g), (v, h // g)))
+        sel_i = rng.integers(0, P["N"], size=rows)
+        sel = np.stack([np.zeros_like(sel_i), np.zeros_like(sel_i), sel_i], axis=1)
         t0 = time.perf_counter()
-        oracle.attention_rows(q, k, v, True, 1 / math.sqrt(PREFILL["D"]), sel, nthreads=cores)
-        dt = time.perf_counter() - t0
-        total_f += f
-        total_t += dt
+        o_ref, l_ref = oracle.attention_rows(qh, kh, vh, True, scale, sel, nthreads=cores)
+        total_t += time.perf_counter() - t0
+        total_f += float(np.sum(4.0 * P["D"] * (sel_i + 1)))
         total_rows += rows
-        seed += 1
+        heads += 1
+        idx = torch.as_tensor(sel_i, dtype=torch.long, device=o.device)
+        og = f64(o[b, h].index_select(0, idx))
+        lg = f64(lse[b, h].index_select(0, idx))
+        e = np.abs(og - o_ref)
+        o_err = max(o_err, float(e.max()))
+        o_sum += float(e.sum())
+        n_el += e.size
+        l_err = max(l_err, float(np.abs(lg - l_ref).max()))
         rows = min(rows * 2, 1 << 16)
-    return total_f / total_t / 1e12, total_rows, total_t, cores
+    qd, kc, vc, od, lsed, L = data["decode"]
+    d_err, dl_err = 0.0, 0.0
+    for b in (0, qd.shape[0] - 1):
+        o_ref, l_ref = oracle.decode(f64(qd[b:b + 1]), f64(kc[b:b + 1]), f64(vc[b:b + 1]), L, scale, nthreads=cores)
+        d_err = max(d_err, float(np.abs(f64(od[b:b + 1]) - o_ref).max()))
+        dl_err = max(dl_err, float(np.abs(f64(lsed[b:b + 1]) - l_ref).max()))
+    ok = (o_err <= 2e-2 and o_sum / max(n_el, 1) <= 2e-3 and l_err <= 1e-3 and d_err <= 2e-2 and dl_err <= 1e-3)
+    return {"value": total_f / total_t / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": (f"{total_rows} random query rows of {heads} single (b, h) heads of the bench's own causal "
+                       f"prefill inputs (N=8192, D=128), {total_t:.1f} s on the host cores; FLOPs 4*D*(i+1) per "
+                       f"row i"),
+            "check": {"ok": ok, "prefill_rows": total_rows, "o_max_abs": o_err, "o_mean_abs": o_sum / max(n_el, 1),
+                      "lse_max_abs": l_err, "decode_batches": [0, int(qd.shape[0]) - 1],
+                      "decode_o_max_abs": d_err, "decode_lse_max_abs": dl_err,
+                      "bounds": "O max 2e-2, mean 2e-3; LSE max 1e-3 (fp64 oracle)"}}
 
 
 def run_reference(args, rank, world):
@@ -506,6 +564,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--passes-per-step", type=int, default=20,
+                    help="passes of the whole path per timed step (keeps the timed region long enough for the "
+                         "clock sampler: 20 steps x 20 passes is about 0.45 s)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--oracle-configs", action="store_true",
@@ -534,14 +595,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        line = run_ours(args, rank, world, local_rank)
+        line, data = run_ours(args, rank, world, local_rank)
         if line is not None:
             if world == 1:
-                tf, rows, secs, cores = time_oracle(args.cpu_baseline_seconds)
-                line["cpu_baseline"] = {
-                    "value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                    "sample": (f"{rows} random query rows of single (b, h) heads of the causal prefill workload "
-                               f"(N=8192, D=128), {secs:.1f} s on the host cores; FLOPs 4*D*(i+1) per row i")}
+                line["cpu_baseline"] = cpu_baseline_leg(args.cpu_baseline_seconds, data)
             print(json.dumps(line), flush=True)
     finally:
         if world > 1:

@@ -157,3 +157,73 @@ def test_decode_split_count_does_not_change_result():
     torch.cuda.synchronize()
     assert A.attn_decode_splits(2, Hq, Hkv, L, D) != A.attn_decode_splits(64, Hq, Hkv, L, D)
     assert_close(o64[:2], np64(o2), l64[:2], np64(l2), "splits")
+
+
+@pytest.mark.parametrize("B", [2, 64])
+def test_decode_one_split_equals_automatic_split(B):
+    """The same problem with the cache read in one pass (num_splits = 1), in the
+    automatic number of splits, and in a forced 3: all match the oracle and each other."""
+    import attention_fa2_fwd_gb300 as A
+    Hq, Hkv, D, L = 32, 8, 128, 8192
+    assert A.attn_decode_splits(B, Hq, Hkv, L, D) > 1
+    k, v = I.decode_stream(B, Hkv, L, D, "bf16", seed=90 + B)
+    q = I.decode_queries(B, Hq, D, [L - 1], "bf16", seed=90 + B)[:, :, 0]
+    qd, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o_auto, l_auto = A.decode(qd, kc, vc, L)
+    o_one, l_one = A.decode(qd, kc, vc, L, num_splits=1)
+    ws3 = torch.empty(4 * B * Hq * 3 * (D + 1) // 4, dtype=torch.float32, device="cuda")
+    o_three, l_three = A.decode(qd, kc, vc, L, num_splits=3, workspace=ws3)
+    torch.cuda.synchronize()
+    A.check_device_error()
+    bs = np.arange(B) if B <= 4 else np.array([0, 21, 63])
+    o_ref, lse_ref = oracle.decode(np64(q[bs]), np64(k[bs]), np64(v[bs]), L, 1 / np.sqrt(D))
+    for name, o, l in (("auto", o_auto, l_auto), ("one", o_one, l_one), ("three", o_three, l_three)):
+        assert_close(np64(o)[bs], o_ref, np64(l)[bs], lse_ref, f"B={B} {name}")
+    assert_close(o_one, np64(o_auto), l_one, np64(l_auto), f"B={B} one vs auto")
+
+
+def test_decode_forced_splits_need_their_workspace():
+    """A forced split count above the automatic one needs a larger workspace."""
+    import attention_fa2_fwd_gb300 as A
+    B, Hq, Hkv, D, L = 64, 32, 8, 128, 8192
+    auto = A.attn_decode_splits(B, Hq, Hkv, L, D)
+    q = torch.zeros((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((B, Hkv, L, D), dtype=torch.bfloat16, device="cuda")
+    ws = A.decode_workspace(B, Hq, Hkv, D)
+    with pytest.raises(A.AttnError) as e:
+        A.decode(q, kc, kc, L, workspace=ws, num_splits=auto + 4)
+    assert e.value.status == A.ATTN_ERR_WORKSPACE
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("B,L", [(2, 8192), (64, 4097), (3, 200)])
+def test_decode_guard_bands(B, L):
+    """Nothing is written outside O, LSE and the first attn_decode_workspace_size
+    bytes of the workspace: canary values around each of them stay untouched."""
+    import attention_fa2_fwd_gb300 as A
+    Hq, Hkv, D = 32, 8, 128
+    k, v = I.decode_stream(B, Hkv, L, D, "bf16", seed=5 + B)
+    q = I.decode_queries(B, Hq, D, [L - 1], "bf16", seed=5 + B)[:, :, 0].cuda()
+    kc, vc = k.cuda(), v.cuda()
+    pad = 1024
+    n_o = B * Hq * D
+    o_buf = torch.full((n_o + 2 * pad,), 3.0, dtype=torch.bfloat16, device="cuda")
+    o = o_buf[pad:pad + n_o].view(B, Hq, D)
+    # Interleaved guard: O as every other row of a (B, H_q, 2, D) buffer.
+    o2_buf = torch.full((B, Hq, 2, D), 5.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((B * Hq + 2 * pad,), 9.0, dtype=torch.float32, device="cuda")
+    lse = l_buf[pad:pad + B * Hq].view(B, Hq)
+    need = A.attn_decode_workspace_size(B, Hq, Hkv, D)
+    ws_buf = torch.full((need // 4 + 2 * pad,), -7.0, dtype=torch.float32, device="cuda")
+    ws = ws_buf[pad:pad + need // 4]
+    A.decode(q, kc, vc, L, out=o, lse_out=lse, workspace=ws if need else None)
+    A.decode(q, kc, vc, L, out=o2_buf[:, :, 0, :], return_lse=False, workspace=ws if need else None)
+    torch.cuda.synchronize()
+    A.check_device_error()
+    assert (o_buf[:pad] == 3.0).all() and (o_buf[pad + n_o:] == 3.0).all()
+    assert (o2_buf[:, :, 1, :] == 5.0).all()
+    assert (l_buf[:pad] == 9.0).all() and (l_buf[pad + B * Hq:] == 9.0).all()
+    assert (ws_buf[:pad] == -7.0).all() and (ws_buf[pad + need // 4:] == -7.0).all()
+    o_ref, lse_ref = oracle.decode(np64(q[:2]), np64(k[:2]), np64(v[:2]), L, 1 / np.sqrt(D))
+    assert_close(np64(o)[:2], o_ref, np64(lse)[:2], lse_ref, "guarded")
+    assert torch.equal(o2_buf[:, :, 0, :], o)

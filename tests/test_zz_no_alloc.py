@@ -3,11 +3,13 @@
 Some callers cannot call cudaMalloc or pass the library a workspace -- a
 plugin whose host framework owns all device memory, or a serving loop that
 must not risk an allocation's device synchronisation or failure mid-request.
-For them the library keeps a 4 MiB scratch array of its own.  This test calls
-that entry point through the C ABI and checks its output against the
-workspace-taking attn_fwd_decode on the same inputs, for two calls in a row
-(the second call finds the first call's partials still in the shared scratch
-array and must not be affected by them).
+For them the library keeps a 4 MiB scratch array of its own.  These tests call
+that entry point through the C ABI and check its output against the fp64
+oracle and against the workspace-taking attn_fwd_decode on the same inputs,
+for two calls in a row (the second call finds the first call's partials still
+in the shared scratch array and must not be affected by them): bf16 with
+D = 128 and many splits, fp16 with D = 64, and short caches that need one
+split and no scratch at all.
 
 The file is named so that pytest collects it last.
 """
@@ -19,6 +21,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from attention_fa2_fwd_gb300 import inputs as I
 from tests.helpers import assert_close, np64
 
@@ -40,27 +43,43 @@ def _call_noalloc(A, q, kc, vc, cache_len):
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     q4, o4 = q.unsqueeze(2), o.unsqueeze(2)
+    code = A.ATTN_BF16 if q.dtype == torch.bfloat16 else A.ATTN_F16
     st = A.attn_fwd_decode_noalloc(q4.data_ptr(), kc.data_ptr(), vc.data_ptr(), o4.data_ptr(), lse.data_ptr(),
-                                   A.ATTN_BF16, B, Hq, Hkv, cache_len, D, q4.stride(), kc.stride(), vc.stride(),
+                                   code, B, Hq, Hkv, cache_len, D, q4.stride(), kc.stride(), vc.stride(),
                                    o4.stride(), 1.0 / math.sqrt(D), torch.cuda.current_stream().cuda_stream)
     assert st == A.ATTN_OK, A.attn_status_string(st)
     return o, lse
 
 
-def test_noalloc_decode_matches_workspace_decode_twice(A):
-    Hq, Hkv, D, L = 32, 8, 128, 4097
-    # B=2 splits the cache many ways, so the scratch array is really used.
-    assert A.attn_decode_splits(2, Hq, Hkv, L, D) > 1
-    k, v = I.decode_stream(2, Hkv, L, D, "bf16", seed=21)
+# (dtype, D, B, H_q, H_kv, cache lengths of the two calls, whether the split scratch is used)
+CASES = [
+    ("bf16", 128, 2, 32, 8, (4097, 2001), True),   # many splits: the scratch array holds the partials
+    ("f16", 64, 3, 16, 4, (3000, 777), True),      # fp16, D = 64
+    ("bf16", 128, 4, 32, 8, (200, 130), False),    # short caches: one split, the scratch is not touched
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}_d{c[1]}_b{c[2]}_{'split' if c[6] else 'onepass'}"
+                                             for c in CASES])
+def test_noalloc_decode_matches_workspace_decode_twice(A, case):
+    """Two calls in a row, each checked against the fp64 oracle and against the
+    workspace-taking attn_fwd_decode on the same inputs."""
+    dt, D, B, Hq, Hkv, lens, split = case
+    L = max(lens)
+    for cl in lens:
+        assert (A.attn_decode_splits(B, Hq, Hkv, cl, D) > 1) == split
+    k, v = I.decode_stream(B, Hkv, L, D, dt, seed=21 + D)
     kc, vc = k.cuda(), v.cuda()
-    queries = I.decode_queries(2, Hq, D, [L - 1, 2000], "bf16", seed=21).cuda()
-    for j, cache_len in enumerate((L, 2001)):
-        q = queries[:, :, j].contiguous()
-        o_ref, lse_ref = A.decode(q, kc, vc, cache_len)
+    queries = I.decode_queries(B, Hq, D, [cl - 1 for cl in lens], dt, seed=21 + D)
+    for j, cache_len in enumerate(lens):
+        q = queries[:, :, j].contiguous().cuda()
+        o_ws, lse_ws = A.decode(q, kc, vc, cache_len)
         o, lse = _call_noalloc(A, q, kc, vc, cache_len)
         torch.cuda.synchronize()
         A.check_device_error()
-        assert_close(o, np64(o_ref), lse, np64(lse_ref), f"call {j + 1}")
+        o_ref, lse_ref = oracle.decode(np64(queries[:, :, j]), np64(k), np64(v), cache_len, 1 / math.sqrt(D))
+        assert_close(o, o_ref, lse, lse_ref, f"call {j + 1} vs oracle")
+        assert_close(o, np64(o_ws), lse, np64(lse_ws), f"call {j + 1} vs attn_fwd_decode")
 
 
 def test_noalloc_decode_rejects_scratch_beyond_limit(A):
