@@ -37,7 +37,8 @@ ATTN_BF16 = 1
 EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_ex", "attn_fwd_prefill_host", "attn_fwd_prefill_host_workspace_size",
            "attn_fwd_prefill_varlen", "attn_fwd_prefill_varlen_ex",
            "attn_fwd_decode_ex", "attn_fwd_decode_paged_ex", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
-           "attn_fwd_decode_noalloc", "kv_cache_write", "attn_fwd_decode_paged", "kv_cache_write_paged",
+           "attn_fwd_decode_noalloc", "kv_cache_write", "kv_cache_write_ex", "attn_fwd_decode_paged",
+           "kv_cache_write_paged", "kv_cache_write_paged_ex",
            "attn_bwd_workspace_size", "attn_bwd",
            "attn_get_device_error", "attn_selftest_wait_timeout", "attn_status_string", "attn_version")
 
@@ -115,6 +116,9 @@ def lib() -> ctypes.CDLL:
             L.kv_cache_write.restype = i32
             L.kv_cache_write.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                          i64p, i64p, i64p, i64p, vp]
+            L.kv_cache_write_ex.restype = i32
+            L.kv_cache_write_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                            i64p, i64p, i64p, i64p, optp, vp]
             i64 = ctypes.c_int64
             L.attn_fwd_decode_paged.restype = i32
             L.attn_fwd_decode_paged.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
@@ -123,6 +127,9 @@ def lib() -> ctypes.CDLL:
             L.kv_cache_write_paged.restype = i32
             L.kv_cache_write_paged.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, i64,
                                                vp, i64p, i64p, i64p, i64p, vp]
+            L.kv_cache_write_paged_ex.restype = i32
+            L.kv_cache_write_paged_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, i32, i64,
+                                                  vp, i64p, i64p, i64p, i64p, optp, vp]
             L.attn_bwd_workspace_size.restype = ctypes.c_size_t
             L.attn_bwd_workspace_size.argtypes = [i32, i32, i32]
             L.attn_bwd.restype = i32
@@ -261,6 +268,21 @@ def kv_cache_write(k_cache, v_cache, k_new, v_new, dtype, B, H_kv, n_new, D, pos
                                 _strides(kc_str), _strides(vc_str), _strides(kn_str), _strides(vn_str), stream)
 
 
+def kv_cache_write_ex(k_cache, v_cache, k_new, v_new, dtype, B, H_kv, n_new, D, pos, max_len, kc_str, vc_str, kn_str,
+                      vn_str, opts, stream) -> int:
+    return lib().kv_cache_write_ex(k_cache, v_cache, k_new, v_new, dtype, B, H_kv, n_new, D, pos, max_len,
+                                   _strides(kc_str), _strides(vc_str), _strides(kn_str), _strides(vn_str), _opts(opts),
+                                   stream)
+
+
+def kv_cache_write_paged_ex(k_pages, v_pages, k_new, v_new, dtype, B, H_kv, n_new, D, num_pages, page_size,
+                            block_table, max_pages, bt_stride, positions, kp_str, vp_str, kn_str, vn_str, opts,
+                            stream) -> int:
+    return lib().kv_cache_write_paged_ex(k_pages, v_pages, k_new, v_new, dtype, B, H_kv, n_new, D, num_pages,
+                                         page_size, block_table, max_pages, bt_stride, positions, _strides(kp_str),
+                                         _strides(vp_str), _strides(kn_str), _strides(vn_str), _opts(opts), stream)
+
+
 def attn_fwd_decode_paged(q, k_pages, v_pages, o, lse, dtype, B, H_q, H_kv, D, num_pages, page_size, block_table,
                           max_pages, bt_stride, cache_lens, max_cache_len, q_str, kp_str, vp_str, o_str, scale,
                           workspace, workspace_bytes, stream) -> int:
@@ -330,7 +352,8 @@ def _check(status: int, where: str):
 
 
 def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_lse: bool = True, out=None,
-            lse_out=None, stream=None, window=(-1, -1), alibi_slopes=None):
+            lse_out=None, stream=None, window=(-1, -1), alibi_slopes=None, rope_theta: float = 0.0,
+            rope_interleaved: bool = False):
     """Fused attention forward.  q (B,H_q,N_q,D); k, v (B,H_kv,N_kv,D) CUDA tensors.
 
     Any (b, h, n) strides are accepted (16-byte multiples, d stride 1), so a
@@ -350,13 +373,15 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_ls
     st = attn_fwd_prefill_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                              lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D,
                              q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
-                             make_options(window[0], window[1], alibi_slopes), _stream_handle(stream))
+                             make_options(window[0], window[1], alibi_slopes, rope_theta, rope_interleaved),
+                             _stream_handle(stream))
     _check(st, "attn_fwd_prefill")
     return o, lse
 
 
 def prefill_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse_out=None,
-                 workspace=None, stream=None, window=(-1, -1), alibi_slopes=None):
+                 workspace=None, stream=None, window=(-1, -1), alibi_slopes=None, rope_theta: float = 0.0,
+                 rope_interleaved: bool = False):
     """Prefill on host tensors (contiguous, ideally pinned) with copies pipelined against the compute.
 
     q (B,H_q,N_q,D), k, v (B,H_kv,N_kv,D) CPU tensors; returns host (O, LSE).  The results are complete
@@ -377,7 +402,8 @@ def prefill_host(q, k, v, causal: bool = False, scale: float | None = None, out=
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
     st = attn_fwd_prefill_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), code, B, Hq,
-                               Hkv, Nq, Nkv, D, causal, scale, make_options(window[0], window[1], alibi_slopes),
+                               Hkv, Nq, Nkv, D, causal, scale,
+                               make_options(window[0], window[1], alibi_slopes, rope_theta, rope_interleaved),
                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                _stream_handle(stream))
     _check(st, "attn_fwd_prefill_host")
@@ -387,7 +413,8 @@ def prefill_host(q, k, v, causal: bool = False, scale: float | None = None, out=
 
 def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                    causal: bool = False, scale: float | None = None, return_lse: bool = True, out=None,
-                   lse_out=None, stream=None, window=(-1, -1), alibi_slopes=None):
+                   lse_out=None, stream=None, window=(-1, -1), alibi_slopes=None, rope_theta: float = 0.0,
+                   rope_interleaved: bool = False):
     """Attention over packed sequences of different lengths.
 
     q (total_q, H_q, D); k, v (total_k, H_kv, D); cu_seqlens_q / cu_seqlens_k int32 CUDA tensors (B + 1).
@@ -409,7 +436,8 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_s
                                     lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, D,
                                     cq.data_ptr(), ck.data_ptr(), int(max_seqlen_q), int(max_seqlen_k), total_q,
                                     total_k, q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
-                                    make_options(window[0], window[1], alibi_slopes), _stream_handle(stream))
+                                    make_options(window[0], window[1], alibi_slopes, rope_theta, rope_interleaved),
+                                    _stream_handle(stream))
     _check(st, "attn_fwd_prefill_varlen")
     return o, lse
 
@@ -450,7 +478,7 @@ def decode_workspace(B, H_q, H_kv, D, device=None):
 
 def decode(q, k_cache, v_cache, cache_len: int, scale: float | None = None, return_lse: bool = True, out=None,
            lse_out=None, workspace=None, stream=None, window_left: int = -1, alibi_slopes=None,
-           num_splits: int = 0):
+           num_splits: int = 0, rope_theta: float = 0.0, rope_interleaved: bool = False):
     """One query token per (batch, q-head) over the first cache_len cache rows.
 
     q (B,H_q,D) or (B,H_q,1,D); caches (B,H_kv,max_len,D).  Returns (O (B,H_q,D), LSE (B,H_q)).
@@ -475,19 +503,23 @@ def decode(q, k_cache, v_cache, cache_len: int, scale: float | None = None, retu
     st = attn_fwd_decode_ex(q4.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), o4.data_ptr(),
                             lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, int(cache_len), D,
                             q4.stride(), k_cache.stride(), v_cache.stride(), o4.stride(), scale, ws_ptr, ws_bytes,
-                            make_options(window_left, -1, alibi_slopes, num_splits=num_splits),
+                            make_options(window_left, -1, alibi_slopes, rope_theta, rope_interleaved, num_splits),
                             _stream_handle(stream))
     _check(st, "attn_fwd_decode")
     return o, lse
 
 
-def write_kv_cache(k_cache, v_cache, k_new, v_new, pos: int, stream=None):
-    """Copy k_new/v_new (B,H_kv,n,D) into cache rows [pos, pos+n) in place."""
+def write_kv_cache(k_cache, v_cache, k_new, v_new, pos: int, stream=None, rope_theta: float = 0.0,
+                   rope_interleaved: bool = False):
+    """Copy k_new/v_new (B,H_kv,n,D) into cache rows [pos, pos+n) in place (keys rotated at their
+    positions when rope_theta > 0)."""
     B, Hkv, max_len, D = k_cache.shape
     n = k_new.shape[2]
-    st = kv_cache_write(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
-                        _dtype_code(k_cache), B, Hkv, n, D, int(pos), max_len, k_cache.stride(), v_cache.stride(),
-                        k_new.stride(), v_new.stride(), _stream_handle(stream))
+    st = kv_cache_write_ex(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                           _dtype_code(k_cache), B, Hkv, n, D, int(pos), max_len, k_cache.stride(), v_cache.stride(),
+                           k_new.stride(), v_new.stride(), make_options(rope_theta=rope_theta,
+                                                                        rope_interleaved=rope_interleaved),
+                           _stream_handle(stream))
     _check(st, "kv_cache_write")
 
 
@@ -500,7 +532,8 @@ def _int32_cuda(t, name):
 
 def decode_paged(q, k_pages, v_pages, block_table, cache_lens, max_cache_len: int, scale: float | None = None,
                  return_lse: bool = True, out=None, lse_out=None, workspace=None, stream=None,
-                 window_left: int = -1, alibi_slopes=None):
+                 window_left: int = -1, alibi_slopes=None, rope_theta: float = 0.0, rope_interleaved: bool = False,
+                 num_splits: int = 0):
     """Decode over paged caches with per-request lengths.
 
     q (B,H_q,D); k_pages, v_pages (num_pages,H_kv,page_size,D); block_table int32 (B,max_pages) and
@@ -528,22 +561,26 @@ def decode_paged(q, k_pages, v_pages, block_table, cache_lens, max_cache_len: in
                                   lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, D,
                                   num_pages, page_size, bt.data_ptr(), bt.shape[1], bt.stride(0), cl.data_ptr(),
                                   int(max_cache_len), q4.stride(), k_pages.stride(), v_pages.stride(), o4.stride(),
-                                  scale, ws_ptr, ws_bytes, make_options(window_left, -1, alibi_slopes),
+                                  scale, ws_ptr, ws_bytes,
+                                  make_options(window_left, -1, alibi_slopes, rope_theta, rope_interleaved, num_splits),
                                   _stream_handle(stream))
     _check(st, "attn_fwd_decode_paged")
     return o, lse
 
 
-def write_kv_cache_paged(k_pages, v_pages, k_new, v_new, block_table, positions, stream=None):
-    """Write k_new/v_new (B,H_kv,n,D) at positions[b] + t of each request's paged cache (in place)."""
+def write_kv_cache_paged(k_pages, v_pages, k_new, v_new, block_table, positions, stream=None,
+                         rope_theta: float = 0.0, rope_interleaved: bool = False):
+    """Write k_new/v_new (B,H_kv,n,D) at positions[b] + t of each request's paged cache (in place; keys
+    rotated at their positions when rope_theta > 0)."""
     num_pages, Hkv, page_size, D = k_pages.shape
     B, _, n, _ = k_new.shape
     bt = _int32_cuda(block_table, "block_table")
     pos = _int32_cuda(positions, "positions")
-    st = kv_cache_write_paged(k_pages.data_ptr(), v_pages.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
-                              _dtype_code(k_pages), B, Hkv, n, D, num_pages, page_size, bt.data_ptr(), bt.shape[1],
-                              bt.stride(0), pos.data_ptr(), k_pages.stride(), v_pages.stride(), k_new.stride(),
-                              v_new.stride(), _stream_handle(stream))
+    st = kv_cache_write_paged_ex(k_pages.data_ptr(), v_pages.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                 _dtype_code(k_pages), B, Hkv, n, D, num_pages, page_size, bt.data_ptr(), bt.shape[1],
+                                 bt.stride(0), pos.data_ptr(), k_pages.stride(), v_pages.stride(), k_new.stride(),
+                                 v_new.stride(), make_options(rope_theta=rope_theta, rope_interleaved=rope_interleaved),
+                                 _stream_handle(stream))
     _check(st, "kv_cache_write_paged")
 
 

@@ -220,6 +220,22 @@ attn_status_t read_opts(const attn_options_t *opts, Opts *o) {
   return ATTN_OK;
 }
 
+// Turn steps of rotary embeddings as 64-bit fractions of a full turn:
+// f_c = frac(theta^(-2c/D) / (2 pi)) * 2^64.  Computed in double precision,
+// whose error (about 1e-16 of a turn per unit position) stays far below fp32
+// resolution for any position an int can hold.
+void fill_rope_steps(float theta, int D, uint64_t *f) {
+  constexpr double kTwoPi = 6.283185307179586476925286766559;
+  for (int c = 0; c < D / 2; ++c) {
+    const double inv = std::pow(static_cast<double>(theta), -2.0 * c / D);
+    double t = inv / kTwoPi;
+    t -= std::floor(t);  // in [0, 1)
+    const double scaled = std::ldexp(t, 64);
+    f[c] = scaled >= 18446744073709551615.0 ? ~uint64_t(0) : static_cast<uint64_t>(scaled);
+  }
+  for (int c = D / 2; c < 64; ++c) f[c] = 0;
+}
+
 // Failure-detection self-test: one thread waits on an mbarrier that nothing
 // ever arrives on.  The bounded wait gives up after its wall-clock limit,
 // records kErrWaitTimeout in the device error word and returns.
@@ -321,10 +337,14 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
   PrefillParams p{};
   Opts op;
   if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
-  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
   p.window_left = op.wl;
   p.window_right = op.wr;
   p.alibi_slopes = op.slopes;
+  const bool rope = op.rope_theta > 0.f;
+  if (rope) {
+    p.rope_inter = op.rope_interleaved;
+    fill_rope_steps(op.rope_theta, D, p.rope_f);
+  }
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
   const bool bf16 = dtype == ATTN_BF16;
@@ -346,7 +366,7 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
   p.n_qtiles = (N_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
   if ((st = prefill_schedule(&p, B, H_q, dev->sm_count)) != ATTN_OK) return st;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  cudaError_t e = launch_prefill(D, causal != 0, bf16, false, prefill_masked(p, causal != 0), tq, tk, tv, p, B,
+  cudaError_t e = launch_prefill(D, causal != 0, bf16, false, prefill_masked(p, causal != 0), rope, tq, tk, tv, p, B,
                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -391,10 +411,14 @@ attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const voi
   PrefillParams p{};
   Opts op;
   if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
-  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
   p.window_left = op.wl;
   p.window_right = op.wr;
   p.alibi_slopes = op.slopes;
+  const bool rope = op.rope_theta > 0.f;
+  if (rope) {
+    p.rope_inter = op.rope_interleaved;
+    fill_rope_steps(op.rope_theta, D, p.rope_f);
+  }
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
   const bool bf16 = dtype == ATTN_BF16;
@@ -420,7 +444,7 @@ attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const voi
   p.cu_k = cu_seqlens_k;
   p.total_q = total_q;
   p.total_k = total_k;
-  cudaError_t e = launch_prefill(D, causal != 0, bf16, true, prefill_masked(p, causal != 0), tq, tk, tv, p, B,
+  cudaError_t e = launch_prefill(D, causal != 0, bf16, true, prefill_masked(p, causal != 0), rope, tq, tk, tv, p, B,
                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -535,7 +559,6 @@ attn_status_t attn_fwd_decode_ex(const void *q, const void *k_cache, const void 
   const int64_t csz[4] = {B, H_kv, cache_len, D};
   Opts op;
   if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
-  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
   const int wl = op.wl;
   const float *slopes = op.slopes;
   const DeviceState *dev = nullptr;
@@ -579,6 +602,10 @@ attn_status_t attn_fwd_decode_ex(const void *q, const void *k_cache, const void 
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.window_left = wl;
   p.alibi_slopes = slopes;
+  if (op.rope_theta > 0.f) {
+    p.rope = op.rope_interleaved ? 2 : 1;
+    fill_rope_steps(op.rope_theta, D, p.rope_f);
+  }
   if (static_cast<int64_t>(H_kv) * nhc > 65535) return ATTN_ERR_INVALID_ARG;
   // Tensor maps over the valid rows only: rows >= cache_len read as zeros.
   CUtensorMap tk, tv;
@@ -594,6 +621,14 @@ attn_status_t kv_cache_write(void *k_cache, void *v_cache, const void *k_new, co
                              int B, int H_kv, int n_new, int D, int pos, int max_len, const int64_t kc_str[4],
                              const int64_t vc_str[4], const int64_t kn_str[4], const int64_t vn_str[4],
                              void *stream) {
+  return kv_cache_write_ex(k_cache, v_cache, k_new, v_new, dtype, B, H_kv, n_new, D, pos, max_len, kc_str, vc_str,
+                           kn_str, vn_str, nullptr, stream);
+}
+
+attn_status_t kv_cache_write_ex(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                                attn_dtype_t dtype, int B, int H_kv, int n_new, int D, int pos, int max_len,
+                                const int64_t kc_str[4], const int64_t vc_str[4], const int64_t kn_str[4],
+                                const int64_t vn_str[4], const attn_options_t *opts, void *stream) {
   if (!k_cache || !v_cache || !k_new || !v_new || !kc_str || !vc_str || !kn_str || !vn_str)
     return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H_kv < 1 || n_new < 1 || D < 1 || max_len < 1 || pos < 0) return ATTN_ERR_INVALID_ARG;
@@ -605,6 +640,8 @@ attn_status_t kv_cache_write(void *k_cache, void *v_cache, const void *k_new, co
   if ((st = check_strides(kc_str, csz)) || (st = check_strides(vc_str, csz)) || (st = check_strides(kn_str, nsz)) ||
       (st = check_strides(vn_str, nsz)))
     return st;
+  Opts op;
+  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
   KvWriteParams p{};
@@ -630,6 +667,11 @@ attn_status_t kv_cache_write(void *k_cache, void *v_cache, const void *k_new, co
   p.D = D;
   p.total_units = static_cast<int64_t>(B) * H_kv * n_new * (D / 8);
   p.err = dev->err;
+  p.is_bf16 = dtype == ATTN_BF16;
+  if (op.rope_theta > 0.f) {
+    p.rope = op.rope_interleaved ? 2 : 1;
+    fill_rope_steps(op.rope_theta, D, p.rope_f);
+  }
   cudaError_t e = launch_kv_cache_write(p, false, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -679,7 +721,6 @@ attn_status_t attn_fwd_decode_paged_ex(const void *q, const void *k_pages, const
     return st;
   Opts op;
   if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
-  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
   const int wl = op.wl;
   const float *slopes = op.slopes;
   const DeviceState *dev = nullptr;
@@ -724,6 +765,10 @@ attn_status_t attn_fwd_decode_paged_ex(const void *q, const void *k_pages, const
   p.num_pages = num_pages;
   p.window_left = wl;
   p.alibi_slopes = slopes;
+  if (op.rope_theta > 0.f) {
+    p.rope = op.rope_interleaved ? 2 : 1;
+    fill_rope_steps(op.rope_theta, D, p.rope_f);
+  }
   // Tensor maps over the page pool: (d, row in page, kv head, page).
   CUtensorMap tk, tv;
   const bool bf16 = dtype == ATTN_BF16;
@@ -740,6 +785,17 @@ attn_status_t kv_cache_write_paged(void *k_pages, void *v_pages, const void *k_n
                                    int page_size, const int32_t *block_table, int max_pages, int64_t bt_stride,
                                    const int32_t *positions, const int64_t kp_str[4], const int64_t vp_str[4],
                                    const int64_t kn_str[4], const int64_t vn_str[4], void *stream) {
+  return kv_cache_write_paged_ex(k_pages, v_pages, k_new, v_new, dtype, B, H_kv, n_new, D, num_pages, page_size,
+                                 block_table, max_pages, bt_stride, positions, kp_str, vp_str, kn_str, vn_str,
+                                 nullptr, stream);
+}
+
+attn_status_t kv_cache_write_paged_ex(void *k_pages, void *v_pages, const void *k_new, const void *v_new,
+                                      attn_dtype_t dtype, int B, int H_kv, int n_new, int D, int num_pages,
+                                      int page_size, const int32_t *block_table, int max_pages, int64_t bt_stride,
+                                      const int32_t *positions, const int64_t kp_str[4], const int64_t vp_str[4],
+                                      const int64_t kn_str[4], const int64_t vn_str[4], const attn_options_t *opts,
+                                      void *stream) {
   if (!k_pages || !v_pages || !k_new || !v_new || !positions || !kp_str || !vp_str || !kn_str || !vn_str)
     return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H_kv < 1 || n_new < 1 || D < 1) return ATTN_ERR_INVALID_ARG;
@@ -753,6 +809,8 @@ attn_status_t kv_cache_write_paged(void *k_pages, void *v_pages, const void *k_n
   if ((st = check_strides(kp_str, psz)) || (st = check_strides(vp_str, psz)) || (st = check_strides(kn_str, nsz)) ||
       (st = check_strides(vn_str, nsz)))
     return st;
+  Opts op;
+  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
   KvWriteParams p{};
@@ -783,6 +841,11 @@ attn_status_t kv_cache_write_paged(void *k_pages, void *v_pages, const void *k_n
   p.page_size = page_size;
   p.max_pages = max_pages;
   p.num_pages = num_pages;
+  p.is_bf16 = dtype == ATTN_BF16;
+  if (op.rope_theta > 0.f) {
+    p.rope = op.rope_interleaved ? 2 : 1;
+    fill_rope_steps(op.rope_theta, D, p.rope_f);
+  }
   cudaError_t e = launch_kv_cache_write(p, true, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -829,7 +892,7 @@ const char *attn_status_string(attn_status_t status) {
   return "ATTN_ERR_UNKNOWN";
 }
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 200; }
 
 }  // extern "C"
 
@@ -910,7 +973,6 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
   attn_status_t st;
   Opts op;
   if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
-  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;
   const int wl = op.wl, wr = op.wr;
   const float *slopes = op.slopes;
   const HostLayout L = host_layout(B, H_q, H_kv, N_q, N_kv, D);
@@ -974,7 +1036,7 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
         // The chunk is a contiguous (1, nqh, N_q, D) / (1, nh, N_kv, D) problem.
         const int64_t sq[4] = {static_cast<int64_t>(nqh) * N_q * D, static_cast<int64_t>(N_q) * D, D, 1};
         const int64_t sk[4] = {static_cast<int64_t>(nh) * N_kv * D, static_cast<int64_t>(N_kv) * D, D, 1};
-        attn_options_t oc{wl, wr, slopes ? slopes + qh0 : nullptr};
+        attn_options_t oc{wl, wr, slopes ? slopes + qh0 : nullptr, op.rope_theta, op.rope_interleaved, 0};
         const attn_status_t cs = attn_fwd_prefill_ex(dq + qo, dk + ko, dv + ko, dout + qo,
                                                      lse ? reinterpret_cast<float *>(reinterpret_cast<char *>(dl) + lo)
                                                          : nullptr,

@@ -42,6 +42,11 @@ struct PrefillParams {
   // alibi_slopes (device fp32, one per q head) adds -slope_h |i - j| to scores.
   int window_left, window_right;
   const float *alibi_slopes;
+  // Rotary embeddings (ROPE builds): pair c of a row at position p turns by
+  // (p * rope_f[c] mod 2^64) / 2^64 of a full turn; rope_inter selects the
+  // pairs (2c, 2c + 1) instead of (c, c + D/2).
+  int rope_inter;
+  uint64_t rope_f[64];
 };
 
 struct DecodeParams {
@@ -66,6 +71,10 @@ struct DecodeParams {
   // (window_left < 0: all); alibi_slopes adds -slope_h (len - 1 - j).
   int window_left;
   const float *alibi_slopes;
+  // Rotary embeddings: the query is rotated at its position (cache length - 1);
+  // the cache holds rotated keys.  rope: 0 none, 1 rotate-half, 2 interleaved.
+  int rope;
+  uint64_t rope_f[64];
 };
 
 struct KvWriteParams {
@@ -82,17 +91,29 @@ struct KvWriteParams {
   const int32_t *positions;
   int64_t bt_stride;
   int page_size, max_pages, num_pages;
+  // Rotary embeddings: each new key is rotated at the cache position it is
+  // written to.  rope: 0 none, 1 rotate-half, 2 interleaved.
+  int rope;
+  bool is_bf16;
+  uint64_t rope_f[64];
 };
 
 // Launchers (return cudaSuccess or the launch error).
 // masked: a window bound or ALiBi slopes are set (a separate kernel build, so
 // that the plain kernel keeps its short softmax loop).
-cudaError_t launch_prefill(int D, bool causal, bool bf16, bool varlen, bool masked, const CUtensorMap &tq,
+// rope: rotary embeddings on the Q and K tiles (two more builds).
+cudaError_t launch_prefill(int D, bool causal, bool bf16, bool varlen, bool masked, bool rope, const CUtensorMap &tq,
                            const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
                            cudaStream_t stream);
 cudaError_t launch_prefill_masked(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq,
                                   const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
                                   cudaStream_t stream);
+cudaError_t launch_prefill_rope(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq,
+                                const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
+                                cudaStream_t stream);
+cudaError_t launch_prefill_rope_masked(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq,
+                                       const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
+                                       cudaStream_t stream);
 
 // Decode: heads served by one CTA, and launch (split kernel, plus the merge
 // kernel when nsplit > 1).

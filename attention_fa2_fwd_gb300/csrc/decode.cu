@@ -33,6 +33,7 @@
 
 #include "attn_internal.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace attn {
 namespace {
@@ -126,7 +127,7 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap *map, i
 template <int D, int GH, bool BF16, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                        const DecodeParams p) {
+                        const __grid_constant__ DecodeParams p) {
   using C = DecCfg<D, GH>;
   extern __shared__ uint8_t smem_raw[];
   griddep_wait();  // before any global memory access (launched with programmatic serialization)
@@ -176,17 +177,29 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_proxy_async_smem();
   }
   // Query rows of this CTA's heads, pre-multiplied by scale * log2(e).
-  for (int idx = threadIdx.x; idx < GH * D; idx += kThreads) {
-    const int i = idx / D, d = idx % D;
-    float x = 0.f;
-    if (i < nh) {
-      const int64_t off = static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(h_first + i) * p.q_sh + d;
-      if constexpr (BF16)
-        x = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.q)[off]);
-      else
-        x = __half2float(reinterpret_cast<const __half *>(p.q)[off]);
+  auto q_at = [&](int i, int d) -> float {
+    if (i >= nh) return 0.f;
+    const int64_t off = static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(h_first + i) * p.q_sh + d;
+    if constexpr (BF16)
+      return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.q)[off]);
+    else
+      return __half2float(reinterpret_cast<const __half *>(p.q)[off]);
+  };
+  if (p.rope == 0) {
+    for (int idx = threadIdx.x; idx < GH * D; idx += kThreads) sq[idx] = q_at(idx / D, idx % D) * p.scale_log2;
+  } else {
+    // Rotary embeddings: the query sits at position len - 1 (the keys in the
+    // cache were rotated when they were written); one pair per thread.
+    const uint32_t qpos = static_cast<uint32_t>(len > 0 ? len - 1 : 0);
+    for (int idx = threadIdx.x; idx < GH * (D / 2); idx += kThreads) {
+      const int i = idx / (D / 2), c = idx % (D / 2);
+      const int da = p.rope == 2 ? 2 * c : c, db = p.rope == 2 ? 2 * c + 1 : c + D / 2;
+      float sn, cs;
+      rope_sincos(qpos, p.rope_f[c], &sn, &cs);
+      const float xa = q_at(i, da), xb = q_at(i, db);
+      sq[i * D + da] = fmaf(xa, cs, -xb * sn) * p.scale_log2;
+      sq[i * D + db] = fmaf(xb, cs, xa * sn) * p.scale_log2;
     }
-    sq[idx] = x * p.scale_log2;
   }
   __syncthreads();
 
@@ -509,6 +522,65 @@ __global__ void __launch_bounds__(256) kv_cache_write_paged_kernel(const KvWrite
   }
 }
 
+// Cache write with rotary embeddings: new keys are rotated at the cache
+// position they are written to (dense: pos + t; paged: positions[b] + t), one
+// group of 8 coordinate pairs (two 16-byte pieces) per thread; values are
+// copied as they are, one 16-byte piece per thread.  A paged write whose page
+// index or page id is out of range is skipped and recorded as kErrBadIndex.
+template <bool PAGED, bool BF16>
+__global__ void __launch_bounds__(256) kv_cache_write_rope_kernel(const __grid_constant__ KvWriteParams p) {
+  griddep_wait();
+  if (load_volatile(p.err) != 0) return;
+  const int pieces = p.D / 8;   // 16-byte pieces per row
+  const int groups = p.D / 16;  // groups of 8 pairs per key row
+  const int64_t rows = p.total_units / pieces;  // B * H_kv * n_new
+  const int64_t k_units = rows * groups;
+  const bool inter = p.rope == 2;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < k_units + p.total_units;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool is_v = u >= k_units;
+    int64_t x = is_v ? u - k_units : u;
+    const int part = static_cast<int>(x % (is_v ? pieces : groups));
+    x /= is_v ? pieces : groups;
+    const int t = static_cast<int>(x % p.n_new);
+    x /= p.n_new;
+    const int hk = static_cast<int>(x % p.Hkv);
+    const int64_t b = x / p.Hkv;
+    int pos = p.pos + t;
+    int64_t row_c;  // cache row offset in elements (page, head, row) or (batch, head, position)
+    if constexpr (PAGED) {
+      pos = p.positions[b] + t;
+      const int pidx = pos >= 0 ? pos / p.page_size : -1;
+      const int page = (pidx >= 0 && pidx < p.max_pages) ? p.block_table[b * p.bt_stride + pidx] : -1;
+      if (page < 0 || page >= p.num_pages) {
+        atomicOr(p.err, kErrBadIndex);
+        continue;
+      }
+      const int r = pos % p.page_size;
+      row_c = is_v ? page * p.vc_sb + hk * p.vc_sh + r * p.vc_sn : page * p.kc_sb + hk * p.kc_sh + r * p.kc_sn;
+    } else {
+      row_c = is_v ? b * p.vc_sb + hk * p.vc_sh + pos * p.vc_sn : b * p.kc_sb + hk * p.kc_sh + pos * p.kc_sn;
+    }
+    if (is_v) {
+      const char *src = reinterpret_cast<const char *>(p.vn) + 2 * (b * p.vn_sb + hk * p.vn_sh + t * p.vn_sn + part * 8);
+      char *dst = reinterpret_cast<char *>(p.vc) + 2 * (row_c + part * 8);
+      *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+      continue;
+    }
+    const int ca = inter ? 2 * part : part, cb = inter ? 2 * part + 1 : part + p.D / 16;
+    const char *src = reinterpret_cast<const char *>(p.kn) + 2 * (b * p.kn_sb + hk * p.kn_sh + t * p.kn_sn);
+    char *dst = reinterpret_cast<char *>(p.kc) + 2 * row_c;
+    uint4 A = *reinterpret_cast<const uint4 *>(src + 16 * ca), Bv = *reinterpret_cast<const uint4 *>(src + 16 * cb);
+    float cs[8], sn[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rope_sincos(static_cast<uint32_t>(pos), p.rope_f[8 * part + i], &sn[i], &cs[i]);
+    if (inter) rope_rotate_group<BF16, true>(A, Bv, cs, sn);
+    else rope_rotate_group<BF16, false>(A, Bv, cs, sn);
+    *reinterpret_cast<uint4 *>(dst + 16 * ca) = A;
+    *reinterpret_cast<uint4 *>(dst + 16 * cb) = Bv;
+  }
+}
+
 // Launches with programmatic stream serialization: the kernel's blocks may be
 // scheduled while the preceding kernel of the stream drains, which hides the
 // launch gap between the short kernels of a decode step.  Every kernel launched
@@ -571,11 +643,19 @@ cudaError_t launch_decode(int D, bool bf16, bool paged, int gh, const CUtensorMa
 }
 
 cudaError_t launch_kv_cache_write(const KvWriteParams &p, bool paged, cudaStream_t stream) {
-  const int64_t work = 2 * p.total_units;
+  const int64_t work = p.rope ? p.total_units * 3 / 2 : 2 * p.total_units;
   int64_t blocks = (work + 255) / 256;
   if (blocks > 65535 * 8) blocks = 65535 * 8;
-  return launch_serialized(paged ? kv_cache_write_paged_kernel : kv_cache_write_kernel,
-                           dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
+  const dim3 grid(static_cast<unsigned>(blocks));
+  if (p.rope) {
+    if (paged)
+      return p.is_bf16 ? launch_serialized(kv_cache_write_rope_kernel<true, true>, grid, dim3(256), 0, stream, p)
+                       : launch_serialized(kv_cache_write_rope_kernel<true, false>, grid, dim3(256), 0, stream, p);
+    return p.is_bf16 ? launch_serialized(kv_cache_write_rope_kernel<false, true>, grid, dim3(256), 0, stream, p)
+                     : launch_serialized(kv_cache_write_rope_kernel<false, false>, grid, dim3(256), 0, stream, p);
+  }
+  return launch_serialized(paged ? kv_cache_write_paged_kernel : kv_cache_write_kernel, grid, dim3(256), 0, stream,
+                           p);
 }
 
 }  // namespace attn

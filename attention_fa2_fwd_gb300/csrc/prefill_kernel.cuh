@@ -1,8 +1,10 @@
 // prefill_kernel.cuh -- fused attention forward (prefill) kernel for sm_103a.
 //
-// Included by prefill.cu (plain causal / full masks) and prefill_masked.cu
-// (sliding windows and ALiBi), which instantiate it with MASKED false / true
-// in separate translation units compiled in parallel.
+// Included by prefill.cu (plain causal / full masks), prefill_masked.cu
+// (sliding windows and ALiBi), prefill_rope.cu and prefill_rope_masked.cu
+// (the same two with rotary position embeddings), which instantiate it with
+// MASKED and ROPE false / true in separate translation units compiled in
+// parallel.
 //
 // Persistent: one CTA per SM walks a sequence of units; a unit is TWO 128-row
 // query tiles (rows q0..q0+255) of one (batch, q-head), so the tensor core
@@ -15,9 +17,11 @@
 //   warp 9      TMEM allocator and tcgen05 MMA issuer (one thread), per KV tile j:
 //                 S0_j = Q0 K_j^T;  O1 += P1_{j-1} V_{j-1};  S1_j = Q1 K_j^T;  O0 += P0_j V_j
 //               (SS form for Q K^T, TS form with P read from TMEM for P V)
-//   warp 10     variable length only: zeroes the rows past a sequence's end in
-//               its last V tile before P V reads it
-//   warp 11     idle (it completes the register split of its warpgroup)
+//   warps 10-11 rotary embeddings only (ROPE builds): rotate both Q tiles and
+//               every K tile in shared memory once TMA has landed them, before
+//               the MMA thread may read them
+//   warp 10     variable length: also zeroes the rows past a sequence's end in
+//               its last V tile before P V reads it (otherwise idle, like warp 11)
 //
 // The algorithm is the online softmax of "Skill: Write a Triton Attention
 // Kernel" (Required reasoning process, steps 4-9): running max m and sum l in
@@ -45,6 +49,7 @@
 
 #include "attn_internal.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace attn {
 namespace {
@@ -86,9 +91,12 @@ struct Cfg {
   static constexpr int B_DONE = 7 + 4 * ST; // every MMA completed
   static constexpr int B_VZ = 8 + 4 * ST;   // variable length: V rows past the sequence zeroed
   static constexpr int B_VT = 9 + 4 * ST;   // variable length: the tail V tile has landed
-  static constexpr int NBAR = 10 + 4 * ST;
+  static constexpr int B_QR = 10 + 4 * ST;  // rotary: both Q tiles rotated
+  static constexpr int B_KR = 11 + 4 * ST;  // + stage: rotary: K tile rotated
+  static constexpr int NBAR = 11 + 5 * ST;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+  static constexpr uint32_t OFF_ROPE = (OFF_MISC + 16 + 7) & ~7u;  // rotary turn steps, uint64 [D/2]
+  static constexpr uint32_t SMEM_USED = OFF_ROPE + (D / 2) * 8;
   // + slack for 1024-byte alignment; at least 116 KB so that only one CTA (which
   // holds all 512 TMEM columns) is resident per SM.
   static constexpr uint32_t SMEM_BYTES = (SMEM_USED + 1024 > 116u * 1024) ? SMEM_USED + 1024 : 116u * 1024;
@@ -227,10 +235,13 @@ __device__ __forceinline__ int unit_index(int k, int c, int g) { return k * g + 
 // of a sequence -- whose tail rows belong to the next sequence -- gets those
 // rows zeroed by warp 10 before P V reads it, so nothing from another sequence
 // (not even a non-finite value times a zero weight) reaches the result.
-template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED>
+// ROPE: warps 10 and 11 rotate the Q tiles and each K tile in shared memory
+// (rows at their positions within the sequence); the MMA thread waits on the
+// "rotated" barriers instead of the TMA ones.
+template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillParams p) {
   using C = Cfg<D>;
   constexpr int ST = C::ST;
   extern __shared__ uint8_t smem_raw[];
@@ -269,6 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::B_DONE), 1);
     mbar_init(BAR(C::B_VZ), 1);
     mbar_init(BAR(C::B_VT), 1);
+    mbar_init(BAR(C::B_QR), 2);  // one arrival per rotating warp
+    for (int s = 0; s < ST; ++s) mbar_init(BAR(C::B_KR + s), 2);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -281,6 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+  }
+  if constexpr (ROPE) {
+    uint64_t *fs = reinterpret_cast<uint64_t *>(smem + C::OFF_ROPE);
+    for (int i = threadIdx.x; i < D / 2; i += kThreads) fs[i] = p.rope_f[i];
   }
   tc_fence_before();
   __syncthreads();
@@ -389,6 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (!first || kk > 0) ? 1u : 0u);
           }
         };
+        // Q and K may be read once they landed (or, with rotary embeddings,
+        // once warps 10-11 rotated them).
+        constexpr int kQReady = ROPE ? C::B_QR : C::B_Q;
+        constexpr int kKReady = ROPE ? C::B_KR : C::B_KF;
         bool ok = true;
         int st = 0;                 // ring stage of the next KV tile
         uint32_t ph = 0;            // its phase
@@ -419,11 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // instead on the all-done barrier's (never incomplete) phase before
             // its first, which passes at once.
             const bool has_kv = J0 < J1;
-            if (!(ok = mbar_wait(BAR(has_kv ? C::B_Q : C::B_DONE), has_kv ? (nq & 1) : 1u, abort_flag, p.err)))
+            if (!(ok = mbar_wait(BAR(has_kv ? kQReady : C::B_DONE), has_kv ? (nq & 1) : 1u, abort_flag, p.err)))
               break;
             nq += has_kv ? 1 : 0;
           } else {
-            if (!(ok = mbar_wait(BAR(C::B_Q), nq & 1, abort_flag, p.err))) break;
+            if (!(ok = mbar_wait(BAR(kQReady), nq & 1, abort_flag, p.err))) break;
             ++nq;
           }
           bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
@@ -436,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // instruction after a P V product is the following S product, so the
           // tensor pipe gets no gap there.
           if (J0 < J1) {
-            ok = mbar_wait(BAR(C::B_KF + st), ph, abort_flag, p.err);
+            ok = mbar_wait(BAR(kKReady + st), ph, abort_flag, p.err);
             if (ok && J0 >= lo0 && J0 < hi0) {
               tc_fence_after();
               issue_s(0, dq0, dk + st * kStage16);
@@ -463,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_commit(BAR(C::B_KE + st));  // both S products that read K_j are issued
             v_waited = false;
-            if (j + 1 < J1 && !(ok = mbar_wait(BAR(C::B_KF + st1), ph1, abort_flag, p.err))) break;
+            if (j + 1 < J1 && !(ok = mbar_wait(BAR(kKReady + st1), ph1, abort_flag, p.err))) break;
             if (h0) {
               // O0 += P0_j V_j
               if (!(ok = mbar_wait(BAR(C::B_PF + 0), pf0, abort_flag, p.err))) break;
@@ -517,22 +538,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(BAR(C::B_DONE), 0, nullptr, p.err);
       }
       __syncwarp();
-    } else if (warp == 10) {
-      // ---------------------------------------------------------- variable length: tail of V
-      if constexpr (VARLEN) {
-        int pos = 0, nvz = 0;  // ring position of the unit's first KV tile; tails zeroed
-        for (int k = 0; k * u_step < n_units; ++k) {
-          const int u = unit_index(k, u_first, u_step);
-          if (u >= n_units) continue;
-          const Unit U = make_unit<CAUSAL, VARLEN>(u, p, win_l, win_r);
-          if (U.kind != kRun) continue;
-          if (U.zero_v) {
-            const int st = (pos + U.j_tail - U.J0) % ST;  // ring stage of the tail tile
+    } else {
+      // ---------------------------------------------------------- warps 10-11
+      // Rotary embeddings (ROPE): both warps rotate each unit's Q tiles and then
+      // its K tiles, in the order the producer loads them.  Variable length:
+      // warp 10 then zeroes the rows past the sequence in the unit's tail V tile.
+      constexpr int G = D / 16;             // groups of 8 pairs per row
+      constexpr int RPT = kBM * G / 64;     // consecutive rows per thread in a 128-row tile
+      const int tid = threadIdx.x - 320;    // 0..63
+      const int g = tid % G, rb = tid / G;  // this thread's pair group and row block
+      float c1[8], s1[8];                   // rotation by one position of the group's 8 pairs
+      const uint64_t *fs = reinterpret_cast<const uint64_t *>(smem + C::OFF_ROPE);
+      if constexpr (ROPE) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rope_sincos(1u, fs[8 * g + i], &s1[i], &c1[i]);
+      }
+      // Rotates rows [rb * RPT, rb * RPT + RPT) of the 128-row tile at `tile`
+      // (64-column blocks CHUNK bytes apart, 128-byte swizzle); row r sits at
+      // position pos0 + r.
+      auto rotate_tile = [&](uint8_t *tile, uint32_t chunk_bytes, int pos0) {
+        int ca, cb;
+        float cs[8], sn[8];
+        const uint32_t r0 = static_cast<uint32_t>(rb * RPT);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rope_sincos(static_cast<uint32_t>(pos0) + r0, fs[8 * g + i], &sn[i], &cs[i]);
+        if (p.rope_inter) rope_group_chunks<D, true>(g, &ca, &cb);
+        else rope_group_chunks<D, false>(g, &ca, &cb);
+        uint8_t *ta = tile + (ca >> 3) * chunk_bytes, *tb = tile + (cb >> 3) * chunk_bytes;
+        ca &= 7;
+        cb &= 7;
+#pragma unroll 2
+        for (int rr = 0; rr < RPT; ++rr) {
+          const uint32_t r = r0 + rr;
+          uint4 *pa = reinterpret_cast<uint4 *>(ta + r * 128 + ((ca ^ (r & 7)) << 4));
+          uint4 *pb = reinterpret_cast<uint4 *>(tb + r * 128 + ((cb ^ (r & 7)) << 4));
+          uint4 A = *pa, Bv = *pb;
+          if (p.rope_inter) rope_rotate_group<BF16, true>(A, Bv, cs, sn);
+          else rope_rotate_group<BF16, false>(A, Bv, cs, sn);
+          *pa = A;
+          *pb = Bv;
+          rope_step(cs, sn, c1, s1);
+        }
+      };
+      int st = 0, nq = 0, pos = 0, nvz = 0;  // K ring stage, Q loads, ring position, tails zeroed
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int k = 0; ok && k * u_step < n_units; ++k) {
+        if constexpr (!ROPE && !VARLEN) break;
+        const int u = unit_index(k, u_first, u_step);
+        if (u >= n_units) continue;
+        const Unit U = make_unit<CAUSAL, VARLEN>(u, p, win_l, win_r);
+        if (U.kind != kRun) continue;
+        if constexpr (ROPE) {
+          if (U.J0 < U.J1) {  // the producer loads Q only for units with KV tiles
+            ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_Q), nq & 1, abort_flag, p.err));
+            ++nq;
+            if (!ok) break;
+            rotate_tile(smem + C::OFF_Q, C::CHUNK_Q, U.q0);
+            rotate_tile(smem + C::OFF_Q + C::QT_BYTES, C::CHUNK_Q, U.q0 + kBM);
+            fence_proxy_async_smem();  // the tensor core reads the rotated rows
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C::B_QR));
+          }
+          for (int j = U.J0; ok && j < U.J1; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_KF + st), ph, abort_flag, p.err));
+            if (!ok) break;
+            rotate_tile(smem + C::OFF_K + st * C::KV_BYTES, C::CHUNK_KV, j * kBN);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C::B_KR + st));
+            if (++st == ST) {
+              st = 0;
+              ph ^= 1;
+            }
+          }
+          if (!ok) break;
+        }
+        if constexpr (VARLEN) {
+          if (warp == 10 && U.zero_v) {
+            const int st_t = (pos + U.j_tail - U.J0) % ST;  // ring stage of the tail tile
             const bool landed = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_VT), nvz & 1, abort_flag, p.err));
             ++nvz;
             if (!landed) break;
             const int r0 = U.Nkv % kBN;  // rows r0..127 of the tile lie past the sequence
-            uint8_t *vt = smem + C::OFF_V + st * C::KV_BYTES;
+            uint8_t *vt = smem + C::OFF_V + st_t * C::KV_BYTES;
             const int pieces = (kBN - r0) * 8;  // 16-byte pieces per 128-byte row chunk
             for (int c = 0; c < C::KCH; ++c)
               for (int i = lane; i < pieces; i += 32)
@@ -761,10 +850,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED>
+template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED, bool ROPE>
 cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p,
                        int B, cudaStream_t stream) {
-  auto kern = prefill_fwd_kernel<D, CAUSAL, BF16, VARLEN, MASKED>;
+  auto kern = prefill_fwd_kernel<D, CAUSAL, BF16, VARLEN, MASKED, ROPE>;
   constexpr uint32_t smem = Cfg<D>::SMEM_BYTES;
   // setmaxnreg redistributes the registers the CTA was launched with; a split
   // larger than that pool would never be granted, so refuse to launch then.
@@ -779,15 +868,15 @@ cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
   return cudaGetLastError();
 }
 
-// Dispatch over D, causal, dtype and varlen for one value of MASKED.
-template <bool MASKED>
+// Dispatch over D, causal, dtype and varlen for one value of MASKED and ROPE.
+template <bool MASKED, bool ROPE>
 cudaError_t launch_prefill_variant(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq,
                                    const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
                                    cudaStream_t stream) {
 #define ATTN_PREFILL_CASE(DD, CC, BB)                                                           \
   if (D == DD && causal == CC && bf16 == BB)                                                    \
-    return varlen ? launch_one<DD, CC, BB, true, MASKED>(tq, tk, tv, p, B, stream)              \
-                  : launch_one<DD, CC, BB, false, MASKED>(tq, tk, tv, p, B, stream);
+    return varlen ? launch_one<DD, CC, BB, true, MASKED, ROPE>(tq, tk, tv, p, B, stream)        \
+                  : launch_one<DD, CC, BB, false, MASKED, ROPE>(tq, tk, tv, p, B, stream);
   ATTN_PREFILL_CASE(128, true, true)
   ATTN_PREFILL_CASE(128, false, true)
   ATTN_PREFILL_CASE(128, true, false)

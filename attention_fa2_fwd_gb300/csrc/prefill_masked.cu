@@ -7,7 +7,7 @@ namespace attn {
 cudaError_t launch_prefill_masked(int D, bool causal, bool bf16, bool varlen, const CUtensorMap &tq,
                                   const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
                                   cudaStream_t stream) {
-  return launch_prefill_variant<true>(D, causal, bf16, varlen, tq, tk, tv, p, B, stream);
+  return launch_prefill_variant<true, false>(D, causal, bf16, varlen, tq, tk, tv, p, B, stream);
 }
 
 }  // namespace attn

@@ -9,6 +9,7 @@
     python -m attention_fa2_fwd_gb300.run_case cross   [--D 64|128: the cross-attention workload, B=4 H_q=16
                                                         H_kv=4 N_q=1024 N_kv=4096, (B,N,H,D) memory, non-causal]
     prefill / decode / decode_paged also take --window-left W and --alibi 1 (sliding window, ALiBi slopes)
+    prefill / varlen / cross / decode / decode_paged take --rope THETA [--rope-interleaved 1] (rotary embeddings)
     decode / decode_paged take --graph 1: the step (cache write of one token + decode) captured once in a
     CUDA graph and replayed, against the same calls launched one by one
 
@@ -44,6 +45,8 @@ def main():
     ap.add_argument("--window-left", type=int, default=-1, help="sliding window: keys i - W .. i (-1: none)")
     ap.add_argument("--alibi", type=int, default=0, help="ALiBi slopes 2^(-8 (h + 1) / H_q)")
     ap.add_argument("--graph", type=int, default=0, help="decode: time a one-token serving step, eager vs CUDA graph")
+    ap.add_argument("--rope", type=float, default=0.0, help="rotary embeddings of this base (0: none)")
+    ap.add_argument("--rope-interleaved", type=int, default=0, help="rotary pairs (2c, 2c+1) instead of (c, c+D/2)")
     a = ap.parse_args()
     dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
     dev = torch.device("cuda", 0)
@@ -55,6 +58,7 @@ def main():
     flush = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     wl = a.window_left
+    rope = dict(rope_theta=a.rope, rope_interleaved=bool(a.rope_interleaved))
     slopes = (torch.tensor([2.0 ** (-8.0 * (h + 1) / a.Hq) for h in range(a.Hq)], dtype=torch.float32, device=dev)
               if a.alibi else None)
     if a.kind == "prefill":
@@ -70,7 +74,8 @@ def main():
         work = 4.0 * B * a.Hq * a.D * pairs if (a.causal or wl >= 0) else 4.0 * B * a.Hq * a.N * a.N * a.D
 
         def call():
-            A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse, window=(wl, -1), alibi_slopes=slopes)
+            A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse, window=(wl, -1), alibi_slopes=slopes,
+                      **rope)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "varlen":
         B = a.B or 16
@@ -86,7 +91,7 @@ def main():
 
         def call():
             A.prefill_varlen(q, k, v, cu, cu, max(lens), max(lens), causal=bool(a.causal), out=o, lse_out=lse,
-                             window=(a.window_left, -1), alibi_slopes=slopes)
+                             window=(a.window_left, -1), alibi_slopes=slopes, **rope)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "cross":
         import attention_fa2_fwd_gb300.inputs as I
@@ -101,7 +106,7 @@ def main():
         work = w.flops
 
         def call():
-            A.prefill(q, k, v, causal=False, out=o, lse_out=lse)
+            A.prefill(q, k, v, causal=False, out=o, lse_out=lse, **rope)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "bwd":
         B = a.B or 2
@@ -138,7 +143,7 @@ def main():
 
         def call():
             A.decode_paged(qd, kp, vp, table, lens, a.L, out=od, lse_out=lsed, workspace=ws, window_left=wl,
-                           alibi_slopes=slopes)
+                           alibi_slopes=slopes, **rope)
         unit, scale = "GB/s", 1e9
     else:
         B = a.B or 64
@@ -150,7 +155,8 @@ def main():
         work = 2.0 * B * a.Hkv * (min(a.L, wl + 1) if wl >= 0 else a.L) * a.D * 2
 
         def call():
-            A.decode(qd, kc, vc, a.L, out=od, lse_out=lsed, workspace=ws, window_left=wl, alibi_slopes=slopes)
+            A.decode(qd, kc, vc, a.L, out=od, lse_out=lsed, workspace=ws, window_left=wl, alibi_slopes=slopes,
+                     **rope)
         unit, scale = "GB/s", 1e9
     if a.graph and a.kind in ("decode", "decode_paged"):
         # one serving step: write one new token per request, then decode
@@ -160,13 +166,13 @@ def main():
             pos = a.L - 1
 
             def serve():
-                A.write_kv_cache(kc, vc, kn, vn, pos)
+                A.write_kv_cache(kc, vc, kn, vn, pos, **rope)
                 call()
         else:
             positions = (lens - 1).clamp(min=0)
 
             def serve():
-                A.write_kv_cache_paged(kp, vp, kn, vn, table, positions)
+                A.write_kv_cache_paged(kp, vp, kn, vn, table, positions, **rope)
                 call()
         serve()
         torch.cuda.synchronize()

@@ -315,6 +315,21 @@ attn_status_t kv_cache_write(void *k_cache, void *v_cache, const void *k_new, co
                              const int64_t vn_str[4], void *stream);
 
 /*
+ * kv_cache_write_ex -- kv_cache_write with options: with rope_theta > 0 each
+ * new key is rotated (rotary position embeddings, see attn_options_t) at the
+ * cache position it is written to, pos + t, so that the cache holds the keys
+ * that attn_fwd_decode_ex with the same rope_theta and rope_interleaved
+ * expects ("Skill: Write a Triton Attention Kernel", Use this when: RoPE-fused
+ * attention; "Triton-FlashAttention", Deferred: fused rotary embeddings).
+ * Values are copied unchanged.  The other option fields are not used here.
+ * The rotation is computed in fp32 and rounded once to the cache's type.
+ */
+attn_status_t kv_cache_write_ex(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                                attn_dtype_t dtype, int B, int H_kv, int n_new, int D, int pos, int max_len,
+                                const int64_t kc_str[4], const int64_t vc_str[4], const int64_t kn_str[4],
+                                const int64_t vn_str[4], const attn_options_t *opts, void *stream);
+
+/*
  * attn_fwd_prefill_host -- attn_fwd_prefill_ex on host-resident tensors, with
  * the host-to-device copies, the compute and the device-to-host copies
  * pipelined.  (The pages time kernels on device-resident inputs; this entry
@@ -450,6 +465,15 @@ attn_status_t kv_cache_write_paged(void *k_pages, void *v_pages, const void *k_n
                                    const int32_t *positions, const int64_t kp_str[4], const int64_t vp_str[4],
                                    const int64_t kn_str[4], const int64_t vn_str[4], void *stream);
 
+/* kv_cache_write_paged with options: with rope_theta > 0 the key of token t of
+ * request b is rotated at its position positions[b] + t (see kv_cache_write_ex). */
+attn_status_t kv_cache_write_paged_ex(void *k_pages, void *v_pages, const void *k_new, const void *v_new,
+                                      attn_dtype_t dtype, int B, int H_kv, int n_new, int D, int num_pages,
+                                      int page_size, const int32_t *block_table, int max_pages, int64_t bt_stride,
+                                      const int32_t *positions, const int64_t kp_str[4], const int64_t vp_str[4],
+                                      const int64_t kn_str[4], const int64_t vn_str[4], const attn_options_t *opts,
+                                      void *stream);
+
 /*
  * attn_get_device_error -- synchronise `stream`, then read and clear the
  * device error word of the current device in one atomic step (a one-thread
@@ -480,7 +504,8 @@ attn_status_t attn_selftest_wait_timeout(void *stream);
  * utility of this library; the pages define no counterpart.) */
 const char *attn_status_string(attn_status_t status);
 
-/* attn_version -- library version as major * 10000 + minor * 100 + patch.
+/* attn_version -- library version as major * 10000 + minor * 100 + patch
+ * (200: options with rotary embeddings and the decode split count).
  * (A utility of this library; the pages define no counterpart.) */
 int attn_version(void);
 
