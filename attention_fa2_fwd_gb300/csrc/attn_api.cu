@@ -200,6 +200,7 @@ struct Opts {
   float rope_theta = 0.f;        // 0: no rotary embedding
   int rope_interleaved = 0;      // 0: pairs (c, c + D/2); 1: pairs (2c, 2c + 1)
   int num_splits = 0;            // decode: 0 automatic, else at most this many KV splits
+  int rope_rotated_keys = 0;     // prefill: the keys come already rotated
 };
 constexpr int kMaxDecodeSplits = 64;
 
@@ -210,6 +211,7 @@ attn_status_t read_opts(const attn_options_t *opts, Opts *o) {
   if (!std::isfinite(opts->rope_theta) || opts->rope_theta < 0.f) return ATTN_ERR_INVALID_ARG;
   if (opts->rope_interleaved != 0 && opts->rope_interleaved != 1) return ATTN_ERR_INVALID_ARG;
   if (opts->num_splits < 0 || opts->num_splits > kMaxDecodeSplits) return ATTN_ERR_INVALID_ARG;
+  if (opts->rope_rotated_keys != 0 && opts->rope_rotated_keys != 1) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(opts->alibi_slopes) & 3) != 0) return ATTN_ERR_ALIGNMENT;
   o->wl = opts->window_left;
   o->wr = opts->window_right;
@@ -217,6 +219,7 @@ attn_status_t read_opts(const attn_options_t *opts, Opts *o) {
   o->rope_theta = opts->rope_theta;
   o->rope_interleaved = opts->rope_interleaved;
   o->num_splits = opts->num_splits;
+  o->rope_rotated_keys = opts->rope_rotated_keys;
   return ATTN_OK;
 }
 
@@ -343,6 +346,7 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
   const bool rope = op.rope_theta > 0.f;
   if (rope) {
     p.rope_inter = op.rope_interleaved;
+    p.rope_k = op.rope_rotated_keys ? 0 : 1;
     fill_rope_steps(op.rope_theta, D, p.rope_f);
   }
   const DeviceState *dev = nullptr;
@@ -417,6 +421,7 @@ attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const voi
   const bool rope = op.rope_theta > 0.f;
   if (rope) {
     p.rope_inter = op.rope_interleaved;
+    p.rope_k = op.rope_rotated_keys ? 0 : 1;
     fill_rope_steps(op.rope_theta, D, p.rope_f);
   }
   const DeviceState *dev = nullptr;
@@ -1036,7 +1041,8 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
         // The chunk is a contiguous (1, nqh, N_q, D) / (1, nh, N_kv, D) problem.
         const int64_t sq[4] = {static_cast<int64_t>(nqh) * N_q * D, static_cast<int64_t>(N_q) * D, D, 1};
         const int64_t sk[4] = {static_cast<int64_t>(nh) * N_kv * D, static_cast<int64_t>(N_kv) * D, D, 1};
-        attn_options_t oc{wl, wr, slopes ? slopes + qh0 : nullptr, op.rope_theta, op.rope_interleaved, 0};
+        attn_options_t oc{wl, wr, slopes ? slopes + qh0 : nullptr, op.rope_theta, op.rope_interleaved, 0,
+                          op.rope_rotated_keys};
         const attn_status_t cs = attn_fwd_prefill_ex(dq + qo, dk + ko, dv + ko, dout + qo,
                                                      lse ? reinterpret_cast<float *>(reinterpret_cast<char *>(dl) + lo)
                                                          : nullptr,

@@ -44,8 +44,9 @@ struct PrefillParams {
   const float *alibi_slopes;
   // Rotary embeddings (ROPE builds): pair c of a row at position p turns by
   // (p * rope_f[c] mod 2^64) / 2^64 of a full turn; rope_inter selects the
-  // pairs (2c, 2c + 1) instead of (c, c + D/2).
-  int rope_inter;
+  // pairs (2c, 2c + 1) instead of (c, c + D/2); rope_k = 0 when the keys come
+  // already rotated (only the Q tiles are rotated then).
+  int rope_inter, rope_k;
   uint64_t rope_f[64];
 };
 

@@ -56,17 +56,32 @@ namespace {
 
 constexpr int kBM = kPrefillBM;  // rows per query tile
 constexpr int kBN = kPrefillBN;  // keys per KV tile
-constexpr int kThreads = 384;
+// 12 warps in every build.  (A 14-warp rotary build with four rotation
+// warps was tried: its launch caps every thread at 128 registers and the
+// warps then spill.)
+template <bool ROPE>
+constexpr int kThreadsFor = 384;
+template <bool ROPE>
+constexpr int kRopeWarps = 2;
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 constexpr int kSoftmaxRegs = 200;
 constexpr int kUnlimited = 0x3fffffff;  // "no window bound" (large, yet safe to add small offsets to)
-constexpr int kOtherRegs = 96;
+// Registers of the non-softmax warps after setmaxnreg: what is left of the
+// launch's pool after the two softmax warpgroups.
+template <bool ROPE>
+constexpr int kOtherRegsFor = 96;
 
-template <int D>
+template <int D, bool ROPE>
 struct Cfg {
   static constexpr int KCH = D / 64;                  // 128-byte chunks along D
-  static constexpr int ST = (D == 128) ? 2 : 3;       // K/V pipeline stages
+  // Shared-memory stages of the K and V rings.  The rotary build at D = 128
+  // keeps a third K stage (K is loaded one tile ahead of V and rotated on chip,
+  // which must stay off the products' critical path); 3 x 32 KB of K + 2 x 32
+  // KB of V + 64 KB of Q still fit in 227 KB.
+  static constexpr int KST = (D == 128) ? (ROPE ? 3 : 2) : 3;
+  static constexpr int VST = (D == 128) ? 2 : 3;
+  static constexpr bool SPLIT = KST != VST;           // the two rings advance separately
   static constexpr uint32_t CHUNK_Q = kBM * 128;      // bytes of one 64-column chunk of a Q tile
   static constexpr uint32_t CHUNK_KV = kBN * 128;
   static constexpr uint32_t QT_BYTES = kBM * D * 2;   // one Q tile
@@ -77,23 +92,23 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + 2 * QT_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + ST * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + ST * KV_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KST * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + VST * KV_BYTES;
   // barrier indices
   static constexpr int B_Q = 0;
-  static constexpr int B_KF = 1;            // + stage
-  static constexpr int B_KE = 1 + ST;       // + stage
-  static constexpr int B_VF = 1 + 2 * ST;   // + stage
-  static constexpr int B_VE = 1 + 3 * ST;   // + stage
-  static constexpr int B_SF = 1 + 4 * ST;   // + tile (2): S_i(j) computed
-  static constexpr int B_PF = 3 + 4 * ST;   // + tile (2): P_i(j) stored (and O_i rescaled)
-  static constexpr int B_OD = 5 + 4 * ST;   // + tile (2): last P_i V done
-  static constexpr int B_DONE = 7 + 4 * ST; // every MMA completed
-  static constexpr int B_VZ = 8 + 4 * ST;   // variable length: V rows past the sequence zeroed
-  static constexpr int B_VT = 9 + 4 * ST;   // variable length: the tail V tile has landed
-  static constexpr int B_QR = 10 + 4 * ST;  // rotary: both Q tiles rotated
-  static constexpr int B_KR = 11 + 4 * ST;  // + stage: rotary: K tile rotated
-  static constexpr int NBAR = 11 + 5 * ST;
+  static constexpr int B_KF = 1;                       // + K stage
+  static constexpr int B_KE = B_KF + KST;              // + K stage
+  static constexpr int B_VF = B_KE + KST;              // + V stage
+  static constexpr int B_VE = B_VF + VST;              // + V stage
+  static constexpr int B_SF = B_VE + VST;              // + tile (2): S_i(j) computed
+  static constexpr int B_PF = B_SF + 2;                // + tile (2): P_i(j) stored (and O_i rescaled)
+  static constexpr int B_OD = B_PF + 2;                // + tile (2): last P_i V done
+  static constexpr int B_DONE = B_OD + 2;              // every MMA completed
+  static constexpr int B_VZ = B_DONE + 1;              // variable length: V rows past the sequence zeroed
+  static constexpr int B_VT = B_VZ + 1;                // variable length: the tail V tile has landed
+  static constexpr int B_QR = B_VT + 1;                // rotary: both Q tiles rotated
+  static constexpr int B_KR = B_QR + 1;                // + K stage: rotary: K tile rotated
+  static constexpr int NBAR = B_KR + KST;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t OFF_ROPE = (OFF_MISC + 16 + 7) & ~7u;  // rotary turn steps, uint64 [D/2]
   static constexpr uint32_t SMEM_USED = OFF_ROPE + (D / 2) * 8;
@@ -239,11 +254,11 @@ __device__ __forceinline__ int unit_index(int k, int c, int g) { return k * g + 
 // (rows at their positions within the sequence); the MMA thread waits on the
 // "rotated" barriers instead of the TMA ones.
 template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED, bool ROPE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillParams p) {
-  using C = Cfg<D>;
-  constexpr int ST = C::ST;
+  using C = Cfg<D, ROPE>;
+  constexpr int KST = C::KST, VST = C::VST;
   extern __shared__ uint8_t smem_raw[];
 
   if (load_volatile(p.err) != 0) return;  // an earlier launch failed; nothing runs until it is read
@@ -266,9 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_Q), 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(BAR(C::B_KF + s), 1);
       mbar_init(BAR(C::B_KE + s), 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(BAR(C::B_VF + s), 1);
       mbar_init(BAR(C::B_VE + s), 1);
     }
@@ -280,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::B_DONE), 1);
     mbar_init(BAR(C::B_VZ), 1);
     mbar_init(BAR(C::B_VT), 1);
-    mbar_init(BAR(C::B_QR), 2);  // one arrival per rotating warp
-    for (int s = 0; s < ST; ++s) mbar_init(BAR(C::B_KR + s), 2);
+    mbar_init(BAR(C::B_QR), kRopeWarps<ROPE>);  // one arrival per rotating warp
+    for (int s = 0; s < KST; ++s) mbar_init(BAR(C::B_KR + s), kRopeWarps<ROPE>);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -297,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if constexpr (ROPE) {
     uint64_t *fs = reinterpret_cast<uint64_t *>(smem + C::OFF_ROPE);
-    for (int i = threadIdx.x; i < D / 2; i += kThreads) fs[i] = p.rope_f[i];
+    for (int i = threadIdx.x; i < D / 2; i += kThreadsFor<ROPE>) fs[i] = p.rope_f[i];
   }
   tc_fence_before();
   __syncthreads();
@@ -305,16 +322,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 8) {
-    setmaxnreg_dec<kOtherRegs>();
+    setmaxnreg_dec<kOtherRegsFor<ROPE>>();
     if (warp == 8) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0) {
         int issued_k = 0, issued_v = 0, nq = 0;  // K, V tiles and Q pairs issued so far
-        int st = 0;                              // ring stage of the next KV tile
-        uint32_t ph = 0;                         // its phase
+        int kst = 0, vst = 0;                    // ring stages of the next K and V tiles
+        uint32_t kph = 0, vph = 0;               // their phases
         int q_wait = -1;                         // what frees Q: -1 nothing, -2 the last Q load, else KE stage
         uint32_t q_phase = 0;
         bool ok = true;
+        // K (or V) tile j of unit U into the next stage of its ring, once the
+        // stage's previous tile (KST or VST loads back) has been released.
+        auto load_k = [&](const Unit &U, int j) -> bool {
+          if (issued_k >= KST && !mbar_wait(BAR(C::B_KE + kst), kph ^ 1, abort_flag, p.err)) return false;
+          mbar_arrive_expect_tx(BAR(C::B_KF + kst), C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+            tma_tile(sK + kst * C::KV_BYTES + c * C::CHUNK_KV, &tmK, c * 64, U.k_base + j * kBN, U.hk, U.bc,
+                     p.slots_k, BAR(C::B_KF + kst));
+          ++issued_k;
+          q_wait = kst;
+          q_phase = kph;
+          if (++kst == KST) {
+            kst = 0;
+            kph ^= 1;
+          }
+          return true;
+        };
+        auto load_v = [&](const Unit &U, int j) -> bool {
+          if (issued_v >= VST && !mbar_wait(BAR(C::B_VE + vst), vph ^ 1, abort_flag, p.err)) return false;
+          mbar_arrive_expect_tx(BAR(C::B_VF + vst), C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+            tma_tile(sV + vst * C::KV_BYTES + c * C::CHUNK_KV, &tmV, c * 64, U.k_base + j * kBN, U.hk, U.bc,
+                     p.slots_v, BAR(C::B_VF + vst));
+          ++issued_v;
+          if (++vst == VST) {
+            vst = 0;
+            vph ^= 1;
+          }
+          return true;
+        };
         for (int k = 0; ok && k * u_step < n_units; ++k) {
           const int u = unit_index(k, u_first, u_step);
           if (u >= n_units) continue;
@@ -343,38 +392,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_tile_once(sQ + t * C::QT_BYTES + c * C::CHUNK_Q, &tmQ, c * 64, U.q_base + U.q0 + t * kBM, U.h,
                             U.bc, p.slots_q, BAR(C::B_Q));
           ++nq;
-          for (int j = U.J0; j < U.J1; ++j) {
-            const bool reuse = issued_k >= ST;  // the stage held the tile ST positions back
-            if (reuse && !(ok = mbar_wait(BAR(C::B_KE + st), ph ^ 1, abort_flag, p.err))) break;
-            mbar_arrive_expect_tx(BAR(C::B_KF + st), C::KV_BYTES);
-#pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-              tma_tile(sK + st * C::KV_BYTES + c * C::CHUNK_KV, &tmK, c * 64, U.k_base + j * kBN, U.hk, U.bc,
-                       p.slots_k, BAR(C::B_KF + st));
-            ++issued_k;
-            if (reuse && !(ok = mbar_wait(BAR(C::B_VE + st), ph ^ 1, abort_flag, p.err))) break;
-            mbar_arrive_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
-#pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-              tma_tile(sV + st * C::KV_BYTES + c * C::CHUNK_KV, &tmV, c * 64, U.k_base + j * kBN, U.hk, U.bc,
-                       p.slots_v, BAR(C::B_VF + st));
-            ++issued_v;
-            q_wait = st;
-            q_phase = ph;
-            if (++st == ST) {
-              st = 0;
-              ph ^= 1;
+          if constexpr (C::SPLIT) {
+            // The K ring is deeper: K_{j+1} is requested before V_j, so each K
+            // tile lands (and is rotated) well before its first product.
+            if (U.J0 < U.J1 && !(ok = load_k(U, U.J0))) break;
+            for (int j = U.J0; j < U.J1; ++j) {
+              if (j + 1 < U.J1 && !(ok = load_k(U, j + 1))) break;
+              if (!(ok = load_v(U, j))) break;
+            }
+          } else {
+            for (int j = U.J0; j < U.J1; ++j) {
+              if (!(ok = load_k(U, j))) break;
+              if (!(ok = load_v(U, j))) break;
             }
           }
+          if (!ok) break;
           if (U.J0 == U.J1) q_wait = -2;
         }
         if (!ok) {
           // Let every copy already issued land before shared memory is released.
           if (nq > 0) mbar_wait(BAR(C::B_Q), (nq - 1) & 1, nullptr, p.err);
-          for (int i = max(0, issued_k - ST); i < issued_k; ++i)
-            mbar_wait(BAR(C::B_KF + i % ST), (i / ST) & 1, nullptr, p.err);
-          for (int i = max(0, issued_v - ST); i < issued_v; ++i)
-            mbar_wait(BAR(C::B_VF + i % ST), (i / ST) & 1, nullptr, p.err);
+          for (int i = max(0, issued_k - KST); i < issued_k; ++i)
+            mbar_wait(BAR(C::B_KF + i % KST), (i / KST) & 1, nullptr, p.err);
+          for (int i = max(0, issued_v - VST); i < issued_v; ++i)
+            mbar_wait(BAR(C::B_VF + i % VST), (i / VST) & 1, nullptr, p.err);
         }
       }
       __syncwarp();
@@ -409,10 +450,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Q and K may be read once they landed (or, with rotary embeddings,
         // once warps 10-11 rotated them).
         constexpr int kQReady = ROPE ? C::B_QR : C::B_Q;
-        constexpr int kKReady = ROPE ? C::B_KR : C::B_KF;
+        const int kKReady = (ROPE && p.rope_k) ? C::B_KR : C::B_KF;
         bool ok = true;
-        int st = 0;                 // ring stage of the next KV tile
-        uint32_t ph = 0;            // its phase
+        int kst = 0;                // K ring stage of the next KV tile
+        uint32_t kph = 0;           // its phase
+        // V ring stage and phase of the next KV tile: the same variables as K's
+        // unless the rings have different depths.
+        int vst_own = 0;
+        uint32_t vph_own = 0;
+        int &vst = C::SPLIT ? vst_own : kst;
+        uint32_t &vph = C::SPLIT ? vph_own : kph;
         uint32_t pf0 = 0, pf1 = 0;  // parities of the P-ready barriers
         int nq = 0, nvz = 0;        // units started; tail V tiles zeroed
         for (int k = 0; ok && k * u_step < n_units; ++k) {
@@ -450,76 +497,82 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
           bool h1p = false;       // tile 1 uses KV tile j-1
           bool first0 = true, first1 = true;
-          int sp = 0;             // ring stage of j-1
-          uint32_t pph = 0;       // and its phase
+          int vsp = 0;            // V ring stage of j-1
+          uint32_t vpph = 0;      // and its phase
           // S0_j is issued at the end of step j-1, right behind P0_{j-1} V_{j-1} (K_j
           // having been waited for before P0_{j-1}): the thread's next tcgen05
           // instruction after a P V product is the following S product, so the
           // tensor pipe gets no gap there.
           if (J0 < J1) {
-            ok = mbar_wait(BAR(kKReady + st), ph, abort_flag, p.err);
+            ok = mbar_wait(BAR(kKReady + kst), kph, abort_flag, p.err);
             if (ok && J0 >= lo0 && J0 < hi0) {
               tc_fence_after();
-              issue_s(0, dq0, dk + st * kStage16);
+              issue_s(0, dq0, dk + kst * kStage16);
             }
           }
           for (int j = J0; ok && j < J1; ++j) {
             const bool h0 = j >= lo0 && j < hi0, h1 = j >= lo1 && j < hi1;
-            const int st1 = st + 1 == ST ? 0 : st + 1;    // ring stage of j + 1
-            const uint32_t ph1 = st1 == 0 ? ph ^ 1 : ph;  // and its phase
+            const int kst1 = kst + 1 == KST ? 0 : kst + 1;    // K ring stage of j + 1
+            const uint32_t kph1 = kst1 == 0 ? kph ^ 1 : kph;  // and its phase
             const bool h0n = j + 1 >= lo0 && j + 1 < hi0;  // tile 0 uses KV tile j + 1
             if (h1p) {
               // O1 += P1_{j-1} V_{j-1}: tile 1 is the last user of V_{j-1}, so its stage is released
               if (!(ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err))) break;
               pf1 ^= 1;
-              if (!v_waited && !(ok = wait_v(j - 1, sp, pph))) break;
+              if (!v_waited && !(ok = wait_v(j - 1, vsp, vpph))) break;
               tc_fence_after();
-              issue_pv(1, first1, dv + sp * kStage16);
+              issue_pv(1, first1, dv + vsp * kStage16);
               first1 = false;
-              tc_commit(BAR(C::B_VE + sp));
+              tc_commit(BAR(C::B_VE + vsp));
             }
             if (h1) {
               tc_fence_after();
-              issue_s(1, dq1, dk + st * kStage16);
+              issue_s(1, dq1, dk + kst * kStage16);
             }
-            tc_commit(BAR(C::B_KE + st));  // both S products that read K_j are issued
+            tc_commit(BAR(C::B_KE + kst));  // both S products that read K_j are issued
             v_waited = false;
-            if (j + 1 < J1 && !(ok = mbar_wait(BAR(kKReady + st1), ph1, abort_flag, p.err))) break;
+            if (j + 1 < J1 && !(ok = mbar_wait(BAR(kKReady + kst1), kph1, abort_flag, p.err))) break;
             if (h0) {
               // O0 += P0_j V_j
               if (!(ok = mbar_wait(BAR(C::B_PF + 0), pf0, abort_flag, p.err))) break;
               pf0 ^= 1;
-              if (!(ok = wait_v(j, st, ph))) break;
+              if (!(ok = wait_v(j, vst, vph))) break;
               v_waited = true;
               tc_fence_after();
-              issue_pv(0, first0, dv + st * kStage16);
+              issue_pv(0, first0, dv + vst * kStage16);
               first0 = false;
-              if (!h1) tc_commit(BAR(C::B_VE + st));  // tile 1 does not use V_j
+              if (!h1) tc_commit(BAR(C::B_VE + vst));  // tile 1 does not use V_j
               if (j == hi0 - 1) tc_commit(BAR(C::B_OD + 0));
             } else if (!h1) {
               // A tile between the two bands: nothing reads V_j.  Its copy must land
               // before the stage is handed back for the next one.
-              if (!(ok = wait_v(j, st, ph))) break;
-              tc_commit(BAR(C::B_VE + st));
+              if (!(ok = wait_v(j, vst, vph))) break;
+              tc_commit(BAR(C::B_VE + vst));
             }
             if (j + 1 < J1 && h0n) {
               tc_fence_after();
-              issue_s(0, dq0, dk + st1 * kStage16);  // S0_{j+1}
+              issue_s(0, dq0, dk + kst1 * kStage16);  // S0_{j+1}
             }
             h1p = h1;
-            sp = st;
-            pph = ph;
-            st = st1;
-            ph = ph1;
+            vsp = vst;
+            vpph = vph;
+            if constexpr (C::SPLIT) {
+              if (++vst == VST) {
+                vst = 0;
+                vph ^= 1;
+              }
+            }
+            kst = kst1;
+            kph = kph1;
           }
           if (ok && h1p) {
             // the last P1 V of tile 1 (its band ends the ring)
-            ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err) && (v_waited || wait_v(J1 - 1, sp, pph));
+            ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err) && (v_waited || wait_v(J1 - 1, vsp, vpph));
             if (ok) {
               pf1 ^= 1;
               tc_fence_after();
-              issue_pv(1, first1, dv + sp * kStage16);
-              tc_commit(BAR(C::B_VE + sp));
+              issue_pv(1, first1, dv + vsp * kStage16);
+              tc_commit(BAR(C::B_VE + vsp));
               tc_commit(BAR(C::B_OD + 1));
             }
           }
@@ -543,9 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Rotary embeddings (ROPE): both warps rotate each unit's Q tiles and then
       // its K tiles, in the order the producer loads them.  Variable length:
       // warp 10 then zeroes the rows past the sequence in the unit's tail V tile.
+      constexpr int NT = kRopeWarps<ROPE> * 32;  // rotating threads
       constexpr int G = D / 16;             // groups of 8 pairs per row
-      constexpr int RPT = kBM * G / 64;     // consecutive rows per thread in a 128-row tile
-      const int tid = threadIdx.x - 320;    // 0..63
+      constexpr int RPT = kBM * G / NT;     // consecutive rows per thread in a 128-row tile
+      const int tid = threadIdx.x - 320;    // 0 .. NT - 1
       const int g = tid % G, rb = tid / G;  // this thread's pair group and row block
       float c1[8], s1[8];                   // rotation by one position of the group's 8 pairs
       const uint64_t *fs = reinterpret_cast<const uint64_t *>(smem + C::OFF_ROPE);
@@ -580,7 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           rope_step(cs, sn, c1, s1);
         }
       };
-      int st = 0, nq = 0, pos = 0, nvz = 0;  // K ring stage, Q loads, ring position, tails zeroed
+      const bool rope_k = p.rope_k != 0;     // K tiles rotated here (else given rotated)
+      int st = 0, nq = 0, pos = 0, nvz = 0;  // K ring stage, Q loads, V ring position, tails zeroed
       uint32_t ph = 0;
       bool ok = true;
       for (int k = 0; ok && k * u_step < n_units; ++k) {
@@ -600,14 +655,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(C::B_QR));
           }
-          for (int j = U.J0; ok && j < U.J1; ++j) {
+          for (int j = U.J0; ok && rope_k && j < U.J1; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_KF + st), ph, abort_flag, p.err));
             if (!ok) break;
             rotate_tile(smem + C::OFF_K + st * C::KV_BYTES, C::CHUNK_KV, j * kBN);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(C::B_KR + st));
-            if (++st == ST) {
+            if (++st == KST) {
               st = 0;
               ph ^= 1;
             }
@@ -616,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if constexpr (VARLEN) {
           if (warp == 10 && U.zero_v) {
-            const int st_t = (pos + U.j_tail - U.J0) % ST;  // ring stage of the tail tile
+            const int st_t = (pos + U.j_tail - U.J0) % VST;  // V ring stage of the tail tile
             const bool landed = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_VT), nvz & 1, abort_flag, p.err));
             ++nvz;
             if (!landed) break;
@@ -854,13 +909,15 @@ template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED, bool ROPE>
 cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p,
                        int B, cudaStream_t stream) {
   auto kern = prefill_fwd_kernel<D, CAUSAL, BF16, VARLEN, MASKED, ROPE>;
-  constexpr uint32_t smem = Cfg<D>::SMEM_BYTES;
+  constexpr uint32_t smem = Cfg<D, ROPE>::SMEM_BYTES;
   // setmaxnreg redistributes the registers the CTA was launched with; a split
   // larger than that pool would never be granted, so refuse to launch then.
   cudaFuncAttributes attr{};
   cudaError_t e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
-  if (attr.numRegs * kThreads < 256 * kSoftmaxRegs + 128 * kOtherRegs) return cudaErrorInvalidConfiguration;
+  constexpr int kThreads = kThreadsFor<ROPE>;
+  if (attr.numRegs * kThreads < 256 * kSoftmaxRegs + (kThreads - 256) * kOtherRegsFor<ROPE>)
+    return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(p.n_ctas);  // persistent: at most one CTA per SM (n_ctas <= number of SMs)

@@ -47,6 +47,7 @@ def main():
     ap.add_argument("--graph", type=int, default=0, help="decode: time a one-token serving step, eager vs CUDA graph")
     ap.add_argument("--rope", type=float, default=0.0, help="rotary embeddings of this base (0: none)")
     ap.add_argument("--rope-interleaved", type=int, default=0, help="rotary pairs (2c, 2c+1) instead of (c, c+D/2)")
+    ap.add_argument("--rope-rotated-keys", type=int, default=0, help="prefill: keys given already rotated")
     a = ap.parse_args()
     dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
     dev = torch.device("cuda", 0)
@@ -59,6 +60,7 @@ def main():
     stream = torch.cuda.current_stream()
     wl = a.window_left
     rope = dict(rope_theta=a.rope, rope_interleaved=bool(a.rope_interleaved))
+    rope_pre = dict(rope, rope_rotated_keys=bool(a.rope_rotated_keys))
     slopes = (torch.tensor([2.0 ** (-8.0 * (h + 1) / a.Hq) for h in range(a.Hq)], dtype=torch.float32, device=dev)
               if a.alibi else None)
     if a.kind == "prefill":
@@ -75,7 +77,7 @@ def main():
 
         def call():
             A.prefill(q, k, v, causal=bool(a.causal), out=o, lse_out=lse, window=(wl, -1), alibi_slopes=slopes,
-                      **rope)
+                      **rope_pre)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "varlen":
         B = a.B or 16

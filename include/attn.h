@@ -91,6 +91,12 @@ typedef enum {
  *                 on chip; the caller's tensors are not modified.
  *   rope_interleaved  which coordinates form pair c: 0 pairs (c, c + D/2)
  *                 (the "rotate half" layout), 1 pairs (2c, 2c + 1)
+ *   rope_rotated_keys  prefill with rope_theta > 0 only: 1 when the keys
+ *                 passed in are already rotated at their positions (for
+ *                 example read back from a cache written by kv_cache_write_ex
+ *                 with the same RoPE options); the kernel then rotates only
+ *                 the query tiles, which costs far less than rotating every K
+ *                 tile it reads.  0: the kernel rotates both.
  *   num_splits    decode only: 0 lets the library choose how many parts the
  *                 cache is split into; n in [1, 64] uses at most n (1: one
  *                 pass, no workspace).  More splits than the automatic choice
@@ -108,7 +114,8 @@ typedef enum {
  * written to).  The values are never rotated.
  *
  * Errors: a window below -1, a rope_theta that is negative or not finite, a
- * rope_interleaved other than 0 or 1, or a num_splits outside [0, 64] gives
+ * rope_interleaved or rope_rotated_keys other than 0 or 1, or a num_splits
+ * outside [0, 64] gives
  * ATTN_ERR_INVALID_ARG; slopes not 4-byte aligned give ATTN_ERR_ALIGNMENT.
  * The struct is read during the call; the slope array is read by the kernel,
  * so it must stay valid until the work enqueued on the stream has finished.
@@ -121,6 +128,7 @@ typedef struct {
     float rope_theta;
     int32_t rope_interleaved;
     int32_t num_splits;
+    int32_t rope_rotated_keys;
 } attn_options_t;
 
 /*

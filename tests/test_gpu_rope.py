@@ -313,3 +313,33 @@ def test_rope_paged_write_and_decode(page_size, inter):
     nz = [b for b in range(B) if lens[b] > 0]
     assert_close(np64(o)[nz], o_t[nz], np64(lse)[nz], l_t[nz], f"paged page_size={page_size}")
     assert (o[1] == 0).all() and torch.isneginf(lse[1]).all()  # the empty request
+
+
+@pytest.mark.parametrize("dt,D,causal,inter", [("bf16", 128, True, False), ("f16", 64, False, True)])
+def test_rope_prefill_with_rotated_keys(dt, D, causal, inter):
+    """rope_rotated_keys: the keys come in rotated (here: the oracle's rotation, rounded to 16 bits);
+    the kernel rotates only the queries."""
+    A = A_()
+    tdt = I.DTYPES[dt]
+    q, k, v = I.prefill_inputs(2, 8, 2, 400, 400, D, dt, seed=77 + D)
+    kr = rot(k, THETA, inter)
+    k_in = torch.from_numpy(kr).to(tdt)
+    o, lse = A.prefill(q.cuda(), k_in.cuda(), v.cuda(), causal=causal, rope_theta=THETA, rope_interleaved=inter,
+                       rope_rotated_keys=True)
+    torch.cuda.synchronize()
+    qh = round16(rot(q, THETA, inter), tdt)
+    o_t, l_t = oracle.attention(qh, np64(k_in), np64(v), causal, 1 / math.sqrt(D))
+    assert_close(o, o_t, lse, l_t, "rotated keys")
+
+
+def test_rope_prefill_over_rope_cache_equals_fused():
+    """The serving flow: keys written to a cache by the RoPE cache write, then a prefill over the
+    cache with rope_rotated_keys, equals the prefill that rotates the raw keys itself."""
+    A = A_()
+    B, Hq, Hkv, N, D = 2, 16, 4, 777, 128
+    q, k, v = I.prefill_inputs(B, Hq, Hkv, N, N, D, "bf16", seed=78)
+    kc, vc = _fill_rope_cache(k, v, [(0, 500), (500, N - 500)], THETA, False)
+    o_c, l_c = A.prefill(q.cuda(), kc, vc, causal=True, rope_theta=THETA, rope_rotated_keys=True)
+    o_f, l_f = A.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, rope_theta=THETA)
+    torch.cuda.synchronize()
+    assert_close(o_c, np64(o_f), l_c, np64(l_f), "cache flow vs fused")
