@@ -47,6 +47,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "attn_internal.h"
 #include "ptx.cuh"
 #include "rope.cuh"
@@ -72,14 +74,17 @@ constexpr int kUnlimited = 0x3fffffff;  // "no window bound" (large, yet safe to
 template <bool ROPE>
 constexpr int kOtherRegsFor = 96;
 
-template <int D, bool ROPE>
+template <int D, bool CAUSAL, bool ROPE>
 struct Cfg {
   static constexpr int KCH = D / 64;                  // 128-byte chunks along D
-  // Shared-memory stages of the K and V rings.  The rotary build at D = 128
-  // keeps a third K stage (K is loaded one tile ahead of V and rotated on chip,
-  // which must stay off the products' critical path); 3 x 32 KB of K + 2 x 32
-  // KB of V + 64 KB of Q still fit in 227 KB.
-  static constexpr int KST = (D == 128) ? (ROPE ? 3 : 2) : 3;
+  // Shared-memory stages of the K and V rings.  At D = 128 the causal and the
+  // rotary builds keep the K ring one stage deeper than the V ring and load K
+  // one tile ahead of V, so that K_{j+1} has landed (and, rotary, been rotated)
+  // before the MMA thread waits for it ahead of P0_j V_j; 3 x 32 KB of K + 2 x
+  // 32 KB of V + 64 KB of Q fit in 227 KB.  Measured A/B on one GPU: causal
+  // N = 8192 +2 %, while non-causal and the cross-attention workload ran 3-4 %
+  // slower (V then arrives later), so the plain non-causal build keeps 2 + 2.
+  static constexpr int KST = (D == 128) ? ((CAUSAL || ROPE) ? 3 : 2) : 3;
   static constexpr int VST = (D == 128) ? 2 : 3;
   static constexpr bool SPLIT = KST != VST;           // the two rings advance separately
   static constexpr uint32_t CHUNK_Q = kBM * 128;      // bytes of one 64-column chunk of a Q tile
@@ -106,8 +111,8 @@ struct Cfg {
   static constexpr int B_DONE = B_OD + 2;              // every MMA completed
   static constexpr int B_VZ = B_DONE + 1;              // variable length: V rows past the sequence zeroed
   static constexpr int B_VT = B_VZ + 1;                // variable length: the tail V tile has landed
-  static constexpr int B_QR = B_VT + 1;                // rotary: both Q tiles rotated
-  static constexpr int B_KR = B_QR + 1;                // + K stage: rotary: K tile rotated
+  static constexpr int B_QR = B_VT + 1;                // + Q tile (2): rotary: Q tile rotated
+  static constexpr int B_KR = B_QR + 2;                // + K stage: rotary: K tile rotated
   static constexpr int NBAR = B_KR + KST;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t OFF_ROPE = (OFF_MISC + 16 + 7) & ~7u;  // rotary turn steps, uint64 [D/2]
@@ -257,7 +262,7 @@ template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED, bool ROPE>
 __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillParams p) {
-  using C = Cfg<D, ROPE>;
+  using C = Cfg<D, CAUSAL, ROPE>;
   constexpr int KST = C::KST, VST = C::VST;
   extern __shared__ uint8_t smem_raw[];
 
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
     mbar_init(BAR(C::B_VZ), 1);
     mbar_init(BAR(C::B_VT), 1);
     mbar_init(BAR(C::B_QR), kRopeWarps<ROPE>);  // one arrival per rotating warp
+    mbar_init(BAR(C::B_QR + 1), kRopeWarps<ROPE>);
     for (int s = 0; s < KST; ++s) mbar_init(BAR(C::B_KR + s), kRopeWarps<ROPE>);
     *abort_flag = 0;
     fence_barrier_init();
@@ -461,6 +467,8 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
         int &vst = C::SPLIT ? vst_own : kst;
         uint32_t &vph = C::SPLIT ? vph_own : kph;
         uint32_t pf0 = 0, pf1 = 0;  // parities of the P-ready barriers
+        uint32_t q_par = 0;         // parity of the current unit's Q barriers
+        bool q1_wait = false;       // rotary: Q1's barrier not yet waited for in this unit
         int nq = 0, nvz = 0;        // units started; tail V tiles zeroed
         for (int k = 0; ok && k * u_step < n_units; ++k) {
           const int u = unit_index(k, u_first, u_step);
@@ -487,13 +495,28 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
             // instead on the all-done barrier's (never incomplete) phase before
             // its first, which passes at once.
             const bool has_kv = J0 < J1;
-            if (!(ok = mbar_wait(BAR(has_kv ? kQReady : C::B_DONE), has_kv ? (nq & 1) : 1u, abort_flag, p.err)))
+            q_par = nq & 1;
+            q1_wait = ROPE && has_kv;
+            if (!(ok = mbar_wait(BAR(has_kv ? kQReady : C::B_DONE), has_kv ? q_par : 1u, abort_flag, p.err)))
               break;
             nq += has_kv ? 1 : 0;
           } else {
-            if (!(ok = mbar_wait(BAR(kQReady), nq & 1, abort_flag, p.err))) break;
+            q_par = nq & 1;
+            q1_wait = ROPE;
+            if (!(ok = mbar_wait(BAR(kQReady), q_par, abort_flag, p.err))) break;
             ++nq;
           }
+          // Rotary: Q1 is signalled after Q0 and waited for before the first S1
+          // product, once per Q load.  A unit without S1 products waits for it
+          // at once: the next unit's Q can only be loaded after this unit's last
+          // S product, so waiting here keeps the barrier within one phase of
+          // this wait (a wait left to the unit's end could see it two ahead).
+          auto wait_q1 = [&]() -> bool {
+            if (!q1_wait) return true;
+            q1_wait = false;
+            return mbar_wait(BAR(C::B_QR + 1), q_par, abort_flag, p.err);
+          };
+          if (ROPE && lo1 >= hi1 && !(ok = wait_q1())) break;
           bool v_waited = false;  // V of tile j-1 already waited for (by P0 V)
           bool h1p = false;       // tile 1 uses KV tile j-1
           bool first0 = true, first1 = true;
@@ -526,6 +549,9 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
               tc_commit(BAR(C::B_VE + vsp));
             }
             if (h1) {
+              if constexpr (ROPE) {
+                if (!(ok = wait_q1())) break;
+              }
               tc_fence_after();
               issue_s(1, dq1, dk + kst * kStage16);
             }
@@ -601,7 +627,7 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
       constexpr int RPT = kBM * G / NT;     // consecutive rows per thread in a 128-row tile
       const int tid = threadIdx.x - 320;    // 0 .. NT - 1
       const int g = tid % G, rb = tid / G;  // this thread's pair group and row block
-      float c1[8], s1[8];                   // rotation by one position of the group's 8 pairs
+      float c1[8], s1[8];                   // cos and sin of one position's angle of the group's 8 pairs
       const uint64_t *fs = reinterpret_cast<const uint64_t *>(smem + C::OFF_ROPE);
       if constexpr (ROPE) {
 #pragma unroll
@@ -610,29 +636,34 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
       // Rotates rows [rb * RPT, rb * RPT + RPT) of the 128-row tile at `tile`
       // (64-column blocks CHUNK bytes apart, 128-byte swizzle); row r sits at
       // position pos0 + r.
-      auto rotate_tile = [&](uint8_t *tile, uint32_t chunk_bytes, int pos0) {
+      auto rotate_rows = [&](auto inter, uint8_t *tile, uint32_t chunk_bytes, int pos0) {
+        constexpr bool IL = decltype(inter)::value;
         int ca, cb;
+        rope_group_chunks<D, IL>(g, &ca, &cb);
         float cs[8], sn[8];
         const uint32_t r0 = static_cast<uint32_t>(rb * RPT);
 #pragma unroll
         for (int i = 0; i < 8; ++i) rope_sincos(static_cast<uint32_t>(pos0) + r0, fs[8 * g + i], &sn[i], &cs[i]);
-        if (p.rope_inter) rope_group_chunks<D, true>(g, &ca, &cb);
-        else rope_group_chunks<D, false>(g, &ca, &cb);
-        uint8_t *ta = tile + (ca >> 3) * chunk_bytes, *tb = tile + (cb >> 3) * chunk_bytes;
+        RopeWalk wk;
+        wk.start(cs, sn);
+        uint8_t *ta = tile + (ca >> 3) * chunk_bytes + r0 * 128, *tb = tile + (cb >> 3) * chunk_bytes + r0 * 128;
         ca &= 7;
         cb &= 7;
 #pragma unroll 2
         for (int rr = 0; rr < RPT; ++rr) {
-          const uint32_t r = r0 + rr;
-          uint4 *pa = reinterpret_cast<uint4 *>(ta + r * 128 + ((ca ^ (r & 7)) << 4));
-          uint4 *pb = reinterpret_cast<uint4 *>(tb + r * 128 + ((cb ^ (r & 7)) << 4));
+          const uint32_t sw = (r0 + rr) & 7;  // 128-byte swizzle of the row
+          uint4 *pa = reinterpret_cast<uint4 *>(ta + rr * 128 + ((ca ^ sw) << 4));
+          uint4 *pb = reinterpret_cast<uint4 *>(tb + rr * 128 + ((cb ^ sw) << 4));
           uint4 A = *pa, Bv = *pb;
-          if (p.rope_inter) rope_rotate_group<BF16, true>(A, Bv, cs, sn);
-          else rope_rotate_group<BF16, false>(A, Bv, cs, sn);
+          rope_rotate_group<BF16, IL>(A, Bv, wk.cs, wk.sn);
           *pa = A;
           *pb = Bv;
-          rope_step(cs, sn, c1, s1);
+          wk.step(c1, s1);
         }
+      };
+      auto rotate_tile = [&](uint8_t *tile, uint32_t chunk_bytes, int pos0) {
+        if (p.rope_inter) rotate_rows(std::true_type{}, tile, chunk_bytes, pos0);
+        else rotate_rows(std::false_type{}, tile, chunk_bytes, pos0);
       };
       const bool rope_k = p.rope_k != 0;     // K tiles rotated here (else given rotated)
       int st = 0, nq = 0, pos = 0, nvz = 0;  // K ring stage, Q loads, V ring position, tails zeroed
@@ -649,11 +680,16 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_Q), nq & 1, abort_flag, p.err));
             ++nq;
             if (!ok) break;
+            // Tile 0 first, signalled on its own: the unit's first product (S0)
+            // needs only Q0 and can run while Q1 is rotated.
             rotate_tile(smem + C::OFF_Q, C::CHUNK_Q, U.q0);
-            rotate_tile(smem + C::OFF_Q + C::QT_BYTES, C::CHUNK_Q, U.q0 + kBM);
             fence_proxy_async_smem();  // the tensor core reads the rotated rows
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(C::B_QR));
+            rotate_tile(smem + C::OFF_Q + C::QT_BYTES, C::CHUNK_Q, U.q0 + kBM);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C::B_QR + 1));
           }
           for (int j = U.J0; ok && rope_k && j < U.J1; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_KF + st), ph, abort_flag, p.err));
@@ -909,7 +945,7 @@ template <int D, bool CAUSAL, bool BF16, bool VARLEN, bool MASKED, bool ROPE>
 cudaError_t launch_one(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p,
                        int B, cudaStream_t stream) {
   auto kern = prefill_fwd_kernel<D, CAUSAL, BF16, VARLEN, MASKED, ROPE>;
-  constexpr uint32_t smem = Cfg<D, ROPE>::SMEM_BYTES;
+  constexpr uint32_t smem = Cfg<D, CAUSAL, ROPE>::SMEM_BYTES;
   // setmaxnreg redistributes the registers the CTA was launched with; a split
   // larger than that pool would never be granted, so refuse to launch then.
   cudaFuncAttributes attr{};

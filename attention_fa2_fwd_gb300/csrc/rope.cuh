@@ -45,10 +45,12 @@ __device__ __forceinline__ uint32_t rope_pack(float a, float b) {
   }
 }
 
-// Rotates the 8 pairs of one group held in two 16-byte chunks.  Rotate-half
-// layout: word k of chunk A holds x_a of pairs 2k, 2k+1 and word k of chunk B
-// their x_b.  Interleaved layout: word k of A holds pair k (x_a, x_b) and word
-// k of B pair 4 + k.  cs[i], sn[i]: cos and sin of pair i of the group.
+// Rotates the 8 pairs of one group held in two 16-byte chunks, in scalar
+// fp32 (one multiply and one fused multiply-add per coordinate; negations fold
+// into the FMA).  Rotate-half layout: word k of chunk A holds x_a of pairs
+// 2k, 2k+1 and word k of chunk B their x_b.  Interleaved layout: word k of A
+// holds pair k (x_a, x_b) and word k of B pair 4 + k.  cs[i], sn[i]: cos and
+// sin of pair i of the group.
 template <bool BF16, bool INTERLEAVED>
 __device__ __forceinline__ void rope_rotate_group(uint4 &A, uint4 &B, const float (&cs)[8], const float (&sn)[8]) {
   uint32_t *a = reinterpret_cast<uint32_t *>(&A);
@@ -57,13 +59,9 @@ __device__ __forceinline__ void rope_rotate_group(uint4 &A, uint4 &B, const floa
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float2 xa = rope_unpack<BF16>(a[k]), xb = rope_unpack<BF16>(b[k]);
-      const uint64_t c2 = pack_f2(cs[2 * k], cs[2 * k + 1]), s2 = pack_f2(sn[2 * k], sn[2 * k + 1]);
-      const uint64_t ns2 = pack_f2(-sn[2 * k], -sn[2 * k + 1]);
-      const uint64_t va = pack_f2(xa.x, xa.y), vb = pack_f2(xb.x, xb.y);
-      const float2 ya = unpack_f2(ffma_f2(va, c2, fmul_f2(vb, ns2)));  // x_a c - x_b s
-      const float2 yb = unpack_f2(ffma_f2(vb, c2, fmul_f2(va, s2)));   // x_b c + x_a s
-      a[k] = rope_pack<BF16>(ya.x, ya.y);
-      b[k] = rope_pack<BF16>(yb.x, yb.y);
+      const float c0 = cs[2 * k], s0 = sn[2 * k], c1 = cs[2 * k + 1], s1 = sn[2 * k + 1];
+      a[k] = rope_pack<BF16>(fmaf(xa.x, c0, -xb.x * s0), fmaf(xa.y, c1, -xb.y * s1));
+      b[k] = rope_pack<BF16>(fmaf(xb.x, c0, xa.x * s0), fmaf(xb.y, c1, xa.y * s1));
     }
   } else {
 #pragma unroll
@@ -73,10 +71,7 @@ __device__ __forceinline__ void rope_rotate_group(uint4 &A, uint4 &B, const floa
       for (int k = 0; k < 4; ++k) {
         const int i = 4 * h + k;
         const float2 x = rope_unpack<BF16>(w[k]);
-        // (x_a', x_b') = (x_a, x_b) c + (x_b, x_a) (-s, s)
-        const float2 y = unpack_f2(
-            ffma_f2(pack_f2(x.x, x.y), pack_f2(cs[i], cs[i]), fmul_f2(pack_f2(x.y, x.x), pack_f2(-sn[i], sn[i]))));
-        w[k] = rope_pack<BF16>(y.x, y.y);
+        w[k] = rope_pack<BF16>(fmaf(x.x, cs[i], -x.y * sn[i]), fmaf(x.y, cs[i], x.x * sn[i]));
       }
     }
   }
@@ -95,20 +90,30 @@ __device__ __forceinline__ void rope_group_chunks(int g, int *ca, int *cb) {
   }
 }
 
-// Advances (cs, sn) of 8 pairs by one position: angle + step.
-__device__ __forceinline__ void rope_step(float (&cs)[8], float (&sn)[8], const float (&c1)[8], const float (&s1)[8]) {
+// (cos, sin) of 8 pairs along consecutive positions: each step turns them by
+// the angle of one position (cos(a + t) = cos a cos t - sin a sin t, sin(a + t)
+// = sin a cos t + cos a sin t), a rotation, so the errors stay near one
+// rounding per step (a thread walks at most 16 rows).  (A three-term
+// recurrence, one FMA per value, was tried: its errors grow quadratically with
+// the steps and visibly moved 16-bit roundings.)
+struct RopeWalk {
+  float cs[8], sn[8];  // at the current position
+  __device__ __forceinline__ void start(const float (&cs0)[8], const float (&sn0)[8]) {
 #pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    const uint64_t c = pack_f2(cs[i], cs[i + 1]), s = pack_f2(sn[i], sn[i + 1]);
-    const uint64_t cc1 = pack_f2(c1[i], c1[i + 1]), ss1 = pack_f2(s1[i], s1[i + 1]);
-    const uint64_t nss1 = pack_f2(-s1[i], -s1[i + 1]);
-    const float2 cn = unpack_f2(ffma_f2(c, cc1, fmul_f2(s, nss1)));  // cos(a + d) = cos a cos d - sin a sin d
-    const float2 sv = unpack_f2(ffma_f2(s, cc1, fmul_f2(c, ss1)));   // sin(a + d) = sin a cos d + cos a sin d
-    cs[i] = cn.x;
-    cs[i + 1] = cn.y;
-    sn[i] = sv.x;
-    sn[i + 1] = sv.y;
+    for (int i = 0; i < 8; ++i) {
+      cs[i] = cs0[i];
+      sn[i] = sn0[i];
+    }
   }
-}
+  // c1, s1: cos and sin of one position's angle.
+  __device__ __forceinline__ void step(const float (&c1)[8], const float (&s1)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float nc = fmaf(cs[i], c1[i], -sn[i] * s1[i]), ns = fmaf(sn[i], c1[i], cs[i] * s1[i]);
+      cs[i] = nc;
+      sn[i] = ns;
+    }
+  }
+};
 
 }  // namespace attn
