@@ -369,8 +369,118 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": n_pass * (1 + 1 + (2 if splits > 1 else 1)),
         "clocks": clocks,
     }
+    if args.also and world == 1:
+        sampler2 = ClockSampler(local_rank)
+        sampler2.start()
+        line["also_measured"] = {"results": measure_also(A, dev, stream, flush, peaks),
+                                 "how": "CUDA events on the launching stream, 3 warm-ups, median of 10 "
+                                        "(backward 5), L2 flushed before each timed call",
+                                 "clocks": sampler2.stop()}
     data = {"prefill": (q, k, v, o, lse), "decode": (qd, kc, vc, od, lsed, Dc["L"])}
     return line, data
+
+
+# --------------------------------------------------------------------------- secondary workloads
+
+def measure_also(A, dev, stream, flush, peaks, reps=10):
+    """Event-timed secondary measurements of the same library (rank 0, one GPU):
+    the D=64 causal prefill, the cross-attention workload at D=128 and 64,
+    the causal prefill with rotary embeddings (keys given rotated, and rotated
+    in the kernel), the backward pass, and the B=2 one-token decode step
+    replayed from a CUDA graph.  Each kernel is timed with CUDA events on the
+    launching stream after 3 warm-ups, the L2 flushed before every timed call;
+    the median is reported against the measured peaks.  Returns a dict."""
+    import torch
+
+    import attention_fa2_fwd_gb300.inputs as I
+
+    g = torch.Generator(device=dev).manual_seed(7)
+
+    def randn(*shape, std=1.0):
+        return (torch.randn(shape, generator=g, device=dev, dtype=torch.float32) * std).to(torch.bfloat16)
+
+    def timed(fn, n=reps):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    def tf_line(name, flops, ms):
+        v = flops / (ms * 1e-3) / 1e12
+        return {"workload": name, "value": round(v, 1), "unit": "TFLOPS", "ms": round(ms, 4),
+                "frac": round(v / peaks["bf16_tflops"], 4)}
+
+    out = []
+    P = PREFILL
+    # D=64 causal prefill, otherwise the headline sizes
+    q, k, v = randn(P["B"], P["Hq"], P["N"], 64), randn(P["B"], P["Hkv"], P["N"], 64), randn(P["B"], P["Hkv"], P["N"], 64)
+    o = torch.empty_like(q)
+    ms = timed(lambda: A.prefill(q, k, v, causal=True, out=o))
+    out.append(tf_line("gqa_causal_prefill_b2_hq32_hkv8_n8192_d64_bf16", prefill_flops(P["B"], P["Hq"], P["N"], 64, True), ms))
+    del q, k, v, o
+    # cross-attention workload: (B,N,H,D) memory, K variance 2, V ~ U(-1,1)
+    for D in (128, 64):
+        w = I.CROSS[D]
+        q = I.to_layout(randn(w.B, w.Hq, w.Nq, D), w.layout)
+        k = I.to_layout(randn(w.B, w.Hkv, w.Nkv, D, std=2 ** 0.5), w.layout)
+        v = I.to_layout(((torch.rand((w.B, w.Hkv, w.Nkv, D), generator=g, device=dev) * 2 - 1).to(torch.bfloat16)),
+                        w.layout)
+        o = I.to_layout(torch.empty_like(q), w.layout)
+        ms = timed(lambda: A.prefill(q, k, v, causal=False, out=o))
+        out.append(tf_line(w.name, w.flops, ms))
+    # rotary embeddings on the headline workload
+    q, k, v = randn(P["B"], P["Hq"], P["N"], P["D"]), randn(P["B"], P["Hkv"], P["N"], P["D"]), randn(P["B"], P["Hkv"], P["N"], P["D"])
+    o = torch.empty_like(q)
+    lse = torch.empty((P["B"], P["Hq"], P["N"]), dtype=torch.float32, device=dev)
+    fl = prefill_flops(**P)
+    ms = timed(lambda: A.prefill(q, k, v, causal=True, out=o, lse_out=lse, rope_theta=10000.0, rope_rotated_keys=True))
+    out.append(tf_line("gqa_causal_prefill_n8192_d128 + RoPE (keys given rotated)", fl, ms))
+    ms = timed(lambda: A.prefill(q, k, v, causal=True, out=o, lse_out=lse, rope_theta=10000.0))
+    out.append(tf_line("gqa_causal_prefill_n8192_d128 + RoPE (keys rotated in the kernel)", fl, ms))
+    # backward of the headline workload (2.5x the forward's FLOPs: S, dP, dV, dK, dQ products)
+    A.prefill(q, k, v, causal=True, out=o, lse_out=lse)
+    dout = randn(P["B"], P["Hq"], P["N"], P["D"])
+    ws = torch.empty((A.attn_bwd_workspace_size(P["B"], P["Hq"], P["N"]) + 3) // 4, dtype=torch.float32, device=dev)
+    ms = timed(lambda: A.backward(q, k, v, o, lse, dout, causal=True, workspace=ws), n=max(3, reps // 2))
+    out.append(tf_line("gqa_causal_backward_b2_hq32_hkv8_n8192_d128_bf16 (2.5x forward FLOPs)", 2.5 * fl, ms))
+    del q, k, v, o, lse, dout, ws
+    # B=2 one-token decode step (cache write + decode) replayed from a CUDA graph
+    Dc = dict(DECODE, B=2)
+    kc, vc = randn(2, Dc["Hkv"], Dc["L"], Dc["D"]), randn(2, Dc["Hkv"], Dc["L"], Dc["D"])
+    kn, vn = randn(2, Dc["Hkv"], 1, Dc["D"]), randn(2, Dc["Hkv"], 1, Dc["D"])
+    qd = randn(2, Dc["Hq"], Dc["D"])
+    od = torch.empty_like(qd)
+    wsd = A.decode_workspace(2, Dc["Hq"], Dc["Hkv"], Dc["D"], dev)
+
+    def step():
+        A.write_kv_cache(kc, vc, kn, vn, Dc["L"] - 1)
+        A.decode(qd, kc, vc, Dc["L"], out=od, return_lse=False, workspace=wsd)
+    step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    n_rep = 50
+    ms = timed(lambda: [graph.replay() for _ in range(n_rep)]) / n_rep
+    kvb = decode_bytes(2, Dc["Hkv"], Dc["L"], Dc["D"])
+    out.append({"workload": "decode_step_b2_hq32_hkv8_l8192_d128_bf16, CUDA graph replay (50 steps back to back)",
+                "value": round(kvb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "us_per_step": round(ms * 1e3, 2),
+                "frac": round(kvb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)})
+    A.check_device_error()
+    return out
 
 
 # --------------------------------------------------------------------------- oracle (CPU)
@@ -569,6 +679,8 @@ def main():
                          "clock sampler: 20 steps x 20 passes is about 0.45 s)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--no-also", dest="also", action="store_false",
+                    help="skip the secondary measurements (D=64, cross-attention, RoPE, backward, B=2 decode step)")
     ap.add_argument("--oracle-configs", action="store_true",
                     help="with --impl reference: time the oracle on every parity configuration (a few minutes)")
     args = ap.parse_args()
