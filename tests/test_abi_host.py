@@ -264,6 +264,12 @@ OPTION_CALLS = {
     "decode_paged": lambda o: A.attn_fwd_decode_paged_ex(
         P, P, P, P, None, A.ATTN_BF16, 2, 32, 8, 128, 100, 16, P, 64, 64, P, 1000, contig(2, 32, 1, 128),
         contig(100, 8, 16, 128), contig(100, 8, 16, 128), contig(2, 32, 1, 128), 0.088, P, 1 << 30, o, None),
+    "cache_write": lambda o: A.kv_cache_write_ex(
+        P, P, P, P, A.ATTN_BF16, 2, 8, 1, 128, 10, 256, contig(2, 8, 256, 128), contig(2, 8, 256, 128),
+        contig(2, 8, 1, 128), contig(2, 8, 1, 128), o, None),
+    "cache_write_paged": lambda o: A.kv_cache_write_paged_ex(
+        P, P, P, P, A.ATTN_BF16, 2, 8, 1, 128, 100, 16, P, 64, 64, P, contig(100, 8, 16, 128),
+        contig(100, 8, 16, 128), contig(2, 8, 1, 128), contig(2, 8, 1, 128), o, None),
 }
 
 
@@ -279,6 +285,8 @@ OPTION_CALLS = {
     ((-1, -1, None, 10000.0, 2, 0), A.ATTN_ERR_INVALID_ARG),
     ((-1, -1, None, 0.0, 0, -1), A.ATTN_ERR_INVALID_ARG),
     ((-1, -1, None, 0.0, 0, 65), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, None, 10000.0, 0, 0, 2), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, None, 10000.0, 0, 0, -1), A.ATTN_ERR_INVALID_ARG),
 ])
 def test_option_errors(lib, call, opts, code):
     """Options are validated with the other arguments, before any CUDA call."""
@@ -353,3 +361,23 @@ def test_noalloc_decode_checks_arguments_before_the_scratch_size(lib):
         assert A.attn_fwd_decode_noalloc(**a) == code, kw
         ws = {k: v for k, v in a.items()}
         assert A.attn_fwd_decode(**ws, workspace=P, workspace_bytes=1 << 30) == code, kw
+
+
+def test_make_options_rope_and_splits():
+    o = A.make_options(rope_theta=10000.0, rope_interleaved=True, num_splits=3, rope_rotated_keys=True)
+    assert (o.window_left, o.window_right, o.alibi_slopes) == (-1, -1, None)
+    assert (o.rope_theta, o.rope_interleaved, o.num_splits, o.rope_rotated_keys) == (10000.0, 1, 3, 1)
+    assert A.make_options(num_splits=0, rope_theta=0.0) is None
+
+
+def test_options_struct_matches_the_header():
+    """The ctypes struct has the fields, order and size of attn_options_t."""
+    import ctypes
+    names = [f[0] for f in A.AttnOptions._fields_]
+    assert names == ["window_left", "window_right", "alibi_slopes", "rope_theta", "rope_interleaved", "num_splits",
+                     "rope_rotated_keys"]
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct {"):text.index("} attn_options_t;")]
+    declared = re.findall(r"\b([a-z_]+);", body)
+    assert declared == names
+    assert ctypes.sizeof(A.AttnOptions) == 32  # 4 + 4 + 8 + 4 + 4 + 4 + 4 on LP64
