@@ -77,14 +77,16 @@ constexpr int kOtherRegsFor = 96;
 template <int D, bool CAUSAL, bool ROPE>
 struct Cfg {
   static constexpr int KCH = D / 64;                  // 128-byte chunks along D
-  // Shared-memory stages of the K and V rings.  At D = 128 the causal and the
-  // rotary builds keep the K ring one stage deeper than the V ring and load K
-  // one tile ahead of V, so that K_{j+1} has landed (and, rotary, been rotated)
-  // before the MMA thread waits for it ahead of P0_j V_j; 3 x 32 KB of K + 2 x
-  // 32 KB of V + 64 KB of Q fit in 227 KB.  Measured A/B on one GPU: causal
-  // N = 8192 +2 %, while non-causal and the cross-attention workload ran 3-4 %
-  // slower (V then arrives later), so the plain non-causal build keeps 2 + 2.
-  static constexpr int KST = (D == 128) ? ((CAUSAL || ROPE) ? 3 : 2) : 3;
+  // Shared-memory stages of the K and V rings.  The causal and the rotary
+  // builds keep the K ring one stage deeper than the V ring and load K one
+  // tile ahead of V, so that K_{j+1} has landed (and, rotary, been rotated)
+  // before the MMA thread waits for it ahead of P0_j V_j (D = 128: 3 x 32 KB of
+  // K + 2 x 32 KB of V + 64 KB of Q fit in 227 KB).  Measured A/B on one GPU:
+  // causal N = 8192 +2 % at D = 128 and +1-2 % at D = 64 (+2-6 % at N = 2048),
+  // while at D = 128 non-causal and the cross-attention workload ran 3-4 %
+  // slower (V then arrives later), so the plain non-causal builds keep equal
+  // rings.
+  static constexpr int KST = (D == 128) ? ((CAUSAL || ROPE) ? 3 : 2) : ((CAUSAL || ROPE) ? 4 : 3);
   static constexpr int VST = (D == 128) ? 2 : 3;
   static constexpr bool SPLIT = KST != VST;           // the two rings advance separately
   static constexpr uint32_t CHUNK_Q = kBM * 128;      // bytes of one 64-column chunk of a Q tile

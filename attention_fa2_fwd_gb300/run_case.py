@@ -48,6 +48,7 @@ def main():
     ap.add_argument("--rope", type=float, default=0.0, help="rotary embeddings of this base (0: none)")
     ap.add_argument("--rope-interleaved", type=int, default=0, help="rotary pairs (2c, 2c+1) instead of (c, c+D/2)")
     ap.add_argument("--rope-rotated-keys", type=int, default=0, help="prefill: keys given already rotated")
+    ap.add_argument("--num-splits", type=int, default=0, help="decode: force at most this many KV splits (0: auto)")
     a = ap.parse_args()
     dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
     dev = torch.device("cuda", 0)
@@ -154,11 +155,13 @@ def main():
         od = torch.empty_like(qd)
         lsed = torch.empty((B, a.Hq), dtype=torch.float32, device=dev)
         ws = A.decode_workspace(B, a.Hq, a.Hkv, a.D, dev)
+        if a.num_splits:
+            ws = torch.empty(B * a.Hq * a.num_splits * (a.D + 1), dtype=torch.float32, device=dev)
         work = 2.0 * B * a.Hkv * (min(a.L, wl + 1) if wl >= 0 else a.L) * a.D * 2
 
         def call():
             A.decode(qd, kc, vc, a.L, out=od, lse_out=lsed, workspace=ws, window_left=wl, alibi_slopes=slopes,
-                     **rope)
+                     num_splits=a.num_splits, **rope)
         unit, scale = "GB/s", 1e9
     if a.graph and a.kind in ("decode", "decode_paged"):
         # one serving step: write one new token per request, then decode
