@@ -23,6 +23,12 @@ the ones in common use:
 * Decode: the single query sits at position cache_len - 1, so key t is visible
   iff t >= cache_len - 1 - window_left, and its bias is
   -slope_h * (cache_len - 1 - t).
+* Custom masks as per-query-row key ranges (a reading of the pages' "custom
+  masks", in the general form that covers block-diagonal, document and
+  prefix masks): row i of batch b sees only keys j with
+  kv_ranges[b][i][0] <= j < kv_ranges[b][i][1], in addition to the other
+  bounds; for packed variable-length batches the ranges are per packed row and
+  count keys from the start of the row's own sequence.
 * A row with no visible key gets O = 0 and LSE = -inf (the convention of the
   plain oracle for empty sequences).
 
@@ -43,11 +49,15 @@ def _f64(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
 
 
-def visible(Nq: int, Nkv: int, causal: bool, window_left: int = -1, window_right: int = -1) -> np.ndarray:
-    """Boolean (Nq, Nkv): key j visible to query row i."""
+def visible(Nq: int, Nkv: int, causal: bool, window_left: int = -1, window_right: int = -1,
+            kv_range=None) -> np.ndarray:
+    """Boolean (Nq, Nkv): key j visible to query row i (kv_range: optional (Nq, 2) [lo, hi) per row)."""
     i = np.arange(Nq)[:, None]
     j = np.arange(Nkv)[None, :]
     keep = np.ones((Nq, Nkv), dtype=bool)
+    if kv_range is not None:
+        kr = np.asarray(kv_range, dtype=np.int64).reshape(Nq, 2)
+        keep &= (j >= kr[:, 0:1]) & (j < kr[:, 1:2])
     if causal:
         keep &= j <= i
     if window_left >= 0:
@@ -74,13 +84,17 @@ def _softmax_rows(s: np.ndarray, v: np.ndarray):
 
 
 def attention_masked(q, k, v, causal: bool, scale: float, window_left: int = -1, window_right: int = -1,
-                     alibi_slopes=None):
-    """O (B,H_q,N_q,D) and LSE (B,H_q,N_q) of windowed / ALiBi attention; K, V are (B,H_kv,N_kv,D)."""
+                     alibi_slopes=None, kv_ranges=None):
+    """O (B,H_q,N_q,D) and LSE (B,H_q,N_q) of windowed / ALiBi / key-range attention; K, V are (B,H_kv,N_kv,D).
+
+    kv_ranges: optional (B, N_q, 2) int array, [lo, hi) of the keys each query row may see.
+    """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Nq, D = q.shape
     _, Hkv, Nkv, _ = k.shape
     group = Hq // Hkv
-    keep = visible(Nq, Nkv, causal, window_left, window_right)
+    keeps = [visible(Nq, Nkv, causal, window_left, window_right,
+                     None if kv_ranges is None else np.asarray(kv_ranges)[b]) for b in range(B)]
     dist = np.abs(np.arange(Nq)[:, None] - np.arange(Nkv)[None, :]).astype(np.float64)
     slopes = None if alibi_slopes is None else np.asarray(alibi_slopes, dtype=np.float64)
     o = np.zeros((B, Hq, Nq, D))
@@ -91,7 +105,7 @@ def attention_masked(q, k, v, causal: bool, scale: float, window_left: int = -1,
             s = scale * (q[b, h] @ k[b, hk].T)
             if slopes is not None:
                 s = s - slopes[h] * dist
-            s = np.where(keep, s, -np.inf)
+            s = np.where(keeps[b], s, -np.inf)
             o[b, h], lse[b, h] = _softmax_rows(s, v[b, hk])
     return o, lse
 
@@ -150,10 +164,11 @@ def decode_paged_masked(q, k_pages, v_pages, block_table, cache_lens, scale: flo
 
 
 def prefill_varlen_masked(q, k, v, cu_q, cu_k, causal: bool, scale: float, window_left: int = -1,
-                          window_right: int = -1, alibi_slopes=None):
+                          window_right: int = -1, alibi_slopes=None, kv_ranges=None):
     """``attention_masked`` of each packed sequence with positions counted from its own start.
 
-    q: (total_q,H_q,D); k, v: (total_k,H_kv,D).  Returns O (total_q,H_q,D), LSE (H_q,total_q).
+    q: (total_q,H_q,D); k, v: (total_k,H_kv,D); kv_ranges: optional (total_q, 2), per packed row,
+    keys counted from the row's sequence start.  Returns O (total_q,H_q,D), LSE (H_q,total_q).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     total_q, Hq, D = q.shape
@@ -166,7 +181,8 @@ def prefill_varlen_masked(q, k, v, cu_q, cu_k, causal: bool, scale: float, windo
         qb = q[qs:qe].transpose(1, 0, 2)[None]
         kb = k[ks:ke].transpose(1, 0, 2)[None]
         vb = v[ks:ke].transpose(1, 0, 2)[None]
-        ob, lb = attention_masked(qb, kb, vb, causal, scale, window_left, window_right, alibi_slopes)
+        kr = None if kv_ranges is None else np.asarray(kv_ranges)[qs:qe][None]
+        ob, lb = attention_masked(qb, kb, vb, causal, scale, window_left, window_right, alibi_slopes, kr)
         o[qs:qe] = ob[0].transpose(1, 0, 2)
         lse[:, qs:qe] = lb[0]
     return o, lse

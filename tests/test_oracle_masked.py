@@ -15,6 +15,10 @@
   left and right of i are two such problems merged by their LSEs.
 * Decode is the last row of a causal prefill of cache_len rows, and paged
   decode is decode over the gathered rows for any page order.
+* Per-row key ranges: each row equals the C oracle's decode over the keys of
+  its range (intersected with the causal bound; empty ranges give 0 / -inf);
+  full ranges are plain attention; block-diagonal ranges over one packed
+  batch equal the C oracle's variable-length attention of the blocks.
 Every planted mistake in ``oracle/masked.py`` (MUTANTS) fails at least one pin.
 """
 from __future__ import annotations
@@ -254,11 +258,95 @@ def check_varlen_equal_lengths_is_dense_batch(mk):
         _close(l, l_ref.transpose(1, 0, 2).reshape(Hq, B * N), "varlen LSE")
 
 
+def _random_ranges(rng, B, Nq, Nkv):
+    lo = rng.integers(0, Nkv + 1, size=(B, Nq))
+    hi = rng.integers(0, Nkv + 1, size=(B, Nq))
+    lo, hi = np.minimum(lo, hi), np.maximum(lo, hi)
+    r = np.stack([lo, hi], axis=-1)
+    r[:, 0] = (0, Nkv)                    # a full row
+    r[:, min(1, Nq - 1)] = (Nkv // 2, Nkv // 2)  # an empty row
+    return r
+
+
+def check_range_rows_are_decode_over_slice(mk):
+    scale = 0.7
+    for causal in (False, True):
+        for Nq, Nkv in ((9, 9), (5, 13), (16, 7)):
+            q, k, v = _qkv(2, 4, 2, Nq, Nkv, 3, "ranges", causal, Nq, Nkv)
+            kr = _random_ranges(_rng("kr", causal, Nq, Nkv), 2, Nq, Nkv)
+            o, l = mk.attention_masked(q, k, v, causal, scale, kv_ranges=kr)
+            for b in range(2):
+                for i in range(Nq):
+                    lo, hi = int(kr[b, i, 0]), int(kr[b, i, 1])
+                    if causal:
+                        hi = min(hi, i + 1)
+                    if lo >= hi:
+                        assert (o[b, :, i] == 0).all() and np.isneginf(l[b, :, i]).all(), f"empty range row {i}"
+                        continue
+                    o_ref, l_ref = oracle.decode(q[b:b + 1, :, i], k[b:b + 1, :, lo:hi], v[b:b + 1, :, lo:hi],
+                                                 hi - lo, scale)
+                    _close(o[b, :, i], o_ref[0], f"O b={b} row {i} range [{lo},{hi}) causal={causal}")
+                    _close(l[b, :, i], l_ref[0], f"LSE b={b} row {i} range [{lo},{hi}) causal={causal}")
+
+
+def check_full_ranges_are_plain(mk):
+    q, k, v = _qkv(2, 4, 2, 11, 17, 3, "fullranges")
+    kr = np.zeros((2, 11, 2), dtype=np.int64)
+    kr[..., 1] = 17
+    for causal in (False, True):
+        o, l = mk.attention_masked(q, k, v, causal, 0.5, kv_ranges=kr)
+        o_ref, l_ref = oracle.attention(q, k, v, causal, 0.5)
+        _close(o, o_ref, "full ranges O")
+        _close(l, l_ref, "full ranges LSE")
+
+
+def check_block_diagonal_ranges_are_varlen(mk):
+    """Documents of lengths 4, 1, 6 packed in one row of 11: each query sees only its own document."""
+    lens = [4, 1, 6]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    N = int(cu[-1])
+    q, k, v = _qkv(1, 4, 2, N, N, 3, "blockdiag")
+    kr = np.zeros((1, N, 2), dtype=np.int64)
+    for d in range(len(lens)):
+        kr[0, cu[d]:cu[d + 1]] = (cu[d], cu[d + 1])
+    for causal in (False, True):
+        o, l = mk.attention_masked(q, k, v, False, 0.8, kv_ranges=kr) if not causal else \
+            mk.attention_masked(q, k, v, True, 0.8, kv_ranges=kr)
+        o_ref, l_ref = oracle.prefill_varlen(q[0].transpose(1, 0, 2), k[0].transpose(1, 0, 2),
+                                             v[0].transpose(1, 0, 2), cu, cu, causal, 0.8)
+        _close(o[0], o_ref.transpose(1, 0, 2), f"block-diagonal O causal={causal}")
+        _close(l[0], l_ref, f"block-diagonal LSE causal={causal}")
+
+
+def check_varlen_ranges_count_from_sequence_start(mk):
+    lq, lk = [5, 3], [7, 4]
+    cq, ck = np.concatenate([[0], np.cumsum(lq)]), np.concatenate([[0], np.cumsum(lk)])
+    r = _rng("varlen-ranges")
+    q, k, v = r.normal(size=(8, 4, 3)), r.normal(size=(11, 2, 3)), r.normal(size=(11, 2, 3))
+    kr = np.stack([r.integers(0, 3, size=8), r.integers(3, 8, size=8)], axis=1)
+    kr[5:, 1] = np.minimum(kr[5:, 1], 4)
+    o, l = mk.prefill_varlen_masked(q, k, v, cq, ck, False, 0.6, kv_ranges=kr)
+    for b in range(2):
+        ob, lb = mk.attention_masked(q[cq[b]:cq[b + 1]].transpose(1, 0, 2)[None], k[ck[b]:ck[b + 1]].transpose(1, 0, 2)[None],
+                                     v[ck[b]:ck[b + 1]].transpose(1, 0, 2)[None], False, 0.6,
+                                     kv_ranges=kr[cq[b]:cq[b + 1]][None])
+        _close(o[cq[b]:cq[b + 1]], ob[0].transpose(1, 0, 2), f"varlen ranges O seq {b}")
+        _close(l[:, cq[b]:cq[b + 1]], lb[0], f"varlen ranges LSE seq {b}")
+    # and against the slice definition for one row of the second sequence
+    i = 6
+    lo, hi = int(kr[i, 0]), int(kr[i, 1])
+    o_ref, l_ref = oracle.decode(q[i][None], k[ck[1] + lo:ck[1] + hi].transpose(1, 0, 2)[None],
+                                 v[ck[1] + lo:ck[1] + hi].transpose(1, 0, 2)[None], hi - lo, 0.6)
+    _close(o[i], o_ref[0], "varlen range row O")
+
+
 CHECKS = [check_unbounded_window_is_plain, check_band_rows_are_decode_over_slice, check_identity_window,
           check_alibi_zero_slope_is_plain, check_alibi_identical_keys_closed_form,
           check_alibi_causal_is_plain_with_extra_dimension, check_alibi_window_two_sided_by_merge,
           check_decode_is_last_prefill_row, check_decode_alibi_extra_dimension,
-          check_paged_is_decode_over_gathered_rows, check_varlen_equal_lengths_is_dense_batch]
+          check_paged_is_decode_over_gathered_rows, check_varlen_equal_lengths_is_dense_batch,
+          check_range_rows_are_decode_over_slice, check_full_ranges_are_plain, check_block_diagonal_ranges_are_varlen,
+          check_varlen_ranges_count_from_sequence_start]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=[c.__name__ for c in CHECKS])
@@ -282,6 +370,13 @@ MUTANTS = {
     "empty rows uniform": ("rows = np.isfinite(s).any(axis=1)", "rows = np.ones(n, dtype=bool)"),
     "paged row index": ("rows = [(int(block_table[b][t // page_size]), t % page_size)",
                         "rows = [(int(block_table[b][t // page_size]), (t + 1) % page_size)"),
+    "range lower bound off by one": ("keep &= (j >= kr[:, 0:1]) & (j < kr[:, 1:2])",
+                                     "keep &= (j > kr[:, 0:1]) & (j < kr[:, 1:2])"),
+    "range upper bound inclusive": ("keep &= (j >= kr[:, 0:1]) & (j < kr[:, 1:2])",
+                                    "keep &= (j >= kr[:, 0:1]) & (j <= kr[:, 1:2])"),
+    "ranges of batch 0 for every batch": ("None if kv_ranges is None else np.asarray(kv_ranges)[b]",
+                                          "None if kv_ranges is None else np.asarray(kv_ranges)[0]"),
+    "varlen ranges of the wrong rows": ("np.asarray(kv_ranges)[qs:qe][None]", "np.asarray(kv_ranges)[:qe - qs][None]"),
     "varlen keys of the next sequence": ("kb = k[ks:ke]", "kb = k[ke:ke + (ke - ks)] if ke + (ke - ks) <= len(k) "
                                                           "else k[ks:ke][::-1]"),
 }
