@@ -59,7 +59,7 @@ class AttnOptions(ctypes.Structure):
     _fields_ = [("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
                 ("alibi_slopes", ctypes.c_void_p), ("rope_theta", ctypes.c_float),
                 ("rope_interleaved", ctypes.c_int32), ("num_splits", ctypes.c_int32),
-                ("rope_rotated_keys", ctypes.c_int32)]
+                ("rope_rotated_keys", ctypes.c_int32), ("kv_ranges", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -208,23 +208,31 @@ def attn_fwd_prefill_host(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, ca
 
 
 def make_options(window_left: int = -1, window_right: int = -1, alibi_slopes=None, rope_theta: float = 0.0,
-                 rope_interleaved: bool = False, num_splits: int = 0, rope_rotated_keys: bool = False):
+                 rope_interleaved: bool = False, num_splits: int = 0, rope_rotated_keys: bool = False,
+                 kv_ranges=None):
     """An AttnOptions for the *_ex calls (None when nothing is set).
 
     alibi_slopes: fp32 CUDA tensor (H_q); rope_theta: base of the rotary embedding (0: none);
     rope_interleaved: pairs (2c, 2c+1) instead of (c, c+D/2); num_splits: decode split count (0: automatic);
-    rope_rotated_keys: prefill keys already rotated (only the queries are rotated).
+    rope_rotated_keys: prefill keys already rotated (only the queries are rotated);
+    kv_ranges: int32 CUDA tensor of per-query-row key ranges [lo, hi), (B, N_q, 2) or packed (total_q, 2).
     """
     if (window_left == -1 and window_right == -1 and alibi_slopes is None and not rope_theta
-            and not num_splits):
+            and not num_splits and kv_ranges is None):
         return None
+    if kv_ranges is not None:
+        import torch
+        if kv_ranges.dtype != torch.int32 or not kv_ranges.is_cuda or not kv_ranges.is_contiguous() \
+                or kv_ranges.shape[-1] != 2:
+            raise TypeError("kv_ranges must be a contiguous int32 CUDA tensor of [lo, hi) pairs")
     if alibi_slopes is not None:
         import torch
         if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda:
             raise TypeError("alibi_slopes must be an fp32 CUDA tensor")
     return AttnOptions(int(window_left), int(window_right),
                        alibi_slopes.data_ptr() if alibi_slopes is not None else None, float(rope_theta),
-                       1 if rope_interleaved else 0, int(num_splits), 1 if rope_rotated_keys else 0)
+                       1 if rope_interleaved else 0, int(num_splits), 1 if rope_rotated_keys else 0,
+                       kv_ranges.data_ptr() if kv_ranges is not None else None)
 
 
 def attn_fwd_prefill_varlen(q, k, v, o, lse, dtype, B, H_q, H_kv, D, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
@@ -355,7 +363,7 @@ def _check(status: int, where: str):
 
 def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_lse: bool = True, out=None,
             lse_out=None, stream=None, window=(-1, -1), alibi_slopes=None, rope_theta: float = 0.0,
-            rope_interleaved: bool = False, rope_rotated_keys: bool = False):
+            rope_interleaved: bool = False, rope_rotated_keys: bool = False, kv_ranges=None):
     """Fused attention forward.  q (B,H_q,N_q,D); k, v (B,H_kv,N_kv,D) CUDA tensors.
 
     Any (b, h, n) strides are accepted (16-byte multiples, d stride 1), so a
@@ -376,7 +384,7 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_ls
                              lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D,
                              q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
                              make_options(window[0], window[1], alibi_slopes, rope_theta, rope_interleaved,
-                                          rope_rotated_keys=rope_rotated_keys),
+                                          rope_rotated_keys=rope_rotated_keys, kv_ranges=kv_ranges),
                              _stream_handle(stream))
     _check(st, "attn_fwd_prefill")
     return o, lse
@@ -384,7 +392,7 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_ls
 
 def prefill_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse_out=None,
                  workspace=None, stream=None, window=(-1, -1), alibi_slopes=None, rope_theta: float = 0.0,
-                 rope_interleaved: bool = False):
+                 rope_interleaved: bool = False, kv_ranges=None):
     """Prefill on host tensors (contiguous, ideally pinned) with copies pipelined against the compute.
 
     q (B,H_q,N_q,D), k, v (B,H_kv,N_kv,D) CPU tensors; returns host (O, LSE).  The results are complete
@@ -406,7 +414,8 @@ def prefill_host(q, k, v, causal: bool = False, scale: float | None = None, out=
         workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
     st = attn_fwd_prefill_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), code, B, Hq,
                                Hkv, Nq, Nkv, D, causal, scale,
-                               make_options(window[0], window[1], alibi_slopes, rope_theta, rope_interleaved),
+                               make_options(window[0], window[1], alibi_slopes, rope_theta, rope_interleaved,
+                                            kv_ranges=kv_ranges),
                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                _stream_handle(stream))
     _check(st, "attn_fwd_prefill_host")
@@ -417,7 +426,7 @@ def prefill_host(q, k, v, causal: bool = False, scale: float | None = None, out=
 def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                    causal: bool = False, scale: float | None = None, return_lse: bool = True, out=None,
                    lse_out=None, stream=None, window=(-1, -1), alibi_slopes=None, rope_theta: float = 0.0,
-                   rope_interleaved: bool = False, rope_rotated_keys: bool = False):
+                   rope_interleaved: bool = False, rope_rotated_keys: bool = False, kv_ranges=None):
     """Attention over packed sequences of different lengths.
 
     q (total_q, H_q, D); k, v (total_k, H_kv, D); cu_seqlens_q / cu_seqlens_k int32 CUDA tensors (B + 1).
@@ -440,7 +449,7 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_s
                                     cq.data_ptr(), ck.data_ptr(), int(max_seqlen_q), int(max_seqlen_k), total_q,
                                     total_k, q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
                                     make_options(window[0], window[1], alibi_slopes, rope_theta, rope_interleaved,
-                                                 rope_rotated_keys=rope_rotated_keys),
+                                                 rope_rotated_keys=rope_rotated_keys, kv_ranges=kv_ranges),
                                     _stream_handle(stream))
     _check(st, "attn_fwd_prefill_varlen")
     return o, lse

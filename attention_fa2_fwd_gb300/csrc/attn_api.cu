@@ -201,6 +201,7 @@ struct Opts {
   int rope_interleaved = 0;      // 0: pairs (c, c + D/2); 1: pairs (2c, 2c + 1)
   int num_splits = 0;            // decode: 0 automatic, else at most this many KV splits
   int rope_rotated_keys = 0;     // prefill: the keys come already rotated
+  const int32_t *kv_ranges = nullptr;  // prefill: per-row key ranges
 };
 constexpr int kMaxDecodeSplits = 64;
 
@@ -213,6 +214,7 @@ attn_status_t read_opts(const attn_options_t *opts, Opts *o) {
   if (opts->num_splits < 0 || opts->num_splits > kMaxDecodeSplits) return ATTN_ERR_INVALID_ARG;
   if (opts->rope_rotated_keys != 0 && opts->rope_rotated_keys != 1) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(opts->alibi_slopes) & 3) != 0) return ATTN_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(opts->kv_ranges) & 7) != 0) return ATTN_ERR_ALIGNMENT;
   o->wl = opts->window_left;
   o->wr = opts->window_right;
   o->slopes = opts->alibi_slopes;
@@ -220,6 +222,7 @@ attn_status_t read_opts(const attn_options_t *opts, Opts *o) {
   o->rope_interleaved = opts->rope_interleaved;
   o->num_splits = opts->num_splits;
   o->rope_rotated_keys = opts->rope_rotated_keys;
+  o->kv_ranges = opts->kv_ranges;
   return ATTN_OK;
 }
 
@@ -270,7 +273,8 @@ attn_status_t prefill_schedule(PrefillParams *p, int B, int H_q, int sm_count) {
 // Whether a prefill needs the masked kernel build: a left window, a right
 // window that the causal mask does not already imply, or ALiBi slopes.
 bool prefill_masked(const PrefillParams &p, bool causal) {
-  return p.window_left >= 0 || (!causal && p.window_right >= 0) || p.alibi_slopes != nullptr;
+  return p.window_left >= 0 || (!causal && p.window_right >= 0) || p.alibi_slopes != nullptr ||
+         p.kv_ranges != nullptr;
 }
 
 // Keys decode streams for a cache of `len` rows under a left window: the
@@ -343,6 +347,7 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
   p.window_left = op.wl;
   p.window_right = op.wr;
   p.alibi_slopes = op.slopes;
+  p.kv_ranges = op.kv_ranges;
   const bool rope = op.rope_theta > 0.f;
   if (rope) {
     p.rope_inter = op.rope_interleaved;
@@ -418,6 +423,7 @@ attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const voi
   p.window_left = op.wl;
   p.window_right = op.wr;
   p.alibi_slopes = op.slopes;
+  p.kv_ranges = op.kv_ranges;
   const bool rope = op.rope_theta > 0.f;
   if (rope) {
     p.rope_inter = op.rope_interleaved;
@@ -564,6 +570,7 @@ attn_status_t attn_fwd_decode_ex(const void *q, const void *k_cache, const void 
   const int64_t csz[4] = {B, H_kv, cache_len, D};
   Opts op;
   if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if (op.kv_ranges != nullptr) return ATTN_ERR_UNSUPPORTED;  // key ranges are a prefill mask
   const int wl = op.wl;
   const float *slopes = op.slopes;
   const DeviceState *dev = nullptr;
@@ -726,6 +733,7 @@ attn_status_t attn_fwd_decode_paged_ex(const void *q, const void *k_pages, const
     return st;
   Opts op;
   if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if (op.kv_ranges != nullptr) return ATTN_ERR_UNSUPPORTED;  // key ranges are a prefill mask
   const int wl = op.wl;
   const float *slopes = op.slopes;
   const DeviceState *dev = nullptr;
@@ -1042,7 +1050,8 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
         const int64_t sq[4] = {static_cast<int64_t>(nqh) * N_q * D, static_cast<int64_t>(N_q) * D, D, 1};
         const int64_t sk[4] = {static_cast<int64_t>(nh) * N_kv * D, static_cast<int64_t>(N_kv) * D, D, 1};
         attn_options_t oc{wl, wr, slopes ? slopes + qh0 : nullptr, op.rope_theta, op.rope_interleaved, 0,
-                          op.rope_rotated_keys};
+                          op.rope_rotated_keys,
+                          op.kv_ranges ? op.kv_ranges + static_cast<size_t>(b) * N_q * 2 : nullptr};
         const attn_status_t cs = attn_fwd_prefill_ex(dq + qo, dk + ko, dv + ko, dout + qo,
                                                      lse ? reinterpret_cast<float *>(reinterpret_cast<char *>(dl) + lo)
                                                          : nullptr,

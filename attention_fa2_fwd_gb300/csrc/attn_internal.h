@@ -42,6 +42,9 @@ struct PrefillParams {
   // alibi_slopes (device fp32, one per q head) adds -slope_h |i - j| to scores.
   int window_left, window_right;
   const float *alibi_slopes;
+  // Custom mask: per query row a key range [lo, hi) (int32 pairs, indexed by
+  // b * Nq + row, or by the packed row for variable length); null: none.
+  const int32_t *kv_ranges;
   // Rotary embeddings (ROPE builds): pair c of a row at position p turns by
   // (p * rope_f[c] mod 2^64) / 2^64 of a full turn; rope_inter selects the
   // pairs (2c, 2c + 1) instead of (c, c + D/2); rope_k = 0 when the keys come

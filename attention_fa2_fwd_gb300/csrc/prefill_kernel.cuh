@@ -746,6 +746,7 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
       const int u = unit_index(k, u_first, u_step);
       if (u >= n_units) continue;
       int q_tile0, Nkv, jlo, jhi;
+      const int2 *krow = nullptr;  // custom mask: this row's key range [lo, hi), or null
       float slope2;
       {
         // Only what the step loop needs stays live through it; the epilogue
@@ -758,6 +759,12 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
         // ALiBi: score += -slope_h |i - j|, in base-2 units.
         slope2 = (MASKED && p.alibi_slopes != nullptr && U.kind == kRun)
                      ? p.alibi_slopes[U.h] * 1.4426950408889634f : 0.f;
+        if (MASKED && p.kv_ranges != nullptr && U.kind == kRun) {
+          // A row past N_q (computed, never stored) reads row 0's range.
+          const int row = q_tile0 + r < U.Nq ? q_tile0 + r : 0;
+          const int64_t ri = VARLEN ? static_cast<int64_t>(U.q_base) + row : static_cast<int64_t>(U.b) * p.Nq + row;
+          krow = reinterpret_cast<const int2 *>(p.kv_ranges) + ri;
+        }
         if (U.kind != kRun) {
           const int q_row = q_tile0 + r;
           if ((U.kind & kBadIndex) && threadIdx.x == 0) atomicOr(p.err, kErrBadIndex);
@@ -787,13 +794,23 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
         for (int i = 0; i < 4; ++i) reg_fence(sr[i]);
 
         const int kv0 = j * kBN;
-        // Masked only where the tile crosses the end of the keys or a band edge.
-        const bool need_mask = (kv0 + kBN > Nkv) || (win_r != kUnlimited && kv0 + kBN - 1 > q_tile0 + win_r) ||
-                               (win_l != kUnlimited && kv0 < q_tile0 + kBM - 1 - win_l);
+        // Masked only where the tile crosses the end of the keys or a band edge
+        // (or, with key ranges, some row's range edge).
+        bool need_mask = (kv0 + kBN > Nkv) || (win_r != kUnlimited && kv0 + kBN - 1 > q_tile0 + win_r) ||
+                         (win_l != kUnlimited && kv0 < q_tile0 + kBM - 1 - win_l);
+        int2 kr = make_int2(0, kUnlimited);
+        if (MASKED && krow != nullptr) {
+          kr = __ldg(krow);
+          need_mask = need_mask || __any_sync(0xffffffffu, kr.x > kv0 || kr.y < kv0 + kBN);
+        }
         if (need_mask) {
           // columns lo_c <= c < hi_c are kept
-          const int hi_c = (win_r == kUnlimited ? Nkv : min(Nkv, q_row + win_r + 1)) - kv0;
-          const int lo_c = win_l == kUnlimited ? 0 : q_row - win_l - kv0;
+          int hi_c = (win_r == kUnlimited ? Nkv : min(Nkv, q_row + win_r + 1)) - kv0;
+          int lo_c = win_l == kUnlimited ? 0 : q_row - win_l - kv0;
+          if constexpr (MASKED) {
+            hi_c = min(hi_c, kr.y - kv0);
+            lo_c = max(lo_c, kr.x - kv0);
+          }
 #pragma unroll
           for (int i = 0; i < 4; ++i)
 #pragma unroll

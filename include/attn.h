@@ -97,6 +97,16 @@ typedef enum {
  *                 with the same RoPE options); the kernel then rotates only
  *                 the query tiles, which costs far less than rotating every K
  *                 tile it reads.  0: the kernel rotates both.
+ *   kv_ranges     prefill only: NULL, or a custom mask given as a device int32
+ *                 array of key ranges, one [lo, hi) pair per query row --
+ *                 (B, N_q, 2) for attn_fwd_prefill_ex and the host-buffer
+ *                 call, (total_q, 2) for the variable-length call (keys
+ *                 counted from the row's sequence start): query row i attends
+ *                 only to keys j with lo <= j < hi, in addition to the causal
+ *                 and window bounds (block-diagonal, document and prefix masks
+ *                 are such ranges).  Tiles are skipped by the causal and
+ *                 window bands only; the ranges mask within them.  Decode calls
+ *                 return ATTN_ERR_UNSUPPORTED when it is set.
  *   num_splits    decode only: 0 lets the library choose how many parts the
  *                 cache is split into; n in [1, 64] uses at most n (1: one
  *                 pass, no workspace).  More splits than the automatic choice
@@ -116,9 +126,11 @@ typedef enum {
  * Errors: a window below -1, a rope_theta that is negative or not finite, a
  * rope_interleaved or rope_rotated_keys other than 0 or 1, or a num_splits
  * outside [0, 64] gives
- * ATTN_ERR_INVALID_ARG; slopes not 4-byte aligned give ATTN_ERR_ALIGNMENT.
- * The struct is read during the call; the slope array is read by the kernel,
- * so it must stay valid until the work enqueued on the stream has finished.
+ * ATTN_ERR_INVALID_ARG; slopes not 4-byte aligned or key ranges not 8-byte
+ * aligned give ATTN_ERR_ALIGNMENT.
+ * The struct is read during the call; the slope and key-range arrays are read
+ * by the kernel, so they must stay valid until the work enqueued on the
+ * stream has finished.
  * The caller owns both.
  */
 typedef struct {
@@ -129,6 +141,7 @@ typedef struct {
     int32_t rope_interleaved;
     int32_t num_splits;
     int32_t rope_rotated_keys;
+    const int32_t *kv_ranges;
 } attn_options_t;
 
 /*

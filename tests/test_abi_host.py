@@ -287,6 +287,7 @@ OPTION_CALLS = {
     ((-1, -1, None, 0.0, 0, 65), A.ATTN_ERR_INVALID_ARG),
     ((-1, -1, None, 10000.0, 0, 0, 2), A.ATTN_ERR_INVALID_ARG),
     ((-1, -1, None, 10000.0, 0, 0, -1), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, None, 0.0, 0, 0, 0, P + 4), A.ATTN_ERR_ALIGNMENT),
 ])
 def test_option_errors(lib, call, opts, code):
     """Options are validated with the other arguments, before any CUDA call."""
@@ -375,9 +376,16 @@ def test_options_struct_matches_the_header():
     import ctypes
     names = [f[0] for f in A.AttnOptions._fields_]
     assert names == ["window_left", "window_right", "alibi_slopes", "rope_theta", "rope_interleaved", "num_splits",
-                     "rope_rotated_keys"]
+                     "rope_rotated_keys", "kv_ranges"]
     text = open(HEADER).read()
     body = text[text.index("typedef struct {"):text.index("} attn_options_t;")]
     declared = re.findall(r"\b([a-z_]+);", body)
     assert declared == names
-    assert ctypes.sizeof(A.AttnOptions) == 32  # 4 + 4 + 8 + 4 + 4 + 4 + 4 on LP64
+    assert ctypes.sizeof(A.AttnOptions) == 40  # 4 + 4 + 8 + 4 + 4 + 4 + 4 + 8 on LP64
+
+
+def test_key_ranges_are_a_prefill_mask(lib):
+    """Decode calls refuse key ranges with ATTN_ERR_UNSUPPORTED; the option checks run before any CUDA call."""
+    opts = A.AttnOptions(-1, -1, None, 0.0, 0, 0, 0, P)
+    assert OPTION_CALLS["decode"](opts) == A.ATTN_ERR_UNSUPPORTED
+    assert OPTION_CALLS["decode_paged"](opts) == A.ATTN_ERR_UNSUPPORTED

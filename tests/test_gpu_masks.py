@@ -194,3 +194,105 @@ def test_paged_decode_window_alibi(page_size, wl, alibi):
     o_ref, lse_ref = M.decode_paged_masked(np64(q), np64(kp), np64(vp), table.numpy(), cl.numpy(),
                                            1 / math.sqrt(D), wl, sl)
     _assert_masked(o, lse, o_ref, lse_ref, f"paged ps={page_size} wl={wl} alibi={alibi}")
+
+
+# ---------------------------------------------------------------- custom masks: per-row key ranges
+
+def _ranges(rng, B, Nq, Nkv):
+    """Random [lo, hi) per row, with a full row, an empty row and ranges reaching past N_kv."""
+    lo = rng.integers(-5, Nkv, size=(B, Nq))
+    hi = lo + rng.integers(0, Nkv // 2 + 2, size=(B, Nq))
+    r = np.stack([lo, hi], axis=-1).astype(np.int32)
+    r[:, 0] = (0, Nkv)
+    r[:, 1] = (7, 7)
+    r[:, 2] = (Nkv - 3, Nkv + 40)
+    return r
+
+
+RANGE_CASES = [(dt, D, causal) for dt in ("bf16", "f16") for D in (64, 128) for causal in (False, True)]
+
+
+@pytest.mark.parametrize("case", RANGE_CASES, ids=[f"{c[0]}_d{c[1]}_{'c' if c[2] else 'nc'}" for c in RANGE_CASES])
+def test_key_ranges_prefill(case):
+    import attention_fa2_fwd_gb300 as A
+    dt, D, causal = case
+    B, Hq, Hkv, Nq, Nkv = 2, 8, 2, 300, 333
+    q, k, v = I.prefill_inputs(B, Hq, Hkv, Nq, Nkv, D, dt, seed=D + causal)
+    kr = _ranges(np.random.default_rng(D + 3 * causal), B, Nq, Nkv)
+    o, lse = A.prefill(q.cuda(), k.cuda(), v.cuda(), causal=causal, kv_ranges=torch.from_numpy(kr).cuda())
+    torch.cuda.synchronize()
+    o_ref, l_ref = M.attention_masked(np64(q), np64(k), np64(v), causal, 1 / math.sqrt(D), kv_ranges=kr)
+    _assert_masked(o, lse, o_ref, l_ref, f"ranges {case}")
+
+
+def test_document_mask_equals_separate_documents():
+    """Block-diagonal ranges over one long row: each query sees only its own document (causal within
+    it); documents of 1000, 1, 3000 and 4191 tokens."""
+    import attention_fa2_fwd_gb300 as A
+    lens = [1000, 1, 3000, 4191]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    N, Hq, Hkv, D = int(cu[-1]), 8, 2, 128
+    q, k, v = I.prefill_inputs(1, Hq, Hkv, N, N, D, "bf16", seed=80)
+    kr = np.zeros((1, N, 2), dtype=np.int32)
+    for d in range(len(lens)):
+        kr[0, cu[d]:cu[d + 1]] = (cu[d], cu[d + 1])
+    o, lse = A.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, kv_ranges=torch.from_numpy(kr).cuda())
+    torch.cuda.synchronize()
+    import oracle
+    o_ref, l_ref = oracle.prefill_varlen(np64(q)[0].transpose(1, 0, 2), np64(k)[0].transpose(1, 0, 2),
+                                         np64(v)[0].transpose(1, 0, 2), cu, cu, True, 1 / math.sqrt(D))
+    assert_close(np64(o)[0], o_ref.transpose(1, 0, 2), np64(lse)[0], l_ref, "document mask")
+
+
+def test_key_ranges_with_window_alibi_and_rope():
+    import attention_fa2_fwd_gb300 as A
+    from oracle import rope as R
+    B, Hq, Hkv, N, D = 1, 4, 1, 500, 128
+    q, k, v = I.prefill_inputs(B, Hq, Hkv, N, N, D, "bf16", seed=81)
+    kr = _ranges(np.random.default_rng(81), B, N, N)
+    s = _slopes(Hq)
+    o, lse = A.prefill(q.cuda(), k.cuda(), v.cuda(), causal=False, window=(120, 30), alibi_slopes=_dev_slopes(s),
+                       kv_ranges=torch.from_numpy(kr).cuda())
+    torch.cuda.synchronize()
+    o_ref, l_ref = M.attention_masked(np64(q), np64(k), np64(v), False, 1 / math.sqrt(D), 120, 30, s.astype(np.float64),
+                                      kv_ranges=kr)
+    _assert_masked(o, lse, o_ref, l_ref, "ranges + window + ALiBi")
+    # with rotary embeddings: the oracle's rotation rounded to 16 bits, then the masked oracle
+    o, lse = A.prefill(q.cuda(), k.cuda(), v.cuda(), causal=True, rope_theta=10000.0,
+                       kv_ranges=torch.from_numpy(kr).cuda())
+    torch.cuda.synchronize()
+    qr = torch.from_numpy(R.rotate(np64(q), np.arange(N), 10000.0)).to(torch.bfloat16).double().numpy()
+    kr_ = torch.from_numpy(R.rotate(np64(k), np.arange(N), 10000.0)).to(torch.bfloat16).double().numpy()
+    o_ref, l_ref = M.attention_masked(qr, kr_, np64(v), True, 1 / math.sqrt(D), kv_ranges=kr)
+    _assert_masked(o, lse, o_ref, l_ref, "ranges + RoPE")
+
+
+def test_key_ranges_varlen_and_host_path():
+    import attention_fa2_fwd_gb300 as A
+    lq, lk = [300, 1, 129, 700], [300, 50, 129, 900]
+    cq, ck = np.concatenate([[0], np.cumsum(lq)]), np.concatenate([[0], np.cumsum(lk)])
+    Hq, Hkv, D = 8, 2, 64
+    g = torch.Generator().manual_seed(82)
+    q = torch.randn((int(cq[-1]), Hq, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((int(ck[-1]), Hkv, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((int(ck[-1]), Hkv, D), generator=g).to(torch.bfloat16)
+    rng = np.random.default_rng(82)
+    kr = np.zeros((int(cq[-1]), 2), dtype=np.int32)
+    for b in range(len(lq)):
+        kr[cq[b]:cq[b + 1]] = _ranges(rng, 1, lq[b] + 3, lk[b])[0][:lq[b]]
+    for causal in (False, True):
+        o, lse = A.prefill_varlen(q.cuda(), k.cuda(), v.cuda(), torch.tensor(cq, dtype=torch.int32).cuda(),
+                                  torch.tensor(ck, dtype=torch.int32).cuda(), max(lq), max(lk), causal=causal,
+                                  kv_ranges=torch.from_numpy(kr).cuda())
+        torch.cuda.synchronize()
+        o_ref, l_ref = M.prefill_varlen_masked(np64(q), np64(k), np64(v), cq, ck, causal, 1 / math.sqrt(D),
+                                               kv_ranges=kr)
+        # varlen LSE is (H_q, total_q): compare it row-aligned with O (total_q, H_q, D)
+        _assert_masked(o, lse.t(), o_ref, l_ref.T, f"varlen ranges causal={causal}")
+    # the host-buffer call cuts the problem per batch element: its result equals the device call's
+    qd, kd, vd = I.prefill_inputs(2, 16, 4, 700, 700, 128, "bf16", seed=83)
+    krd = torch.from_numpy(_ranges(np.random.default_rng(83), 2, 700, 700)).cuda()
+    o_d, l_d = A.prefill(qd.cuda(), kd.cuda(), vd.cuda(), causal=True, kv_ranges=krd)
+    o_h, l_h = A.prefill_host(qd.pin_memory(), kd.pin_memory(), vd.pin_memory(), causal=True, kv_ranges=krd)
+    torch.cuda.synchronize()
+    assert torch.equal(o_d.cpu(), o_h) and torch.equal(l_d.cpu(), l_h)
