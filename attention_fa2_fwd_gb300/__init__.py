@@ -55,11 +55,13 @@ class AttnError(RuntimeError):
 
 class AttnOptions(ctypes.Structure):
     """attn_options_t: sliding-window bounds (-1: none), ALiBi slopes (device fp32 pointer or None),
-    rotary embedding base (0: none) and pairing, and the decode split count (0: automatic)."""
+    rotary embedding base (0: none) and pairing, the decode split count (0: automatic), key ranges and the
+    prefill kernel (0 automatic, 1 one-CTA, 2 CTA pair)."""
     _fields_ = [("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
                 ("alibi_slopes", ctypes.c_void_p), ("rope_theta", ctypes.c_float),
                 ("rope_interleaved", ctypes.c_int32), ("num_splits", ctypes.c_int32),
-                ("rope_rotated_keys", ctypes.c_int32), ("kv_ranges", ctypes.c_void_p)]
+                ("rope_rotated_keys", ctypes.c_int32), ("kv_ranges", ctypes.c_void_p),
+                ("prefill_kernel", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -209,16 +211,17 @@ def attn_fwd_prefill_host(q, k, v, o, lse, dtype, B, H_q, H_kv, N_q, N_kv, D, ca
 
 def make_options(window_left: int = -1, window_right: int = -1, alibi_slopes=None, rope_theta: float = 0.0,
                  rope_interleaved: bool = False, num_splits: int = 0, rope_rotated_keys: bool = False,
-                 kv_ranges=None):
+                 kv_ranges=None, prefill_kernel: int = 0):
     """An AttnOptions for the *_ex calls (None when nothing is set).
 
     alibi_slopes: fp32 CUDA tensor (H_q); rope_theta: base of the rotary embedding (0: none);
     rope_interleaved: pairs (2c, 2c+1) instead of (c, c+D/2); num_splits: decode split count (0: automatic);
     rope_rotated_keys: prefill keys already rotated (only the queries are rotated);
-    kv_ranges: int32 CUDA tensor of per-query-row key ranges [lo, hi), (B, N_q, 2) or packed (total_q, 2).
+    kv_ranges: int32 CUDA tensor of per-query-row key ranges [lo, hi), (B, N_q, 2) or packed (total_q, 2);
+    prefill_kernel: 0 automatic, 1 the one-CTA kernel, 2 the CTA-pair kernel (D = 128, no masks or RoPE).
     """
     if (window_left == -1 and window_right == -1 and alibi_slopes is None and not rope_theta
-            and not num_splits and kv_ranges is None):
+            and not num_splits and kv_ranges is None and not prefill_kernel):
         return None
     if kv_ranges is not None:
         import torch
@@ -232,7 +235,7 @@ def make_options(window_left: int = -1, window_right: int = -1, alibi_slopes=Non
     return AttnOptions(int(window_left), int(window_right),
                        alibi_slopes.data_ptr() if alibi_slopes is not None else None, float(rope_theta),
                        1 if rope_interleaved else 0, int(num_splits), 1 if rope_rotated_keys else 0,
-                       kv_ranges.data_ptr() if kv_ranges is not None else None)
+                       kv_ranges.data_ptr() if kv_ranges is not None else None, int(prefill_kernel))
 
 
 def attn_fwd_prefill_varlen(q, k, v, o, lse, dtype, B, H_q, H_kv, D, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
@@ -363,7 +366,8 @@ def _check(status: int, where: str):
 
 def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_lse: bool = True, out=None,
             lse_out=None, stream=None, window=(-1, -1), alibi_slopes=None, rope_theta: float = 0.0,
-            rope_interleaved: bool = False, rope_rotated_keys: bool = False, kv_ranges=None):
+            rope_interleaved: bool = False, rope_rotated_keys: bool = False, kv_ranges=None,
+            prefill_kernel: int = 0):
     """Fused attention forward.  q (B,H_q,N_q,D); k, v (B,H_kv,N_kv,D) CUDA tensors.
 
     Any (b, h, n) strides are accepted (16-byte multiples, d stride 1), so a
@@ -384,7 +388,8 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_ls
                              lse.data_ptr() if lse is not None else None, _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D,
                              q.stride(), k.stride(), v.stride(), o.stride(), 1 if causal else 0, scale,
                              make_options(window[0], window[1], alibi_slopes, rope_theta, rope_interleaved,
-                                          rope_rotated_keys=rope_rotated_keys, kv_ranges=kv_ranges),
+                                          rope_rotated_keys=rope_rotated_keys, kv_ranges=kv_ranges,
+                                          prefill_kernel=prefill_kernel),
                              _stream_handle(stream))
     _check(st, "attn_fwd_prefill")
     return o, lse
@@ -392,7 +397,7 @@ def prefill(q, k, v, causal: bool = False, scale: float | None = None, return_ls
 
 def prefill_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse_out=None,
                  workspace=None, stream=None, window=(-1, -1), alibi_slopes=None, rope_theta: float = 0.0,
-                 rope_interleaved: bool = False, kv_ranges=None):
+                 rope_interleaved: bool = False, kv_ranges=None, prefill_kernel: int = 0):
     """Prefill on host tensors (contiguous, ideally pinned) with copies pipelined against the compute.
 
     q (B,H_q,N_q,D), k, v (B,H_kv,N_kv,D) CPU tensors; returns host (O, LSE).  The results are complete
@@ -415,7 +420,7 @@ def prefill_host(q, k, v, causal: bool = False, scale: float | None = None, out=
     st = attn_fwd_prefill_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), code, B, Hq,
                                Hkv, Nq, Nkv, D, causal, scale,
                                make_options(window[0], window[1], alibi_slopes, rope_theta, rope_interleaved,
-                                            kv_ranges=kv_ranges),
+                                            kv_ranges=kv_ranges, prefill_kernel=prefill_kernel),
                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                _stream_handle(stream))
     _check(st, "attn_fwd_prefill_host")

@@ -28,6 +28,7 @@ struct DeviceState {
   bool ready = false;
   bool supported = false;
   int sm_count = 0;
+  int pair_clusters = 0;  // CTA-pair prefill clusters resident at once (0: pair kernel not used)
   unsigned *err = nullptr;
   unsigned *taken = nullptr;
 };
@@ -70,6 +71,7 @@ attn_status_t device_state(const DeviceState **out) {
           return ATTN_ERR_CUDA;
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
       }
+      s.pair_clusters = prefill_pair_max_clusters();
     }
     s.ready = true;
   }
@@ -202,12 +204,17 @@ struct Opts {
   int num_splits = 0;            // decode: 0 automatic, else at most this many KV splits
   int rope_rotated_keys = 0;     // prefill: the keys come already rotated
   const int32_t *kv_ranges = nullptr;  // prefill: per-row key ranges
+  int prefill_kernel = 0;        // dense prefill: 0 automatic, 1 one-CTA, 2 CTA pair
 };
 constexpr int kMaxDecodeSplits = 64;
 
-attn_status_t read_opts(const attn_options_t *opts, Opts *o) {
+// kernel_choice: the call can run either prefill kernel (else prefill_kernel
+// must be 0).
+attn_status_t read_opts(const attn_options_t *opts, Opts *o, bool kernel_choice = false) {
   *o = Opts{};
   if (opts == nullptr) return ATTN_OK;
+  if (opts->prefill_kernel < 0 || opts->prefill_kernel > 2 || (!kernel_choice && opts->prefill_kernel != 0))
+    return ATTN_ERR_INVALID_ARG;
   if (opts->window_left < -1 || opts->window_right < -1) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(opts->rope_theta) || opts->rope_theta < 0.f) return ATTN_ERR_INVALID_ARG;
   if (opts->rope_interleaved != 0 && opts->rope_interleaved != 1) return ATTN_ERR_INVALID_ARG;
@@ -223,6 +230,7 @@ attn_status_t read_opts(const attn_options_t *opts, Opts *o) {
   o->num_splits = opts->num_splits;
   o->rope_rotated_keys = opts->rope_rotated_keys;
   o->kv_ranges = opts->kv_ranges;
+  o->prefill_kernel = opts->prefill_kernel;
   return ATTN_OK;
 }
 
@@ -257,16 +265,16 @@ __global__ void selftest_wait_kernel(unsigned *err) {
   if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, err);
 }
 
-// Persistent prefill schedule: units = query-tile pairs x heads x batches,
-// one CTA per SM at most.
-attn_status_t prefill_schedule(PrefillParams *p, int B, int H_q, int sm_count) {
+// Persistent prefill schedule: units = query-row blocks x heads x batches,
+// walked by at most `slots` workers (CTAs, or CTA pairs) resident at once.
+attn_status_t prefill_schedule(PrefillParams *p, int B, int H_q, int slots) {
   const int64_t units = static_cast<int64_t>(H_q) * B * p->n_qtiles;
-  // The kernel walks units in rounds of up to sm_count; every index it forms
-  // (round * CTAs + CTA) stays below units + sm_count, which must fit an int.
-  if (units + sm_count > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
+  // The kernel walks units in rounds of up to `slots`; every index it forms
+  // (round * workers + worker) stays below units + slots, which must fit an int.
+  if (units + slots > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
   p->B = B;
   p->n_units = static_cast<int>(units);
-  p->n_ctas = static_cast<int>(units < sm_count ? units : sm_count);
+  p->n_ctas = static_cast<int>(units < slots ? units : slots);
   return ATTN_OK;
 }
 
@@ -343,7 +351,7 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
 
   PrefillParams p{};
   Opts op;
-  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if ((st = read_opts(opts, &op, true)) != ATTN_OK) return st;
   p.window_left = op.wl;
   p.window_right = op.wr;
   p.alibi_slopes = op.slopes;
@@ -357,9 +365,15 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
   const bool bf16 = dtype == ATTN_BF16;
+  const bool masked = prefill_masked(p, causal != 0);
+  // The CTA-pair kernel (on request only): head dimension 128 without
+  // windows, ALiBi, key ranges or rotary embeddings; each CTA loads half of
+  // every K tile (64-row boxes).
+  const bool pair = op.prefill_kernel == 2;
+  if (pair && (D != 128 || masked || rope || dev->pair_clusters <= 0)) return ATTN_ERR_UNSUPPORTED;
   CUtensorMap tq, tk, tv;
   if ((st = make_map(&tq, q, bf16, qsz, q_str, kPrefillBM, &p.slots_q)) ||
-      (st = make_map(&tk, k, bf16, kvsz, k_str, kPrefillBN, &p.slots_k)) ||
+      (st = make_map(&tk, k, bf16, kvsz, k_str, pair ? kPrefillBN / 2 : kPrefillBN, &p.slots_k)) ||
       (st = make_map(&tv, v, bf16, kvsz, v_str, kPrefillBN, &p.slots_v)))
     return st;
   p.o = o;
@@ -372,11 +386,18 @@ attn_status_t attn_fwd_prefill_ex(const void *q, const void *k, const void *v, v
   p.Nkv = N_kv;
   p.Hq = H_q;
   p.group = H_q / H_kv;
-  p.n_qtiles = (N_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
-  if ((st = prefill_schedule(&p, B, H_q, dev->sm_count)) != ATTN_OK) return st;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  cudaError_t e = launch_prefill(D, causal != 0, bf16, false, prefill_masked(p, causal != 0), rope, tq, tk, tv, p, B,
-                                 static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (pair) {
+    p.n_qtiles = (N_q + kPairUnitRows - 1) / kPairUnitRows;
+    if ((st = prefill_schedule(&p, B, H_q, dev->pair_clusters)) != ATTN_OK) return st;
+    p.n_ctas *= 2;  // clusters of two CTAs
+    e = launch_prefill_pair(causal != 0, bf16, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  } else {
+    p.n_qtiles = (N_q + 2 * kPrefillBM - 1) / (2 * kPrefillBM);
+    if ((st = prefill_schedule(&p, B, H_q, dev->sm_count)) != ATTN_OK) return st;
+    e = launch_prefill(D, causal != 0, bf16, false, masked, rope, tq, tk, tv, p, B, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -985,7 +1006,7 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
   if (!valid_dtype(dtype) || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
   attn_status_t st;
   Opts op;
-  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if ((st = read_opts(opts, &op, true)) != ATTN_OK) return st;
   const int wl = op.wl, wr = op.wr;
   const float *slopes = op.slopes;
   const HostLayout L = host_layout(B, H_q, H_kv, N_q, N_kv, D);
@@ -993,6 +1014,11 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
   if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return ATTN_ERR_ALIGNMENT;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
+  // The chunks run attn_fwd_prefill_ex; a kernel choice it would refuse is
+  // refused here, before anything is enqueued.
+  const bool masked = wl >= 0 || (causal == 0 && wr >= 0) || slopes != nullptr || op.kv_ranges != nullptr;
+  if (op.prefill_kernel == 2 && (D != 128 || masked || op.rope_theta > 0.f || dev->pair_clusters <= 0))
+    return ATTN_ERR_UNSUPPORTED;
   cudaStream_t s_in, s_out;
   if ((st = copy_streams(&s_in, &s_out)) != ATTN_OK) return st;
   const cudaStream_t s_comp = static_cast<cudaStream_t>(stream);
@@ -1051,7 +1077,8 @@ attn_status_t attn_fwd_prefill_host(const void *q, const void *k, const void *v,
         const int64_t sk[4] = {static_cast<int64_t>(nh) * N_kv * D, static_cast<int64_t>(N_kv) * D, D, 1};
         attn_options_t oc{wl, wr, slopes ? slopes + qh0 : nullptr, op.rope_theta, op.rope_interleaved, 0,
                           op.rope_rotated_keys,
-                          op.kv_ranges ? op.kv_ranges + static_cast<size_t>(b) * N_q * 2 : nullptr};
+                          op.kv_ranges ? op.kv_ranges + static_cast<size_t>(b) * N_q * 2 : nullptr,
+                          op.prefill_kernel};
         const attn_status_t cs = attn_fwd_prefill_ex(dq + qo, dk + ko, dv + ko, dout + qo,
                                                      lse ? reinterpret_cast<float *>(reinterpret_cast<char *>(dl) + lo)
                                                          : nullptr,

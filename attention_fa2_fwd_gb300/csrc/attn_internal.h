@@ -119,6 +119,15 @@ cudaError_t launch_prefill_rope_masked(int D, bool causal, bool bf16, bool varle
                                        const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p, int B,
                                        cudaStream_t stream);
 
+// CTA-pair prefill (head dimension 128, no window, ALiBi, key ranges or
+// rotary embeddings): units of 512 query rows (p.n_qtiles per (b, h)), p.n_ctas
+// = 2 x clusters; tk_half has 64-row boxes (half a K tile per CTA).
+cudaError_t launch_prefill_pair(bool causal, bool bf16, const CUtensorMap &tq, const CUtensorMap &tk_half,
+                                const CUtensorMap &tv, const PrefillParams &p, cudaStream_t stream);
+// Clusters of two such CTAs that fit on the device at once (0: none / query failed).
+int prefill_pair_max_clusters();
+constexpr int kPairUnitRows = 512;  // query rows of a CTA-pair unit (two tiles of 256)
+
 // Decode: heads served by one CTA, and launch (split kernel, plus the merge
 // kernel when nsplit > 1).
 int decode_heads_per_cta(int group);

@@ -49,6 +49,8 @@ def main():
     ap.add_argument("--rope-interleaved", type=int, default=0, help="rotary pairs (2c, 2c+1) instead of (c, c+D/2)")
     ap.add_argument("--rope-rotated-keys", type=int, default=0, help="prefill: keys given already rotated")
     ap.add_argument("--num-splits", type=int, default=0, help="decode: force at most this many KV splits (0: auto)")
+    ap.add_argument("--prefill-kernel", type=int, default=0,
+                    help="prefill / cross: 0 automatic, 1 one-CTA kernel, 2 CTA-pair kernel")
     a = ap.parse_args()
     dt = torch.bfloat16 if a.dtype == "bf16" else torch.float16
     dev = torch.device("cuda", 0)
@@ -61,7 +63,7 @@ def main():
     stream = torch.cuda.current_stream()
     wl = a.window_left
     rope = dict(rope_theta=a.rope, rope_interleaved=bool(a.rope_interleaved))
-    rope_pre = dict(rope, rope_rotated_keys=bool(a.rope_rotated_keys))
+    rope_pre = dict(rope, rope_rotated_keys=bool(a.rope_rotated_keys), prefill_kernel=a.prefill_kernel)
     slopes = (torch.tensor([2.0 ** (-8.0 * (h + 1) / a.Hq) for h in range(a.Hq)], dtype=torch.float32, device=dev)
               if a.alibi else None)
     if a.kind == "prefill":
@@ -109,7 +111,7 @@ def main():
         work = w.flops
 
         def call():
-            A.prefill(q, k, v, causal=False, out=o, lse_out=lse, **rope)
+            A.prefill(q, k, v, causal=False, out=o, lse_out=lse, prefill_kernel=a.prefill_kernel, **rope)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "bwd":
         B = a.B or 2

@@ -111,6 +111,17 @@ typedef enum {
  *                 cache is split into; n in [1, 64] uses at most n (1: one
  *                 pass, no workspace).  More splits than the automatic choice
  *                 need a workspace of 4 * B * H_q * n * (D + 1) bytes.
+ *   prefill_kernel  attn_fwd_prefill_ex and the host-buffer call only (the
+ *                 other calls accept only 0): which kernel computes it.
+ *                 0 = automatic, 1 = the one-CTA kernel (every variant),
+ *                 2 = the CTA-pair kernel: clusters of two CTAs on
+ *                 neighbouring SMs share each tensor-core product (M = 256
+ *                 rows, each CTA holding half of every K and V tile) and keep
+ *                 P in shared memory; head dimension 128 without windows,
+ *                 ALiBi, rotary embeddings or key ranges, else
+ *                 ATTN_ERR_UNSUPPORTED.  Both compute the same function to the
+ *                 same tolerances; automatic runs the one-CTA kernel, which
+ *                 measures faster on GB300.
  *
  * Positions are those of the causal mask (top-left, per sequence for the
  * variable-length call); for decode the query sits at position cache_len - 1
@@ -124,8 +135,9 @@ typedef enum {
  * written to).  The values are never rotated.
  *
  * Errors: a window below -1, a rope_theta that is negative or not finite, a
- * rope_interleaved or rope_rotated_keys other than 0 or 1, or a num_splits
- * outside [0, 64] gives
+ * rope_interleaved or rope_rotated_keys other than 0 or 1, a num_splits
+ * outside [0, 64], or a prefill_kernel outside [0, 2] (or not 0 where the call
+ * has no choice) gives
  * ATTN_ERR_INVALID_ARG; slopes not 4-byte aligned or key ranges not 8-byte
  * aligned give ATTN_ERR_ALIGNMENT.
  * The struct is read during the call; the slope and key-range arrays are read
@@ -142,6 +154,7 @@ typedef struct {
     int32_t num_splits;
     int32_t rope_rotated_keys;
     const int32_t *kv_ranges;
+    int32_t prefill_kernel;
 } attn_options_t;
 
 /*

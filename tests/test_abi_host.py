@@ -288,10 +288,19 @@ OPTION_CALLS = {
     ((-1, -1, None, 10000.0, 0, 0, 2), A.ATTN_ERR_INVALID_ARG),
     ((-1, -1, None, 10000.0, 0, 0, -1), A.ATTN_ERR_INVALID_ARG),
     ((-1, -1, None, 0.0, 0, 0, 0, P + 4), A.ATTN_ERR_ALIGNMENT),
+    ((-1, -1, None, 0.0, 0, 0, 0, None, 3), A.ATTN_ERR_INVALID_ARG),
+    ((-1, -1, None, 0.0, 0, 0, 0, None, -1), A.ATTN_ERR_INVALID_ARG),
 ])
 def test_option_errors(lib, call, opts, code):
     """Options are validated with the other arguments, before any CUDA call."""
     assert OPTION_CALLS[call](A.AttnOptions(*opts)) == code
+
+
+@pytest.mark.parametrize("call", sorted(set(OPTION_CALLS) - {"prefill"}))
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_prefill_kernel_choice_only_where_offered(lib, call, kernel):
+    """Only the dense prefill (and the host-buffer call) take a kernel choice; the others accept only 0."""
+    assert OPTION_CALLS[call](A.AttnOptions(-1, -1, None, 0.0, 0, 0, 0, None, kernel)) == A.ATTN_ERR_INVALID_ARG
 
 
 def test_option_argument_errors_still_checked_first(lib):
@@ -376,12 +385,12 @@ def test_options_struct_matches_the_header():
     import ctypes
     names = [f[0] for f in A.AttnOptions._fields_]
     assert names == ["window_left", "window_right", "alibi_slopes", "rope_theta", "rope_interleaved", "num_splits",
-                     "rope_rotated_keys", "kv_ranges"]
+                     "rope_rotated_keys", "kv_ranges", "prefill_kernel"]
     text = open(HEADER).read()
     body = text[text.index("typedef struct {"):text.index("} attn_options_t;")]
     declared = re.findall(r"\b([a-z_]+);", body)
     assert declared == names
-    assert ctypes.sizeof(A.AttnOptions) == 40  # 4 + 4 + 8 + 4 + 4 + 4 + 4 + 8 on LP64
+    assert ctypes.sizeof(A.AttnOptions) == 48  # 4 + 4 + 8 + 4 + 4 + 4 + 4 + 8 + 4 (+ 4 padding) on LP64
 
 
 def test_key_ranges_are_a_prefill_mask(lib):
