@@ -148,6 +148,11 @@ struct BwdParams {
   int Nq, Nkv, Hq, group;
   float scale, scale_log2;
   uint32_t slots_q, slots_do, slots_k, slots_v;
+  // Tile order of the two tiled kernels (1-D grids): (batch, kv head) groups are
+  // walked in chunks of chunk_dq / chunk_dkv groups, the longest causal tiles
+  // of a chunk first, so that the CTAs in flight share a few groups' operands
+  // in L2 (Q and dO of a group's heads for dK/dV, K and V for dQ).
+  int B, Hkv, chunk_dq, chunk_dkv;
 };
 struct BwdMaps {
   CUtensorMap q, dout, k, v;  // 4-D tiled maps, 64 x 128 boxes, 128-byte swizzle

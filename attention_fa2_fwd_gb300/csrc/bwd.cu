@@ -169,11 +169,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_qt = (p.Nq + kT - 1) / kT;
-  // Grid (H_q, B, query tiles), heads first: under the causal mask every CTA
-  // of the longest query tile starts before any shorter one.
-  const int qt = CAUSAL ? (n_qt - 1 - static_cast<int>(blockIdx.z)) : static_cast<int>(blockIdx.z);
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int hk = h / p.group;
+  // 1-D grid over (group chunk, query tile, group, q head of the group): the
+  // longest causal query tiles of a chunk start first.
+  int qt, h, b, hk;
+  {
+    const int per_group = p.group * n_qt;
+    const int n_groups = p.Hkv * p.B;
+    const int lin = static_cast<int>(blockIdx.x);
+    const int c = lin / (p.chunk_dq * per_group);
+    const int gc = min(p.chunk_dq, n_groups - c * p.chunk_dq);  // groups in this chunk
+    const int r = lin - c * p.chunk_dq * per_group;
+    const int tidx = r / (gc * p.group), rem = r - tidx * gc * p.group;
+    const int g = c * p.chunk_dq + rem / p.group;
+    qt = CAUSAL ? (n_qt - 1 - tidx) : tidx;
+    hk = g % p.Hkv;
+    b = g / p.Hkv;
+    h = hk * p.group + rem % p.group;
+  }
   const int q0 = qt * kT;
   const int nkv_all = (p.Nkv + kT - 1) / kT;
   const int n_kv = CAUSAL ? min(nkv_all, qt + 1) : nkv_all;
@@ -427,17 +439,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_kt = (p.Nkv + kT - 1) / kT;
-  // Grid (H_kv, B, key tiles), heads first: under the causal mask key tile 0
-  // sees every query tile, so the longest CTAs all start first.
-  const int kt = static_cast<int>(blockIdx.z);
-  const int hk = blockIdx.x, b = blockIdx.y;
+  // 1-D grid over (group chunk, key tile, group): under the causal mask key
+  // tile 0 sees every query tile, so the longest tiles of a chunk start first.
+  int kt, hk, b;
+  {
+    const int n_groups = p.Hkv * p.B;
+    const int lin = static_cast<int>(blockIdx.x);
+    const int c = lin / (p.chunk_dkv * n_kt);
+    const int gc = min(p.chunk_dkv, n_groups - c * p.chunk_dkv);
+    const int r = lin - c * p.chunk_dkv * n_kt;
+    kt = r / gc;
+    const int g = c * p.chunk_dkv + (r - kt * gc);
+    hk = g % p.Hkv;
+    b = g / p.Hkv;
+  }
   const int kv0 = kt * kT;
   const int n_qt = (p.Nq + kT - 1) / kT;
   // Query tiles that see this key tile: causal (top-left) keeps key j for query i iff j <= i.
   const int i_first = CAUSAL ? min(kv0 / kT, n_qt) : 0;
   const int n_i = n_qt - i_first;
   const int n_steps = n_i * p.group;  // (q head of the group, query tile) pairs
-  (void)n_kt;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_KVF), 1);
@@ -690,7 +711,7 @@ cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv,
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
         cudaSuccess)
       return e;
-    kern<<<dim3(p.Hq, B, (p.Nq + kT - 1) / kT), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
+    kern<<<dim3(p.Hq * B * ((p.Nq + kT - 1) / kT)), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
@@ -699,7 +720,7 @@ cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv,
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
         cudaSuccess)
       return e;
-    kern<<<dim3(Hkv, B, (p.Nkv + kT - 1) / kT), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
+    kern<<<dim3(Hkv * B * ((p.Nkv + kT - 1) / kT)), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
     e = cudaGetLastError();
   }
   return e;
