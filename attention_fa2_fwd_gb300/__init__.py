@@ -485,10 +485,13 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     return dq, dk, dv
 
 
-def decode_workspace(B, H_q, H_kv, D, device=None):
-    """A workspace tensor of attn_decode_workspace_size bytes (None when 0 bytes)."""
+def decode_workspace(B, H_q, H_kv, D, device=None, num_splits: int = 0):
+    """A workspace tensor for attn_fwd_decode (None when it needs 0 bytes): attn_decode_workspace_size bytes,
+    or -- for a forced split count num_splits above the automatic one -- the 4 B H_q n (D + 1) bytes it needs."""
     import torch
     n = attn_decode_workspace_size(B, H_q, H_kv, D)
+    if num_splits > 1:
+        n = max(n, 4 * B * H_q * num_splits * (D + 1))
     if n == 0:
         return None
     return torch.empty((n + 15) // 16 * 4, dtype=torch.float32, device=device or "cuda")

@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import oracle
+import oracle.masked
 from attention_fa2_fwd_gb300 import inputs as I
 from tests.helpers import assert_close, np64
 
@@ -171,7 +172,7 @@ def test_decode_one_split_equals_automatic_split(B):
     qd, kc, vc = q.cuda(), k.cuda(), v.cuda()
     o_auto, l_auto = A.decode(qd, kc, vc, L)
     o_one, l_one = A.decode(qd, kc, vc, L, num_splits=1)
-    ws3 = torch.empty(4 * B * Hq * 3 * (D + 1) // 4, dtype=torch.float32, device="cuda")
+    ws3 = A.decode_workspace(B, Hq, Hkv, D, num_splits=3)
     o_three, l_three = A.decode(qd, kc, vc, L, num_splits=3, workspace=ws3)
     torch.cuda.synchronize()
     A.check_device_error()
@@ -227,3 +228,28 @@ def test_decode_guard_bands(B, L):
     o_ref, lse_ref = oracle.decode(np64(q[:2]), np64(k[:2]), np64(v[:2]), L, 1 / np.sqrt(D))
     assert_close(np64(o)[:2], o_ref, np64(lse)[:2], lse_ref, "guarded")
     assert torch.equal(o2_buf[:, :, 0, :], o)
+
+
+def test_decode_workspace_reused_across_sizes_and_split_counts():
+    """One workspace serves a series of calls with different batch sizes, cache lengths, windows and
+    forced split counts: each result matches the oracle, whatever garbage the workspace holds between calls
+    (its contents need not be initialised)."""
+    import attention_fa2_fwd_gb300 as A
+    Hq, Hkv, D = 32, 8, 128
+    ws = A.decode_workspace(8, Hq, Hkv, D, num_splits=40)
+    cases = [(2, 8192, 0, -1), (8, 3000, 0, -1), (1, 9000, 17, -1), (2, 5000, 40, 700), (8, 300, 3, -1),
+             (2, 8192, 0, -1)]
+    for i, (B, L, splits, wl) in enumerate(cases):
+        k, v = I.decode_stream(B, Hkv, L, D, "bf16", seed=300 + i)
+        q = I.decode_queries(B, Hq, D, [L - 1], "bf16", seed=300 + i)[:, :, 0]
+        ws.view(torch.int32).fill_(0x7fc00000 + i)  # NaN garbage
+        o, lse = A.decode(q.cuda(), k.cuda(), v.cuda(), L, workspace=ws, num_splits=splits, window_left=wl)
+        torch.cuda.synchronize()
+        A.check_device_error()
+        bs = np.arange(min(B, 2))
+        if wl >= 0:
+            o_ref, lse_ref = oracle.masked.decode_masked(np64(q[bs]), np64(k[bs]), np64(v[bs]), L, 1 / np.sqrt(D),
+                                                         window_left=wl)
+        else:
+            o_ref, lse_ref = oracle.decode(np64(q[bs]), np64(k[bs]), np64(v[bs]), L, 1 / np.sqrt(D))
+        assert_close(np64(o)[bs], o_ref, np64(lse)[bs], lse_ref, f"case {i}")

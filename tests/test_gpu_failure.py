@@ -43,10 +43,19 @@ def test_bounded_wait_times_out_and_the_context_stays_usable():
     # a prefill enqueued behind the timed-out kernel sees the error word and computes nothing
     sentinel = torch.full((1, 4, 200, 64), 7.0, dtype=torch.bfloat16, device="cuda")
     A.prefill(qd, kd, vd, causal=True, out=sentinel, return_lse=False)
+    # so does a split decode (split and merge kernels)
+    Bd, Hq, Hkv, Dd, L = 2, 32, 8, 128, 8192
+    kc, vc = (t.cuda() for t in I.decode_stream(Bd, Hkv, L, Dd, "bf16", seed=9))
+    qdec = I.decode_queries(Bd, Hq, Dd, [L - 1], "bf16", seed=9)[:, :, 0].cuda()
+    ws = A.decode_workspace(Bd, Hq, Hkv, Dd)
+    assert A.attn_decode_splits(Bd, Hq, Hkv, L, Dd) > 1
+    dec_sentinel = torch.full((Bd, Hq, Dd), 7.0, dtype=torch.bfloat16, device="cuda")
+    A.decode(qdec, kc, vc, L, out=dec_sentinel, return_lse=False, workspace=ws)
     assert A.attn_get_device_error() == A.ATTN_ERR_DEVICE_TIMEOUT
     waited = time.perf_counter() - t0
     assert 1.0 < waited < 60.0, f"the wait gave up after {waited:.1f} s"
     assert bool((sentinel == 7.0).all()), "a kernel ran while the error word was set"
+    assert bool((dec_sentinel == 7.0).all()), "a decode ran while the error word was set"
 
     # the read cleared the word: the next read is clean and the library computes again
     assert A.attn_get_device_error() == A.ATTN_OK
@@ -54,3 +63,8 @@ def test_bounded_wait_times_out_and_the_context_stays_usable():
     assert A.attn_get_device_error() == A.ATTN_OK
     o_ref, lse_ref = oracle.attention(np64(q), np64(k), np64(v), True, 1 / math.sqrt(64))
     assert_close(o, o_ref, lse, lse_ref, "after a time-out")
+    # and so does the decode, on the same workspace
+    od, ld = A.decode(qdec, kc, vc, L, workspace=ws)
+    assert A.attn_get_device_error() == A.ATTN_OK
+    od_ref, ld_ref = oracle.decode(np64(qdec.cpu()), np64(kc.cpu()), np64(vc.cpu()), L, 1 / math.sqrt(Dd))
+    assert_close(od, od_ref, ld, ld_ref, "decode after a time-out")
