@@ -38,7 +38,10 @@ m = row max, p = exp(s - m), l = sum p, O = p V / l, LSE = m + ln l.
 
 Parity status: pinned by ``tests/test_oracle_masked.py`` against the C oracle
 on band slices, the identity window, closed forms for identical keys, an
-ALiBi-as-extra-dimension construction, and planted-mistake checks.
+ALiBi-as-extra-dimension construction, and planted-mistake checks; the
+backward (``attention_bwd_masked``) against the plain backward oracle without
+options and against central finite differences through ``attention_masked``
+with windows, ALiBi and key ranges.
 """
 from __future__ import annotations
 
@@ -81,6 +84,49 @@ def _softmax_rows(s: np.ndarray, v: np.ndarray):
         o[rows] = (p @ v) / l
         lse[rows] = (m + np.log(l))[:, 0]
     return o, lse
+
+
+def attention_bwd_masked(q, k, v, dout, causal: bool, scale: float, window_left: int = -1, window_right: int = -1,
+                         alibi_slopes=None, kv_ranges=None):
+    """(dQ, dK, dV) of attention_masked for the incoming gradient dout, in fp64.
+
+    With P the masked softmax of S = scale Q K^T - slope_h |i - j| (-inf where
+    masked) and O = P V:  dV = P^T dO,  dP = dO V^T,  dS = P * (dP - rowsum(dO * O)),
+    dQ = scale dS K,  dK = scale dS^T Q.  The bias and the mask do not depend on
+    Q or K, so they enter the gradients only through P; a row with no visible
+    key has P = 0 and contributes nothing.  GQA heads of a group add into their
+    kv head's dK, dV.  q, dout (B,H_q,N_q,D); k, v (B,H_kv,N_kv,D).
+    """
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    group = Hq // Hkv
+    keeps = [visible(Nq, Nkv, causal, window_left, window_right,
+                     None if kv_ranges is None else np.asarray(kv_ranges)[b]) for b in range(B)]
+    dist = np.abs(np.arange(Nq)[:, None] - np.arange(Nkv)[None, :]).astype(np.float64)
+    slopes = None if alibi_slopes is None else np.asarray(alibi_slopes, dtype=np.float64)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // group
+            qb, kb, vb, gb = q[b, h], k[b, hk], v[b, hk], dout[b, h]
+            scores = scale * (qb @ kb.T)
+            if slopes is not None:
+                scores = scores - slopes[h] * dist
+            scores = np.where(keeps[b], scores, -np.inf)
+            prob = np.zeros((Nq, Nkv))
+            live = np.isfinite(scores).any(axis=1)
+            if live.any():
+                sl = scores[live]
+                ex = np.exp(sl - sl.max(axis=1, keepdims=True))
+                prob[live] = ex / ex.sum(axis=1, keepdims=True)
+            out = prob @ vb
+            dv[b, hk] += prob.T @ gb
+            dprob = gb @ vb.T
+            dscore = prob * (dprob - (gb * out).sum(axis=1, keepdims=True))
+            dq[b, h] = scale * (dscore @ kb)
+            dk[b, hk] += scale * (dscore.T @ qb)
+    return dq, dk, dv
 
 
 def attention_masked(q, k, v, causal: bool, scale: float, window_left: int = -1, window_right: int = -1,

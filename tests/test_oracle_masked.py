@@ -340,13 +340,69 @@ def check_varlen_ranges_count_from_sequence_start(mk):
     _close(o[i], o_ref[0], "varlen range row O")
 
 
+def check_bwd_without_options_is_plain_bwd(mk):
+    """No window, bias or ranges: the masked backward is the plain backward oracle."""
+    q, k, v = _qkv(2, 4, 2, 6, 9, 3, "bwd-plain")
+    g = _rng("bwd-plain-g").normal(size=q.shape)
+    for causal in (False, True):
+        got = mk.attention_bwd_masked(q, k, v, g, causal, 0.7)
+        ref = oracle.attention_bwd(q, k, v, g, causal, 0.7)
+        for name, a, b in zip("qkv", got, ref):
+            _close(a, b, f"plain bwd d{name} causal={causal}")
+
+
+def _fd_loss(mk, q, k, v, g, causal, scale, **kw):
+    o, _ = mk.attention_masked(q, k, v, causal, scale, **kw)
+    return float(np.sum(o * g))
+
+
+def check_bwd_matches_finite_differences(mk):
+    """Every gradient entry of a small GQA case with a window, ALiBi and key ranges (one row empty) against
+    central finite differences of L = sum(O * G) through the masked forward."""
+    q, k, v = _qkv(1, 4, 2, 5, 7, 3, "bwd-fd")
+    r = _rng("bwd-fd-g")
+    g = r.normal(size=q.shape)
+    kr = np.array([[[0, 7], [1, 5], [2, 2], [0, 4], [3, 7]]])
+    for causal, kw in ((False, dict(window_left=2, window_right=1, alibi_slopes=[0.5, 0.25, 0.8, 0.1])),
+                       (True, dict(window_left=3, alibi_slopes=[0.3, 0.0, 1.1, 0.7], kv_ranges=kr))):
+        dq, dk, dv = mk.attention_bwd_masked(q, k, v, g, causal, 0.6, **kw)
+        eps = 1e-5
+        for name, grad in (("q", dq), ("k", dk), ("v", dv)):
+            base = {"q": q, "k": k, "v": v}
+            for idx in np.ndindex(base[name].shape):
+                xp, xm = base[name].copy(), base[name].copy()
+                xp[idx] += eps
+                xm[idx] -= eps
+                ap, am = dict(base), dict(base)
+                ap[name], am[name] = xp, xm
+                fd = (_fd_loss(mk, ap["q"], ap["k"], ap["v"], g, causal, 0.6, **kw)
+                      - _fd_loss(mk, am["q"], am["k"], am["v"], g, causal, 0.6, **kw)) / (2 * eps)
+                assert abs(fd - grad[idx]) < 1e-7 * max(1.0, abs(fd)), (name, idx, fd, grad[idx], causal)
+
+
+def check_bwd_empty_row_has_zero_dq(mk):
+    """A query row whose key range is empty gets dQ = 0 and leaves dK, dV as if it were absent."""
+    q, k, v = _qkv(1, 2, 1, 4, 6, 3, "bwd-empty")
+    g = _rng("bwd-empty-g").normal(size=q.shape)
+    kr = np.array([[[0, 6], [2, 2], [1, 4], [0, 6]]])
+    dq, dk, dv = mk.attention_bwd_masked(q, k, v, g, False, 0.9, kv_ranges=kr)
+    if not np.all(dq[:, :, 1] == 0.0):
+        raise AssertionError("empty row has a non-zero dQ")
+    g0 = g.copy()
+    g0[:, :, 1] = 0.0
+    _, dk0, dv0 = mk.attention_bwd_masked(q, k, v, g0, False, 0.9, kv_ranges=kr)
+    _close(dk, dk0, "empty row dK")
+    _close(dv, dv0, "empty row dV")
+
+
 CHECKS = [check_unbounded_window_is_plain, check_band_rows_are_decode_over_slice, check_identity_window,
           check_alibi_zero_slope_is_plain, check_alibi_identical_keys_closed_form,
           check_alibi_causal_is_plain_with_extra_dimension, check_alibi_window_two_sided_by_merge,
           check_decode_is_last_prefill_row, check_decode_alibi_extra_dimension,
           check_paged_is_decode_over_gathered_rows, check_varlen_equal_lengths_is_dense_batch,
           check_range_rows_are_decode_over_slice, check_full_ranges_are_plain, check_block_diagonal_ranges_are_varlen,
-          check_varlen_ranges_count_from_sequence_start]
+          check_varlen_ranges_count_from_sequence_start, check_bwd_without_options_is_plain_bwd,
+          check_bwd_matches_finite_differences, check_bwd_empty_row_has_zero_dq]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=[c.__name__ for c in CHECKS])
@@ -377,6 +433,13 @@ MUTANTS = {
     "ranges of batch 0 for every batch": ("None if kv_ranges is None else np.asarray(kv_ranges)[b]",
                                           "None if kv_ranges is None else np.asarray(kv_ranges)[0]"),
     "varlen ranges of the wrong rows": ("np.asarray(kv_ranges)[qs:qe][None]", "np.asarray(kv_ranges)[:qe - qs][None]"),
+    "bwd rowsum term dropped": ("dscore = prob * (dprob - (gb * out).sum(axis=1, keepdims=True))",
+                                "dscore = prob * dprob"),
+    "bwd dK without the scale": ("dk[b, hk] += scale * (dscore.T @ qb)", "dk[b, hk] += dscore.T @ qb"),
+    "bwd dV of the unnormalised P": ("prob[live] = ex / ex.sum(axis=1, keepdims=True)", "prob[live] = ex"),
+    "bwd bias ignored": ("                scores = scores - slopes[h] * dist", "                scores = scores"),
+    "bwd mask ignored": ("scores = np.where(keeps[b], scores, -np.inf)", "scores = scores"),
+    "bwd dK of the first head only": ("dk[b, hk] += scale", "dk[b, hk] = scale"),
     "varlen keys of the next sequence": ("kb = k[ks:ke]", "kb = k[ke:ke + (ke - ks)] if ke + (ke - ks) <= len(k) "
                                                           "else k[ks:ke][::-1]"),
 }
