@@ -39,7 +39,7 @@ EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_ex", "attn_fwd_prefill_host", "
            "attn_fwd_decode_ex", "attn_fwd_decode_paged_ex", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
            "attn_fwd_decode_noalloc", "kv_cache_write", "kv_cache_write_ex", "attn_fwd_decode_paged",
            "kv_cache_write_paged", "kv_cache_write_paged_ex",
-           "attn_bwd_workspace_size", "attn_bwd",
+           "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_ex",
            "attn_get_device_error", "attn_selftest_wait_timeout", "attn_status_string", "attn_version")
 
 
@@ -138,6 +138,10 @@ def lib() -> ctypes.CDLL:
             L.attn_bwd.restype = i32
             L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                    i64p, i64p, i64p, i64p, i64p, i64p, i64p, i64p, i32, f32, vp, ctypes.c_size_t, vp]
+            L.attn_bwd_ex.restype = i32
+            L.attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                      i64p, i64p, i64p, i64p, i64p, i64p, i64p, i64p, i32, f32, vp, vp,
+                                      ctypes.c_size_t, vp]
             L.attn_get_device_error.restype = i32
             L.attn_get_device_error.argtypes = [vp]
             L.attn_selftest_wait_timeout.restype = i32
@@ -325,6 +329,14 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, dtype, B, H_q, H_kv, N_q, N_kv, 
                           stream)
 
 
+def attn_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, k_str, v_str, o_str,
+                do_str, dq_str, dk_str, dv_str, causal, scale, opts, workspace, workspace_bytes, stream) -> int:
+    return lib().attn_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, dtype, B, H_q, H_kv, N_q, N_kv, D, _strides(q_str),
+                             _strides(k_str), _strides(v_str), _strides(o_str), _strides(do_str), _strides(dq_str),
+                             _strides(dk_str), _strides(dv_str), int(causal), float(scale), _opts(opts), workspace,
+                             workspace_bytes, stream)
+
+
 def attn_get_device_error(stream=None) -> int:
     return lib().attn_get_device_error(stream)
 
@@ -460,10 +472,12 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_s
     return o, lse
 
 
-def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None, stream=None):
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None, stream=None,
+             window=(-1, -1), alibi_slopes=None, kv_ranges=None):
     """Gradients (dQ, dK, dV) of attn_fwd_prefill from its output O and LSE and the incoming dO.
 
-    Shapes as for prefill; dK, dV are summed over each GQA group.  Returns new contiguous tensors.
+    Shapes as for prefill; dK, dV are summed over each GQA group.  window, alibi_slopes and kv_ranges must be
+    those of the forward call.  Returns new contiguous tensors.
     """
     import torch
     B, Hq, Nq, D = q.shape
@@ -476,11 +490,11 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     n = attn_bwd_workspace_size(B, Hq, Nq)
     if workspace is None:
         workspace = torch.empty((n + 3) // 4, dtype=torch.float32, device=q.device)
-    st = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, q.stride(),
-                  k.stride(), v.stride(), o.stride(), dout.stride(), dq.stride(), dk.stride(), dv.stride(),
-                  1 if causal else 0, scale, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                  _stream_handle(stream))
+    st = attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, q.stride(),
+                     k.stride(), v.stride(), o.stride(), dout.stride(), dq.stride(), dk.stride(), dv.stride(),
+                     1 if causal else 0, scale, make_options(window[0], window[1], alibi_slopes, kv_ranges=kv_ranges),
+                     workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "attn_bwd")
     return dq, dk, dv
 

@@ -513,6 +513,17 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
                        const int64_t v_str[4], const int64_t o_str[4], const int64_t do_str[4],
                        const int64_t dq_str[4], const int64_t dk_str[4], const int64_t dv_str[4], int causal,
                        float scale, void *workspace, size_t workspace_bytes, void *stream) {
+  return attn_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, k_str, v_str, o_str,
+                     do_str, dq_str, dk_str, dv_str, causal, scale, nullptr, workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                          const float *lse, void *dq, void *dk, void *dv, attn_dtype_t dtype, int B, int H_q,
+                          int H_kv, int N_q, int N_kv, int D, const int64_t q_str[4], const int64_t k_str[4],
+                          const int64_t v_str[4], const int64_t o_str[4], const int64_t do_str[4],
+                          const int64_t dq_str[4], const int64_t dk_str[4], const int64_t dv_str[4], int causal,
+                          float scale, const attn_options_t *opts, void *workspace, size_t workspace_bytes,
+                          void *stream) {
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !q_str || !k_str || !v_str || !o_str ||
       !do_str || !dq_str || !dk_str || !dv_str)
     return ATTN_ERR_INVALID_ARG;
@@ -533,6 +544,9 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
       (st = check_strides(o_str, qsz)) || (st = check_strides(do_str, qsz)) || (st = check_strides(dq_str, qsz)) ||
       (st = check_strides(dk_str, kvsz)) || (st = check_strides(dv_str, kvsz)))
     return st;
+  Opts op;
+  if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
+  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;  // no rotary embeddings in the backward
   const size_t need = attn_bwd_workspace_size(B, H_q, N_q);
   if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 15) != 0) return ATTN_ERR_ALIGNMENT;
@@ -541,6 +555,11 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
   const bool bf16 = dtype == ATTN_BF16;
   BwdMaps m;
   BwdParams p{};
+  p.window_left = op.wl;
+  p.window_right = op.wr;
+  p.alibi_slopes = op.slopes;
+  p.kv_ranges = op.kv_ranges;
+  const bool masked = op.wl >= 0 || (causal == 0 && op.wr >= 0) || op.slopes != nullptr || op.kv_ranges != nullptr;
   if ((st = make_map(&m.q, q, bf16, qsz, q_str, 128, &p.slots_q)) ||
       (st = make_map(&m.dout, dout, bf16, qsz, do_str, 128, &p.slots_do)) ||
       (st = make_map(&m.k, k, bf16, kvsz, k_str, 128, &p.slots_k)) ||
@@ -578,7 +597,7 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
   p.B = B;
   p.Hkv = H_kv;
   bwd_chunks(&p, D, causal != 0);
-  cudaError_t e = launch_bwd(D, causal != 0, bf16, m, p, B, H_kv, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_bwd(D, causal != 0, bf16, masked, m, p, B, H_kv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

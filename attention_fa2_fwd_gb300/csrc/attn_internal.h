@@ -153,11 +153,20 @@ struct BwdParams {
   // of a chunk first, so that the CTAs in flight share a few groups' operands
   // in L2 (Q and dO of a group's heads for dK/dV, K and V for dQ).
   int B, Hkv, chunk_dq, chunk_dkv;
+  // Masks and bias of the forward (masked build only), as in PrefillParams:
+  // window bounds (-1: none), ALiBi slopes (device fp32, H_q), per-row key
+  // ranges (device int32 pairs, (B, N_q, 2)).
+  int window_left, window_right;
+  const float *alibi_slopes;
+  const int32_t *kv_ranges;
 };
 struct BwdMaps {
   CUtensorMap q, dout, k, v;  // 4-D tiled maps, 64 x 128 boxes, 128-byte swizzle
 };
-cudaError_t launch_bwd(int D, bool causal, bool bf16, const BwdMaps &m, const BwdParams &p, int B, int Hkv,
-                       cudaStream_t stream);
+// masked: a window, ALiBi slopes or key ranges are set (the MASKED build).
+cudaError_t launch_bwd(int D, bool causal, bool bf16, bool masked, const BwdMaps &m, const BwdParams &p, int B,
+                       int Hkv, cudaStream_t stream);
+cudaError_t launch_bwd_masked(int D, bool causal, bool bf16, const BwdMaps &m, const BwdParams &p, int B, int Hkv,
+                              cudaStream_t stream);
 
 }  // namespace attn

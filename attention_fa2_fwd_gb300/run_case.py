@@ -117,14 +117,18 @@ def main():
         B = a.B or 2
         q, k, v = randn(B, a.Hq, a.N, a.D), randn(B, a.Hkv, a.N, a.D), randn(B, a.Hkv, a.N, a.D)
         dout = randn(B, a.Hq, a.N, a.D)
-        o, lse = A.prefill(q, k, v, causal=bool(a.causal))
+        mk = dict(window=(wl, -1), alibi_slopes=slopes)  # the forward's masks, passed to the backward too
+        o, lse = A.prefill(q, k, v, causal=bool(a.causal), **mk)
         nbytes = A.attn_bwd_workspace_size(B, a.Hq, a.N)
         ws = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=dev)
-        # five matrix products of the forward's size (S, dP, dV, dK, dQ): 2.5 x its FLOPs
-        work = 2.5 * 4.0 * B * a.Hq * a.N * a.N * a.D / (2 if a.causal else 1)
+        # five matrix products of the forward's size (S, dP, dV, dK, dQ) over the visible pairs: 2.5 x its FLOPs
+        i = torch.arange(a.N, dtype=torch.float64)
+        hi = i if a.causal else torch.full_like(i, a.N - 1)
+        lo = torch.clamp(i - wl, min=0) if wl >= 0 else torch.zeros_like(i)
+        work = 2.5 * 4.0 * B * a.Hq * a.D * float((hi - lo + 1).sum())
 
         def call():
-            A.backward(q, k, v, o, lse, dout, causal=bool(a.causal), workspace=ws)
+            A.backward(q, k, v, o, lse, dout, causal=bool(a.causal), workspace=ws, **mk)
         unit, scale = "TFLOPS", 1e12
     elif a.kind == "decode_paged":
         B = a.B or 64

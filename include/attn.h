@@ -271,6 +271,24 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
                        float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * attn_bwd with the forward's mask and bias options (see attn_options_t):
+ * window_left, window_right, alibi_slopes and kv_ranges, the same as the
+ * attn_fwd_prefill_ex call whose O and LSE are passed in (a query row the
+ * forward left without keys, O = 0 and LSE = -inf, gets dQ = 0 and adds
+ * nothing to dK, dV).  The bias enters the gradients only through P.  Rotary
+ * embeddings (rope_theta > 0) are not supported here (ATTN_ERR_UNSUPPORTED);
+ * num_splits and prefill_kernel must be 0.  Option errors as for the other
+ * *_ex calls.
+ */
+attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                          const float *lse, void *dq, void *dk, void *dv, attn_dtype_t dtype, int B, int H_q,
+                          int H_kv, int N_q, int N_kv, int D, const int64_t q_str[4], const int64_t k_str[4],
+                          const int64_t v_str[4], const int64_t o_str[4], const int64_t do_str[4],
+                          const int64_t dq_str[4], const int64_t dk_str[4], const int64_t dv_str[4], int causal,
+                          float scale, const attn_options_t *opts, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
  * attn_decode_workspace_size -- bytes of scratch attn_fwd_decode needs.
  *
  * Split-KV decode writes one partial output (D fp32) and one partial LSE per

@@ -264,6 +264,10 @@ OPTION_CALLS = {
     "decode_paged": lambda o: A.attn_fwd_decode_paged_ex(
         P, P, P, P, None, A.ATTN_BF16, 2, 32, 8, 128, 100, 16, P, 64, 64, P, 1000, contig(2, 32, 1, 128),
         contig(100, 8, 16, 128), contig(100, 8, 16, 128), contig(2, 32, 1, 128), 0.088, P, 1 << 30, o, None),
+    "bwd": lambda o: A.attn_bwd_ex(
+        P, P, P, P, P, P, P, P, P, A.ATTN_BF16, 2, 8, 2, 64, 64, 128, contig(2, 8, 64, 128), contig(2, 2, 64, 128),
+        contig(2, 2, 64, 128), contig(2, 8, 64, 128), contig(2, 8, 64, 128), contig(2, 8, 64, 128),
+        contig(2, 2, 64, 128), contig(2, 2, 64, 128), 1, 0.088, o, P, 1 << 20, None),
     "cache_write": lambda o: A.kv_cache_write_ex(
         P, P, P, P, A.ATTN_BF16, 2, 8, 1, 128, 10, 256, contig(2, 8, 256, 128), contig(2, 8, 256, 128),
         contig(2, 8, 1, 128), contig(2, 8, 1, 128), o, None),
