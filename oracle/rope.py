@@ -32,7 +32,10 @@ Every function rotates explicitly in fp64 and then calls the plain C oracle
 Parity status: pinned by ``tests/test_oracle_rope.py`` against hand-derived
 rotations (``tests/golden/rope_d4.json``), closed forms for D = 2, a matrix
 formulation of the rotation, the relative-position property, norm
-preservation, decode = last causal prefill row, and planted-mistake checks.
+preservation, decode = last causal prefill row, and planted-mistake checks;
+the backward (``attention_bwd``) against central finite differences through
+``attention`` (both layouts, windows and ALiBi, keys given rotated) and the
+plain backward at position 0.
 """
 from __future__ import annotations
 
@@ -92,6 +95,31 @@ def attention(q, k, v, causal: bool, scale: float, theta: float, interleaved: bo
     if _plain(window_left, window_right, alibi_slopes):
         return oracle.attention(qr, kr, v, causal, scale)
     return masked.attention_masked(qr, kr, v, causal, scale, window_left, window_right, alibi_slopes)
+
+
+def attention_bwd(q, k, v, dout, causal: bool, scale: float, theta: float, interleaved: bool = False,
+                  rotated_keys: bool = False, window_left: int = -1, window_right: int = -1, alibi_slopes=None):
+    """(dQ, dK, dV) of ``attention`` (queries and keys rotated at their positions) for the incoming
+    gradient dout, in fp64.
+
+    With R the per-row rotation, the forward is attention(R q, R k, v); the gradients of attention with
+    respect to its rotated inputs (dQ', dK', dV) come from the backward oracles, and by the chain rule
+    dQ = R^T dQ', dK = R^T dK' -- R is orthogonal, so R^T is the rotation by the opposite angle -- while
+    dV is unchanged.  rotated_keys: the keys were given already rotated (not rotated here), so dK is the
+    gradient with respect to those rotated keys, dK'.
+    """
+    q, k = _f64(q), _f64(k)
+    qpos, kpos = np.arange(q.shape[2]), np.arange(k.shape[2])
+    qr = rotate(q, qpos, theta, interleaved)
+    kr = k if rotated_keys else rotate(k, kpos, theta, interleaved)
+    if _plain(window_left, window_right, alibi_slopes):
+        dqr, dkr, dv = oracle.attention_bwd(qr, kr, v, dout, causal, scale)
+    else:
+        dqr, dkr, dv = masked.attention_bwd_masked(qr, kr, v, dout, causal, scale, window_left, window_right,
+                                                   alibi_slopes)
+    dq = rotate(dqr, -qpos, theta, interleaved)
+    dk = dkr if rotated_keys else rotate(dkr, -kpos, theta, interleaved)
+    return dq, dk, dv
 
 
 def kv_cache_write(k_cache, v_cache, k_new, v_new, pos: int, theta: float, interleaved: bool = False):

@@ -206,9 +206,60 @@ def check_varlen_positions_per_sequence(R):
             assert np.allclose(lse[:, qs:qe], lb[0], atol=TOL)
 
 
+def _fd_check(R, grads, loss, base, what):
+    """Every entry of grads (dict name -> array) against central differences of loss(**inputs)."""
+    eps = 1e-5
+    for name, grad in grads.items():
+        for idx in np.ndindex(base[name].shape):
+            xp, xm = base[name].copy(), base[name].copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            ap, am = dict(base), dict(base)
+            ap[name], am[name] = xp, xm
+            fd = (loss(**ap) - loss(**am)) / (2 * eps)
+            assert abs(fd - grad[idx]) < 1e-7 * max(1.0, abs(fd)), (what, name, idx, fd, grad[idx])
+
+
+def check_bwd_matches_finite_differences(R):
+    """Gradients of the rotary attention against central finite differences through ``attention`` (both
+    pair layouts, causal and windowed + ALiBi) and, with keys given rotated, through attention of the
+    rotated queries over those keys."""
+    r = _rng("bwd-fd")
+    B, Hq, Hkv, Nq, Nkv, D = 1, 2, 1, 4, 6, 4
+    q, k, v = r.normal(size=(B, Hq, Nq, D)), r.normal(size=(B, Hkv, Nkv, D)), r.normal(size=(B, Hkv, Nkv, D))
+    g = r.normal(size=q.shape)
+    base = {"q": q, "k": k, "v": v}
+    for inter, causal, kw in ((False, True, {}), (True, False, dict(window_left=2, window_right=1,
+                                                                   alibi_slopes=[0.4, 0.15]))):
+        dq, dk, dv = R.attention_bwd(q, k, v, g, causal, 0.7, 100.0, inter, **kw)
+
+        def loss(q, k, v):
+            o, _ = R.attention(q, k, v, causal, 0.7, 100.0, inter, **kw)
+            return float(np.sum(o * g))
+        _fd_check(R, {"q": dq, "k": dk, "v": dv}, loss, base, f"inter={inter}")
+    dq, dk, dv = R.attention_bwd(q, k, v, g, True, 0.7, 100.0, False, rotated_keys=True)
+
+    def loss_rk(q, k, v):
+        o, _ = oracle.attention(R.rotate(q, np.arange(Nq), 100.0), k, v, True, 0.7)
+        return float(np.sum(o * g))
+    _fd_check(R, {"q": dq, "k": dk, "v": dv}, loss_rk, base, "rotated keys")
+
+
+def check_bwd_at_position_zero_is_plain(R):
+    """One query and one key at position 0: no rotation, so the plain backward."""
+    r = _rng("bwd-p0")
+    q, k, v, g = (r.normal(size=(2, 4, 1, 8)), r.normal(size=(2, 2, 1, 8)), r.normal(size=(2, 2, 1, 8)),
+                  r.normal(size=(2, 4, 1, 8)))
+    got = R.attention_bwd(q, k, v, g, True, 0.3, 10000.0)
+    ref = oracle.attention_bwd(q, k, v, g, True, 0.3)
+    for a, b in zip(got, ref):
+        assert np.allclose(a, b, atol=TOL)
+
+
 CHECKS = [check_golden_d4, check_complex_formulation, check_d2_closed_forms, check_norm_and_relative_position,
           check_attention_is_plain_on_rotated_rows, check_gqa_is_mha_expanded, check_cache_write_rotates_keys_only,
-          check_decode_is_last_prefill_row, check_paged_equals_dense, check_varlen_positions_per_sequence]
+          check_decode_is_last_prefill_row, check_paged_equals_dense, check_varlen_positions_per_sequence,
+          check_bwd_matches_finite_differences, check_bwd_at_position_zero_is_plain]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=[c.__name__ for c in CHECKS])
@@ -234,6 +285,15 @@ MUTANTS = {
     "paged write one position late": ("int(positions[b]) + np.arange(k_new.shape[2])",
                                       "int(positions[b]) + 1 + np.arange(k_new.shape[2])"),
     "paged decode query at the length": ("[int(cache_lens[b]) - 1]", "[int(cache_lens[b])]"),
+    "bwd dQ not rotated back": ("dq = rotate(dqr, -qpos, theta, interleaved)", "dq = dqr"),
+    "bwd dQ rotated forward again": ("dq = rotate(dqr, -qpos, theta, interleaved)",
+                                     "dq = rotate(dqr, qpos, theta, interleaved)"),
+    "bwd dK not rotated back": ("dk = dkr if rotated_keys else rotate(dkr, -kpos, theta, interleaved)", "dk = dkr"),
+    "bwd rotated keys rotated again": ("kr = k if rotated_keys else rotate(k, kpos, theta, interleaved)",
+                                       "kr = rotate(k, kpos, theta, interleaved)"),
+    "bwd keys rotated at query positions": ("kr = k if rotated_keys else rotate(k, kpos, theta, interleaved)",
+                                            "kr = k if rotated_keys else rotate(k, np.arange(k.shape[2]) + 1, "
+                                            "theta, interleaved)"),
 }
 
 
