@@ -39,7 +39,7 @@ EXPORTS = ("attn_fwd_prefill", "attn_fwd_prefill_ex", "attn_fwd_prefill_host", "
            "attn_fwd_decode_ex", "attn_fwd_decode_paged_ex", "attn_decode_workspace_size", "attn_decode_splits", "attn_fwd_decode",
            "attn_fwd_decode_noalloc", "kv_cache_write", "kv_cache_write_ex", "attn_fwd_decode_paged",
            "kv_cache_write_paged", "kv_cache_write_paged_ex",
-           "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_ex",
+           "attn_bwd_workspace_size", "attn_bwd_ex_workspace_size", "attn_bwd", "attn_bwd_ex",
            "attn_get_device_error", "attn_selftest_wait_timeout", "attn_status_string", "attn_version")
 
 
@@ -135,6 +135,8 @@ def lib() -> ctypes.CDLL:
                                                   vp, i64p, i64p, i64p, i64p, optp, vp]
             L.attn_bwd_workspace_size.restype = ctypes.c_size_t
             L.attn_bwd_workspace_size.argtypes = [i32, i32, i32]
+            L.attn_bwd_ex_workspace_size.restype = ctypes.c_size_t
+            L.attn_bwd_ex_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, optp]
             L.attn_bwd.restype = i32
             L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                    i64p, i64p, i64p, i64p, i64p, i64p, i64p, i64p, i32, f32, vp, ctypes.c_size_t, vp]
@@ -321,6 +323,10 @@ def attn_bwd_workspace_size(B, H_q, N_q) -> int:
     return int(lib().attn_bwd_workspace_size(B, H_q, N_q))
 
 
+def attn_bwd_ex_workspace_size(B, H_q, H_kv, N_q, N_kv, D, opts) -> int:
+    return int(lib().attn_bwd_ex_workspace_size(B, H_q, H_kv, N_q, N_kv, D, _opts(opts)))
+
+
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, dtype, B, H_q, H_kv, N_q, N_kv, D, q_str, k_str, v_str, o_str,
              do_str, dq_str, dk_str, dv_str, causal, scale, workspace, workspace_bytes, stream) -> int:
     return lib().attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, dtype, B, H_q, H_kv, N_q, N_kv, D, _strides(q_str),
@@ -473,11 +479,13 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_s
 
 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None, stream=None,
-             window=(-1, -1), alibi_slopes=None, kv_ranges=None):
+             window=(-1, -1), alibi_slopes=None, kv_ranges=None, rope_theta: float = 0.0,
+             rope_interleaved: bool = False, rope_rotated_keys: bool = False):
     """Gradients (dQ, dK, dV) of attn_fwd_prefill from its output O and LSE and the incoming dO.
 
-    Shapes as for prefill; dK, dV are summed over each GQA group.  window, alibi_slopes and kv_ranges must be
-    those of the forward call.  Returns new contiguous tensors.
+    Shapes as for prefill; dK, dV are summed over each GQA group.  window, alibi_slopes, kv_ranges and the
+    rope_* options must be those of the forward call (with rope_rotated_keys, dK is the gradient with respect
+    to the rotated keys passed in).  Returns new contiguous tensors.
     """
     import torch
     B, Hq, Nq, D = q.shape
@@ -487,14 +495,15 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     dq = torch.empty((B, Hq, Nq, D), dtype=q.dtype, device=q.device)
     dk = torch.empty((B, Hkv, Nkv, D), dtype=q.dtype, device=q.device)
     dv = torch.empty((B, Hkv, Nkv, D), dtype=q.dtype, device=q.device)
-    n = attn_bwd_workspace_size(B, Hq, Nq)
+    opts = make_options(window[0], window[1], alibi_slopes, kv_ranges=kv_ranges, rope_theta=rope_theta,
+                        rope_interleaved=rope_interleaved, rope_rotated_keys=rope_rotated_keys)
+    n = attn_bwd_ex_workspace_size(B, Hq, Hkv, Nq, Nkv, D, opts)
     if workspace is None:
-        workspace = torch.empty((n + 3) // 4, dtype=torch.float32, device=q.device)
+        workspace = torch.empty((n + 15) // 16 * 4, dtype=torch.float32, device=q.device)
     st = attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, q.stride(),
                      k.stride(), v.stride(), o.stride(), dout.stride(), dq.stride(), dk.stride(), dv.stride(),
-                     1 if causal else 0, scale, make_options(window[0], window[1], alibi_slopes, kv_ranges=kv_ranges),
-                     workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+                     1 if causal else 0, scale, opts, workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "attn_bwd")
     return dq, dk, dv
 

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libattn_gb300.so")
 OBJDIR = os.path.join(PKG, "_build")
 SOURCES = ["attn_api.cu", "prefill.cu", "prefill_pair.cu", "prefill_masked.cu", "prefill_rope.cu", "prefill_rope_masked.cu",
-           "decode.cu", "bwd.cu", "bwd_masked.cu"]
+           "decode.cu", "bwd.cu", "bwd_masked.cu", "rope_rows.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

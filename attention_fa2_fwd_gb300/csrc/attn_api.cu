@@ -507,6 +507,30 @@ size_t attn_bwd_workspace_size(int B, int H_q, int N_q) {
   return (static_cast<size_t>(B) * H_q * N_q * sizeof(float) + 15) & ~size_t(15);
 }
 
+namespace {
+// Backward workspace: D_i (fp32 per query row), then, with rotary embeddings,
+// the rotated queries Q' (B, H_q, N_q, D) and -- unless the keys come rotated
+// -- the rotated keys K' (B, H_kv, N_kv, D), both contiguous 16-bit rows.
+struct BwdWorkspace {
+  size_t q_off, k_off, total;
+};
+BwdWorkspace bwd_workspace(int B, int H_q, int H_kv, int N_q, int N_kv, int D, bool rope, bool rotate_k) {
+  BwdWorkspace w;
+  w.q_off = attn_bwd_workspace_size(B, H_q, N_q);
+  w.k_off = w.q_off + (rope ? static_cast<size_t>(B) * H_q * N_q * D * 2 : 0);
+  w.total = w.k_off + (rope && rotate_k ? static_cast<size_t>(B) * H_kv * N_kv * D * 2 : 0);
+  return w;
+}
+}  // namespace
+
+size_t attn_bwd_ex_workspace_size(int B, int H_q, int H_kv, int N_q, int N_kv, int D, const attn_options_t *opts) {
+  if (B < 1 || H_q < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || H_q % H_kv != 0 || (D != 64 && D != 128)) return 0;
+  Opts op;
+  if (read_opts(opts, &op) != ATTN_OK) return 0;
+  const bool rope = op.rope_theta > 0.f;
+  return bwd_workspace(B, H_q, H_kv, N_q, N_kv, D, rope, rope && !op.rope_rotated_keys).total;
+}
+
 attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
                        const float *lse, void *dq, void *dk, void *dv, attn_dtype_t dtype, int B, int H_q, int H_kv,
                        int N_q, int N_kv, int D, const int64_t q_str[4], const int64_t k_str[4],
@@ -546,9 +570,9 @@ attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, const voi
     return st;
   Opts op;
   if ((st = read_opts(opts, &op)) != ATTN_OK) return st;
-  if (op.rope_theta > 0.f) return ATTN_ERR_UNSUPPORTED;  // no rotary embeddings in the backward
-  const size_t need = attn_bwd_workspace_size(B, H_q, N_q);
-  if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  const bool rope = op.rope_theta > 0.f, rotate_k = rope && !op.rope_rotated_keys;
+  const BwdWorkspace ws = bwd_workspace(B, H_q, H_kv, N_q, N_kv, D, rope, rotate_k);
+  if (workspace == nullptr || workspace_bytes < ws.total) return ATTN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 15) != 0) return ATTN_ERR_ALIGNMENT;
   const DeviceState *dev = nullptr;
   if ((st = device_state(&dev)) != ATTN_OK) return st;
@@ -560,9 +584,31 @@ attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, const voi
   p.alibi_slopes = op.slopes;
   p.kv_ranges = op.kv_ranges;
   const bool masked = op.wl >= 0 || (causal == 0 && op.wr >= 0) || op.slopes != nullptr || op.kv_ranges != nullptr;
-  if ((st = make_map(&m.q, q, bf16, qsz, q_str, 128, &p.slots_q)) ||
+  // Rotary embeddings: the kernels run on Q' = R Q and K' = R K, rotated into
+  // the workspace first; dQ and dK are turned back by R^T in place at the end.
+  const void *q_in = q, *k_in = k;
+  const int64_t *q_in_str = q_str, *k_in_str = k_str;
+  const int64_t qr_str[4] = {static_cast<int64_t>(H_q) * N_q * D, static_cast<int64_t>(N_q) * D, D, 1};
+  const int64_t kr_str[4] = {static_cast<int64_t>(H_kv) * N_kv * D, static_cast<int64_t>(N_kv) * D, D, 1};
+  RopeRowsParams rp{};
+  if (rope) {
+    char *base = static_cast<char *>(workspace);
+    rp.B = B;
+    fill_rope_steps(op.rope_theta, D, rp.rope_f);
+    rp.job[0] = RopeRowsJob{q, base + ws.q_off, q_str[0], q_str[1], q_str[2], qr_str[0], qr_str[1], qr_str[2],
+                            H_q, N_q};
+    q_in = base + ws.q_off;
+    q_in_str = qr_str;
+    if (rotate_k) {
+      rp.job[1] = RopeRowsJob{k, base + ws.k_off, k_str[0], k_str[1], k_str[2], kr_str[0], kr_str[1], kr_str[2],
+                              H_kv, N_kv};
+      k_in = base + ws.k_off;
+      k_in_str = kr_str;
+    }
+  }
+  if ((st = make_map(&m.q, q_in, bf16, qsz, q_in_str, 128, &p.slots_q)) ||
       (st = make_map(&m.dout, dout, bf16, qsz, do_str, 128, &p.slots_do)) ||
-      (st = make_map(&m.k, k, bf16, kvsz, k_str, 128, &p.slots_k)) ||
+      (st = make_map(&m.k, k_in, bf16, kvsz, k_in_str, 128, &p.slots_k)) ||
       (st = make_map(&m.v, v, bf16, kvsz, v_str, 128, &p.slots_v)))
     return st;
   p.o = o;
@@ -597,7 +643,22 @@ attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, const voi
   p.B = B;
   p.Hkv = H_kv;
   bwd_chunks(&p, D, causal != 0);
-  cudaError_t e = launch_bwd(D, causal != 0, bf16, masked, m, p, B, H_kv, static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (rope) {
+    rp.sin_sign = 1.f;
+    e = launch_rope_rows(D, bf16, op.rope_interleaved != 0, rp, rotate_k ? 2 : 1, s);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  e = launch_bwd(D, causal != 0, bf16, masked, m, p, B, H_kv, s);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (rope) {
+    // dQ = R^T dQ', dK = R^T dK' (dK' itself when the keys came rotated).
+    rp.sin_sign = -1.f;
+    rp.job[0] = RopeRowsJob{dq, dq, dq_str[0], dq_str[1], dq_str[2], dq_str[0], dq_str[1], dq_str[2], H_q, N_q};
+    rp.job[1] = RopeRowsJob{dk, dk, dk_str[0], dk_str[1], dk_str[2], dk_str[0], dk_str[1], dk_str[2], H_kv, N_kv};
+    e = launch_rope_rows(D, bf16, op.rope_interleaved != 0, rp, rotate_k ? 2 : 1, s);
+  }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -169,4 +169,24 @@ cudaError_t launch_bwd(int D, bool causal, bool bf16, bool masked, const BwdMaps
 cudaError_t launch_bwd_masked(int D, bool causal, bool bf16, const BwdMaps &m, const BwdParams &p, int B, int Hkv,
                               cudaStream_t stream);
 
+// Rotary embedding of whole rows (rope_rows.cu): job j rotates the (B, H, N, D)
+// 16-bit tensor src into dst (the same place for an in-place rotation), the row
+// at sequence index n by n times each pair's turn step; sin_sign -1 applies the
+// inverse rotation.  Element strides; the d stride is 1 and every row starts on
+// 16 bytes.
+struct RopeRowsJob {
+  const void *src;
+  void *dst;
+  int64_t s_sb, s_sh, s_sn, d_sb, d_sh, d_sn;
+  int H, N;
+};
+struct RopeRowsParams {
+  RopeRowsJob job[2];
+  int B;
+  float sin_sign;
+  uint64_t rope_f[64];  // pair turn steps, as in PrefillParams
+};
+cudaError_t launch_rope_rows(int D, bool bf16, bool interleaved, const RopeRowsParams &p, int n_jobs,
+                             cudaStream_t stream);
+
 }  // namespace attn

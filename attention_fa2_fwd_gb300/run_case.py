@@ -9,7 +9,8 @@
     python -m attention_fa2_fwd_gb300.run_case cross   [--D 64|128: the cross-attention workload, B=4 H_q=16
                                                         H_kv=4 N_q=1024 N_kv=4096, (B,N,H,D) memory, non-causal]
     prefill / decode / decode_paged also take --window-left W and --alibi 1 (sliding window, ALiBi slopes)
-    prefill / varlen / cross / decode / decode_paged take --rope THETA [--rope-interleaved 1] (rotary embeddings)
+    prefill / varlen / cross / decode / decode_paged / bwd take --rope THETA [--rope-interleaved 1] (rotary
+    embeddings; prefill and bwd also --rope-rotated-keys 1)
     decode / decode_paged take --graph 1: the step (cache write of one token + decode) captured once in a
     CUDA graph and replayed, against the same calls launched one by one
 
@@ -47,7 +48,7 @@ def main():
     ap.add_argument("--graph", type=int, default=0, help="decode: time a one-token serving step, eager vs CUDA graph")
     ap.add_argument("--rope", type=float, default=0.0, help="rotary embeddings of this base (0: none)")
     ap.add_argument("--rope-interleaved", type=int, default=0, help="rotary pairs (2c, 2c+1) instead of (c, c+D/2)")
-    ap.add_argument("--rope-rotated-keys", type=int, default=0, help="prefill: keys given already rotated")
+    ap.add_argument("--rope-rotated-keys", type=int, default=0, help="prefill, bwd: keys given already rotated")
     ap.add_argument("--num-splits", type=int, default=0, help="decode: force at most this many KV splits (0: auto)")
     ap.add_argument("--prefill-kernel", type=int, default=0,
                     help="prefill / cross: 0 automatic, 1 one-CTA kernel, 2 CTA-pair kernel")
@@ -117,10 +118,13 @@ def main():
         B = a.B or 2
         q, k, v = randn(B, a.Hq, a.N, a.D), randn(B, a.Hkv, a.N, a.D), randn(B, a.Hkv, a.N, a.D)
         dout = randn(B, a.Hq, a.N, a.D)
-        mk = dict(window=(wl, -1), alibi_slopes=slopes)  # the forward's masks, passed to the backward too
+        # the forward's masks and rotary embedding, passed to the backward too
+        mk = dict(window=(wl, -1), alibi_slopes=slopes, rope_theta=a.rope, rope_interleaved=bool(a.rope_interleaved),
+                  rope_rotated_keys=bool(a.rope_rotated_keys))
         o, lse = A.prefill(q, k, v, causal=bool(a.causal), **mk)
-        nbytes = A.attn_bwd_workspace_size(B, a.Hq, a.N)
-        ws = torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=dev)
+        nbytes = A.attn_bwd_ex_workspace_size(B, a.Hq, a.Hkv, a.N, a.N, a.D,
+                                              A.make_options(rope_theta=a.rope, rope_rotated_keys=bool(a.rope_rotated_keys)))
+        ws = torch.empty((nbytes + 15) // 16 * 4, dtype=torch.float32, device=dev)
         # five matrix products of the forward's size (S, dP, dV, dK, dQ) over the visible pairs: 2.5 x its FLOPs
         i = torch.arange(a.N, dtype=torch.float64)
         hi = i if a.causal else torch.full_like(i, a.N - 1)

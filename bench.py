@@ -454,6 +454,13 @@ def measure_also(A, dev, stream, flush, peaks, reps=10):
     ws = torch.empty((A.attn_bwd_workspace_size(P["B"], P["Hq"], P["N"]) + 3) // 4, dtype=torch.float32, device=dev)
     ms = timed(lambda: A.backward(q, k, v, o, lse, dout, causal=True, workspace=ws), n=max(3, reps // 2))
     out.append(tf_line("gqa_causal_backward_b2_hq32_hkv8_n8192_d128_bf16 (2.5x forward FLOPs)", 2.5 * fl, ms))
+    # the same backward with rotary embeddings (Q and K rotated into the workspace, dQ and dK turned back)
+    A.prefill(q, k, v, causal=True, out=o, lse_out=lse, rope_theta=10000.0)
+    nb = A.attn_bwd_ex_workspace_size(P["B"], P["Hq"], P["Hkv"], P["N"], P["N"], P["D"], A.make_options(rope_theta=10000.0))
+    ws = torch.empty((nb + 15) // 16 * 4, dtype=torch.float32, device=dev)
+    ms = timed(lambda: A.backward(q, k, v, o, lse, dout, causal=True, workspace=ws, rope_theta=10000.0),
+               n=max(3, reps // 2))
+    out.append(tf_line("gqa_causal_backward_n8192_d128 + RoPE (2.5x forward FLOPs)", 2.5 * fl, ms))
     del q, k, v, o, lse, dout, ws
     # B=2 one-token decode step (cache write + decode) replayed from a CUDA graph
     Dc = dict(DECODE, B=2)

@@ -91,7 +91,7 @@ typedef enum {
  *                 on chip; the caller's tensors are not modified.
  *   rope_interleaved  which coordinates form pair c: 0 pairs (c, c + D/2)
  *                 (the "rotate half" layout), 1 pairs (2c, 2c + 1)
- *   rope_rotated_keys  prefill with rope_theta > 0 only: 1 when the keys
+ *   rope_rotated_keys  prefill and backward with rope_theta > 0: 1 when the keys
  *                 passed in are already rotated at their positions (for
  *                 example read back from a cache written by kv_cache_write_ex
  *                 with the same RoPE options); the kernel then rotates only
@@ -271,14 +271,37 @@ attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *
                        float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * attn_bwd with the forward's mask and bias options (see attn_options_t):
- * window_left, window_right, alibi_slopes and kv_ranges, the same as the
- * attn_fwd_prefill_ex call whose O and LSE are passed in (a query row the
- * forward left without keys, O = 0 and LSE = -inf, gets dQ = 0 and adds
- * nothing to dK, dV).  The bias enters the gradients only through P.  Rotary
- * embeddings (rope_theta > 0) are not supported here (ATTN_ERR_UNSUPPORTED);
- * num_splits and prefill_kernel must be 0.  Option errors as for the other
- * *_ex calls.
+ * attn_bwd_ex_workspace_size -- bytes of scratch attn_bwd_ex needs with these
+ * options: attn_bwd_workspace_size(B, H_q, N_q), plus, with rope_theta > 0,
+ * 2 * B * H_q * N_q * D for the rotated queries and -- unless
+ * rope_rotated_keys -- 2 * B * H_kv * N_kv * D for the rotated keys.  Equal to
+ * attn_bwd_workspace_size without rotary embeddings.  Returns 0 on bad
+ * arguments or options.  (A sizing utility of this library.)
+ */
+size_t attn_bwd_ex_workspace_size(int B, int H_q, int H_kv, int N_q, int N_kv, int D, const attn_options_t *opts);
+
+/*
+ * attn_bwd with the forward's mask, bias and position options (see
+ * attn_options_t): window_left, window_right, alibi_slopes, kv_ranges and the
+ * rotary embedding (rope_theta, rope_interleaved, rope_rotated_keys), the same
+ * as the attn_fwd_prefill_ex call whose O and LSE are passed in (a query row
+ * the forward left without keys, O = 0 and LSE = -inf, gets dQ = 0 and adds
+ * nothing to dK, dV).  The bias enters the gradients only through P.
+ *
+ * Rotary embeddings ("Triton-FlashAttention" names RoPE among the fused
+ * extensions): with R the rotation of each row at its position, the forward
+ * is attention(R Q, R K, V), so the gradients with respect to the caller's Q
+ * and K are dQ = R^T dQ', dK = R^T dK', where dQ', dK' are the backward's
+ * gradients with respect to the rotated rows and R^T rotates each pair by the
+ * opposite angle; dV is unchanged.  The call rotates Q (and K) into the
+ * workspace, runs the backward kernels on them and rotates dQ (and dK) back in
+ * place: two more kernels.  With rope_rotated_keys = 1, k holds the rotated
+ * keys and dk receives the gradient with respect to them (not turned back).
+ *
+ *   workspace        attn_bwd_ex_workspace_size() bytes with the same options
+ *
+ * num_splits is ignored; prefill_kernel must be 0.  Option errors as for the
+ * other *_ex calls.
  */
 attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, const void *o, const void *dout,
                           const float *lse, void *dq, void *dk, void *dv, attn_dtype_t dtype, int B, int H_q,

@@ -98,9 +98,11 @@ def attention(q, k, v, causal: bool, scale: float, theta: float, interleaved: bo
 
 
 def attention_bwd(q, k, v, dout, causal: bool, scale: float, theta: float, interleaved: bool = False,
-                  rotated_keys: bool = False, window_left: int = -1, window_right: int = -1, alibi_slopes=None):
+                  rotated_keys: bool = False, window_left: int = -1, window_right: int = -1, alibi_slopes=None,
+                  kv_ranges=None):
     """(dQ, dK, dV) of ``attention`` (queries and keys rotated at their positions) for the incoming
-    gradient dout, in fp64.
+    gradient dout, in fp64; kv_ranges: per-row key ranges as in ``masked.attention_masked``, applied to the
+    rotated rows.
 
     With R the per-row rotation, the forward is attention(R q, R k, v); the gradients of attention with
     respect to its rotated inputs (dQ', dK', dV) come from the backward oracles, and by the chain rule
@@ -112,11 +114,11 @@ def attention_bwd(q, k, v, dout, causal: bool, scale: float, theta: float, inter
     qpos, kpos = np.arange(q.shape[2]), np.arange(k.shape[2])
     qr = rotate(q, qpos, theta, interleaved)
     kr = k if rotated_keys else rotate(k, kpos, theta, interleaved)
-    if _plain(window_left, window_right, alibi_slopes):
+    if _plain(window_left, window_right, alibi_slopes) and kv_ranges is None:
         dqr, dkr, dv = oracle.attention_bwd(qr, kr, v, dout, causal, scale)
     else:
         dqr, dkr, dv = masked.attention_bwd_masked(qr, kr, v, dout, causal, scale, window_left, window_right,
-                                                   alibi_slopes)
+                                                   alibi_slopes, kv_ranges)
     dq = rotate(dqr, -qpos, theta, interleaved)
     dk = dkr if rotated_keys else rotate(dkr, -kpos, theta, interleaved)
     return dq, dk, dv

@@ -251,6 +251,34 @@ def test_bwd_workspace_size():
     assert A.attn_bwd_workspace_size(0, 8, 64) == 0
 
 
+def test_bwd_ex_workspace_size(lib):
+    """Without rotary embeddings the plain size; with them room for the rotated Q (and K unless given rotated)."""
+    plain = A.attn_bwd_workspace_size(2, 8, 64)
+    assert A.attn_bwd_ex_workspace_size(2, 8, 2, 64, 96, 128, None) == plain
+    assert A.attn_bwd_ex_workspace_size(2, 8, 2, 64, 96, 128, A.make_options(window_left=5)) == plain
+    rope = A.make_options(rope_theta=10000.0)
+    assert A.attn_bwd_ex_workspace_size(2, 8, 2, 64, 96, 128, rope) == plain + 2 * 8 * 64 * 128 * 2 + 2 * 2 * 96 * 128 * 2
+    rk = A.make_options(rope_theta=10000.0, rope_rotated_keys=True)
+    assert A.attn_bwd_ex_workspace_size(2, 8, 2, 64, 96, 64, rk) == plain + 2 * 8 * 64 * 64 * 2
+    for args in ((0, 8, 2, 64, 96, 128), (2, 8, 3, 64, 96, 128), (2, 8, 2, 64, 0, 128), (2, 8, 2, 64, 96, 80)):
+        assert A.attn_bwd_ex_workspace_size(*args, rope) == 0
+    assert A.attn_bwd_ex_workspace_size(2, 8, 2, 64, 96, 128, A.AttnOptions(-1, -1, None, -1.0, 0, 0, 0)) == 0
+
+
+def test_bwd_rope_needs_the_larger_workspace(lib):
+    """A workspace of the plain size is too small once rotary embeddings are on (checked before any CUDA call)."""
+    rope = A.make_options(rope_theta=10000.0)
+    n = A.attn_bwd_ex_workspace_size(2, 8, 2, 64, 64, 128, rope)
+    assert A.attn_bwd_ex(P, P, P, P, P, P, P, P, P, A.ATTN_BF16, 2, 8, 2, 64, 64, 128, contig(2, 8, 64, 128),
+                         contig(2, 2, 64, 128), contig(2, 2, 64, 128), contig(2, 8, 64, 128), contig(2, 8, 64, 128),
+                         contig(2, 8, 64, 128), contig(2, 2, 64, 128), contig(2, 2, 64, 128), 1, 0.088, rope, P,
+                         A.attn_bwd_workspace_size(2, 8, 64), None) == A.ATTN_ERR_WORKSPACE
+    assert A.attn_bwd_ex(P, P, P, P, P, P, P, P, P, A.ATTN_BF16, 2, 8, 2, 64, 64, 128, contig(2, 8, 64, 128),
+                         contig(2, 2, 64, 128), contig(2, 2, 64, 128), contig(2, 8, 64, 128), contig(2, 8, 64, 128),
+                         contig(2, 8, 64, 128), contig(2, 2, 64, 128), contig(2, 2, 64, 128), 1, 0.088, rope, P,
+                         n - 1, None) == A.ATTN_ERR_WORKSPACE
+
+
 OPTION_CALLS = {
     "prefill": lambda o: A.attn_fwd_prefill_ex(
         P, P, P, P, None, A.ATTN_BF16, 2, 8, 2, 64, 64, 128, contig(2, 8, 64, 128), contig(2, 2, 64, 128),

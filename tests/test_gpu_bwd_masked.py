@@ -8,8 +8,8 @@ under the bounds of the plain backward tests (max error 2 % of the largest
 reference magnitude, mean error 1 % of the mean magnitude).  Covered: left and
 two-sided windows, causal and not, ALiBi alone and with windows, key ranges
 with empty, full and past-the-end rows, rows that a window leaves without
-keys (dQ = 0), GQA, fp16/bf16, D 64/128, ragged and unequal lengths; rotary
-embeddings are refused, and no options gives the plain kernels' result.
+keys (dQ = 0), GQA, fp16/bf16, D 64/128, ragged and unequal lengths, and no
+options gives the plain kernels' result.  (Rotary embeddings: test_gpu_bwd_rope.)
 """
 from __future__ import annotations
 
@@ -99,21 +99,6 @@ def test_masked_backward_against_oracle(case):
     if name == "rows_without_keys":
         # rows i > N_kv - 1 + window_left see no key: their dQ is exactly zero
         assert torch.count_nonzero(dq[:, :, Nkv + window[0]:]) == 0
-
-
-def test_masked_backward_refuses_rope():
-    import attention_fa2_fwd_gb300 as A
-    q, k, v = (t.cuda() for t in I.prefill_inputs(1, 4, 2, 128, 128, 128, "bf16", seed=1))
-    o, lse = A.prefill(q, k, v, causal=True)
-    opts = A.make_options(rope_theta=10000.0)
-    n = A.attn_bwd_workspace_size(1, 4, 128)
-    ws = torch.empty((n + 3) // 4, dtype=torch.float32, device="cuda")
-    out = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
-    st = A.attn_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), q.data_ptr(), lse.data_ptr(),
-                       out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(), A.ATTN_BF16, 1, 4, 2, 128, 128, 128,
-                       q.stride(), k.stride(), v.stride(), o.stride(), q.stride(), out[0].stride(), out[1].stride(),
-                       out[2].stride(), 1, 0.088, opts, ws.data_ptr(), n, None)
-    assert st == A.ATTN_ERR_UNSUPPORTED
 
 
 def test_masked_backward_without_options_matches_plain():

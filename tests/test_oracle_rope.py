@@ -222,8 +222,8 @@ def _fd_check(R, grads, loss, base, what):
 
 def check_bwd_matches_finite_differences(R):
     """Gradients of the rotary attention against central finite differences through ``attention`` (both
-    pair layouts, causal and windowed + ALiBi) and, with keys given rotated, through attention of the
-    rotated queries over those keys."""
+    pair layouts, causal and windowed + ALiBi, key ranges) and, with keys given rotated, through attention of
+    the rotated queries over those keys."""
     r = _rng("bwd-fd")
     B, Hq, Hkv, Nq, Nkv, D = 1, 2, 1, 4, 6, 4
     q, k, v = r.normal(size=(B, Hq, Nq, D)), r.normal(size=(B, Hkv, Nkv, D)), r.normal(size=(B, Hkv, Nkv, D))
@@ -237,6 +237,15 @@ def check_bwd_matches_finite_differences(R):
             o, _ = R.attention(q, k, v, causal, 0.7, 100.0, inter, **kw)
             return float(np.sum(o * g))
         _fd_check(R, {"q": dq, "k": dk, "v": dv}, loss, base, f"inter={inter}")
+    kr = np.array([[[0, 3], [2, 6], [1, 1], [0, 6]]], dtype=np.int32)  # one row without keys
+    dq, dk, dv = R.attention_bwd(q, k, v, g, False, 0.7, 100.0, True, kv_ranges=kr)
+
+    def loss_ranges(q, k, v):
+        o, _ = masked.attention_masked(R.rotate(q, np.arange(Nq), 100.0, True), R.rotate(k, np.arange(Nkv), 100.0,
+                                                                                          True), v, False, 0.7,
+                                       kv_ranges=kr)
+        return float(np.sum(o * g))
+    _fd_check(R, {"q": dq, "k": dk, "v": dv}, loss_ranges, base, "key ranges")
     dq, dk, dv = R.attention_bwd(q, k, v, g, True, 0.7, 100.0, False, rotated_keys=True)
 
     def loss_rk(q, k, v):
