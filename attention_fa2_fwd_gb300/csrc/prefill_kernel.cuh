@@ -104,10 +104,11 @@ struct Cfg {
   // barrier indices
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 1;                       // + K stage
+  // K stage released: K_j is free, and so is V_{j-1} (every product that
+  // reads V_{j-1} is issued before the release of K_j, so one commit frees both)
   static constexpr int B_KE = B_KF + KST;              // + K stage
   static constexpr int B_VF = B_KE + KST;              // + V stage
-  static constexpr int B_VE = B_VF + VST;              // + V stage
-  static constexpr int B_SF = B_VE + VST;              // + tile (2): S_i(j) computed
+  static constexpr int B_SF = B_VF + VST;              // + tile (2): S_i(j) computed
   static constexpr int B_PF = B_SF + 2;                // + tile (2): P_i(j) stored (and O_i rescaled)
   static constexpr int B_OD = B_PF + 2;                // + tile (2): last P_i V done
   static constexpr int B_DONE = B_OD + 2;              // every MMA completed
@@ -292,10 +293,7 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
       mbar_init(BAR(C::B_KF + s), 1);
       mbar_init(BAR(C::B_KE + s), 1);
     }
-    for (int s = 0; s < VST; ++s) {
-      mbar_init(BAR(C::B_VF + s), 1);
-      mbar_init(BAR(C::B_VE + s), 1);
-    }
+    for (int s = 0; s < VST; ++s) mbar_init(BAR(C::B_VF + s), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(C::B_SF + i), 1);
       mbar_init(BAR(C::B_PF + i), 4);  // one arrival per softmax warp
@@ -358,8 +356,16 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
           }
           return true;
         };
+        // V tile number issued_v (counted over the whole walk) reuses the stage
+        // of V tile issued_v - VST, which is released with K tile m =
+        // issued_v - VST + 1 (already loaded: K runs level with or ahead of V).
+        // Its release barrier cannot be a phase further on: that would need K
+        // tile m + KST, which is not loaded yet.
         auto load_v = [&](const Unit &U, int j) -> bool {
-          if (issued_v >= VST && !mbar_wait(BAR(C::B_VE + vst), vph ^ 1, abort_flag, p.err)) return false;
+          if (issued_v >= VST) {
+            const int m = issued_v - VST + 1;
+            if (!mbar_wait(BAR(C::B_KE + m % KST), (m / KST) & 1, abort_flag, p.err)) return false;
+          }
           mbar_arrive_expect_tx(BAR(C::B_VF + vst), C::KV_BYTES);
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c)
@@ -541,14 +547,13 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
             const uint32_t kph1 = kst1 == 0 ? kph ^ 1 : kph;  // and its phase
             const bool h0n = j + 1 >= lo0 && j + 1 < hi0;  // tile 0 uses KV tile j + 1
             if (h1p) {
-              // O1 += P1_{j-1} V_{j-1}: tile 1 is the last user of V_{j-1}, so its stage is released
+              // O1 += P1_{j-1} V_{j-1}: tile 1 is the last user of V_{j-1} (released with K_j below)
               if (!(ok = mbar_wait(BAR(C::B_PF + 1), pf1, abort_flag, p.err))) break;
               pf1 ^= 1;
               if (!v_waited && !(ok = wait_v(j - 1, vsp, vpph))) break;
               tc_fence_after();
               issue_pv(1, first1, dv + vsp * kStage16);
               first1 = false;
-              tc_commit(BAR(C::B_VE + vsp));
             }
             if (h1) {
               if constexpr (ROPE) {
@@ -557,7 +562,7 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
               tc_fence_after();
               issue_s(1, dq1, dk + kst * kStage16);
             }
-            tc_commit(BAR(C::B_KE + kst));  // both S products that read K_j are issued
+            tc_commit(BAR(C::B_KE + kst));  // both S products that read K_j, and every P V of V_{j-1}, are issued
             v_waited = false;
             if (j + 1 < J1 && !(ok = mbar_wait(BAR(kKReady + kst1), kph1, abort_flag, p.err))) break;
             if (h0) {
@@ -569,13 +574,11 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
               tc_fence_after();
               issue_pv(0, first0, dv + vst * kStage16);
               first0 = false;
-              if (!h1) tc_commit(BAR(C::B_VE + vst));  // tile 1 does not use V_j
               if (j == hi0 - 1) tc_commit(BAR(C::B_OD + 0));
             } else if (!h1) {
               // A tile between the two bands: nothing reads V_j.  Its copy must land
-              // before the stage is handed back for the next one.
+              // before the stage is handed back (with K_{j+1}) for the next one.
               if (!(ok = wait_v(j, vst, vph))) break;
-              tc_commit(BAR(C::B_VE + vst));
             }
             if (j + 1 < J1 && h0n) {
               tc_fence_after();
@@ -600,7 +603,6 @@ __global__ void __launch_bounds__(kThreadsFor<ROPE>, 1)
               pf1 ^= 1;
               tc_fence_after();
               issue_pv(1, first1, dv + vsp * kStage16);
-              tc_commit(BAR(C::B_VE + vsp));
               tc_commit(BAR(C::B_OD + 1));
             }
           }
