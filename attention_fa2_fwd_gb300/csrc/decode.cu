@@ -433,23 +433,50 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// Merge of one (b, q head): O = sum_s w_s O_s / sum_s w_s and LSE = M + ln
+// sum_s w_s, with w_s = exp(lse_s - M) and M the largest partial LSE.  One
+// thread per output column.  Each partial LSE is read by one thread (nsplit <=
+// 64 <= D) and the weights are shared, and the partial outputs are read in
+// batches of 8 independent loads: a handful of memory round trips, not two
+// per split.  The sums run in split order, as a plain loop would.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(D) decode_merge_kernel(const DecodeParams p) {
+  constexpr int kWarps = D / 32;
+  __shared__ float w_s[64];
+  __shared__ float red[kWarps];
+  __shared__ int stop;
   griddep_wait();
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, hq = bh % p.Hq;
-  const int d = threadIdx.x;
-  if (load_volatile(p.err) != 0) return;
-  const float *ls = p.ws_lse + static_cast<int64_t>(bh) * p.nsplit;
-  const float *os = p.ws_o + static_cast<int64_t>(bh) * p.nsplit * D;
-  float M = -INFINITY;
-  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, ls[s]);
+  const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+  if (d == 0) stop = load_volatile(p.err) != 0;
+  __syncthreads();
+  if (stop) return;
+  const int nsplit = p.nsplit;
+  const float *ls = p.ws_lse + static_cast<int64_t>(bh) * nsplit;
+  const float *os = p.ws_o + static_cast<int64_t>(bh) * nsplit * D;
+  const float l = d < nsplit ? ls[d] : -INFINITY;
+  float m = l;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w]);
+  if (d < nsplit) w_s[d] = M == -INFINITY ? 0.f : expf(l - M);
+  __syncthreads();
   float W = 0.f, A = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < p.nsplit; ++s) {
-      const float w = expf(ls[s] - M);
-      W += w;
-      A = fmaf(w, os[static_cast<int64_t>(s) * D + d], A);
+  for (int s0 = 0; s0 < nsplit; s0 += 8) {
+    float o8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o8[i] = s0 + i < nsplit ? os[static_cast<int64_t>(s0 + i) * D + d] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (s0 + i < nsplit) {
+        W += w_s[s0 + i];
+        A = fmaf(w_s[s0 + i], o8[i], A);
+      }
     }
   }
   store_out<BF16>(p.o, static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(hq) * p.o_sh + d,
@@ -611,6 +638,7 @@ cudaError_t launch_split(const CUtensorMap &tk, const CUtensorMap &tv, const Dec
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   dim3 grid(p.nsplit, Hkv * p.nhc, B);
+  if (p.nsplit > 64 || p.nsplit > D) return cudaErrorInvalidValue;  // the merge holds one weight per thread
   e = launch_serialized(kern, grid, dim3(kThreads), C::SMEM_BYTES, stream, tk, tv, p);
   if (e != cudaSuccess || p.nsplit == 1) return e;
   return launch_serialized(decode_merge_kernel<D, BF16>, dim3(B * p.Hq), dim3(D), 0, stream, p);
