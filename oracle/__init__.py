@@ -26,6 +26,11 @@ Definitions followed (see the header of ``attn_oracle.c`` for the steps):
   GQA backward that sums dK, dV over a group): with the explicit weights P,
   dV = P^T dO, dP = dO V^T, dS = P o (dP - rowsum(dO o O)), dQ = scale dS K,
   dK = scale dS^T Q, dK and dV summed over the q heads of each kv head.
+* ``attention_bwd_dq_rows``, ``attention_bwd_dkv_rows``: selected rows of the
+  same gradients, by the same definitions restricted to those rows (a query
+  row's dQ needs only its own weights; a key row's dK, dV need the weights of
+  every query row of every q head of the group, whose row sums are formed in
+  blocks of query rows), for inputs too large for ``attention_bwd``.
 * ``gather_pages``, ``decode_paged``, ``kv_cache_write_paged``: the paged,
   per-request-length decode that "Triton-FlashAttention" lists as deferred
   work (Deferred / explicitly out of scope).  Row t of request b's cache is row
@@ -195,6 +200,53 @@ def kv_cache_write(k_cache, v_cache, k_new, v_new, pos: int):
     kc[:, :, pos:pos + n, :] = k_new
     vc[:, :, pos:pos + n, :] = v_new
     return kc, vc
+
+
+def attention_bwd_dq_rows(q, k, v, dout, causal: bool, scale: float, b: int, h: int, rows):
+    """dQ[b, h, rows, :] of ``attention_bwd``, each row from its own weights, in fp64."""
+    hk = h // (q.shape[1] // k.shape[1])
+    q, k, v, dout = _f64(q[b, h]), _f64(k[b, hk]), _f64(v[b, hk]), _f64(dout[b, h])
+    Nkv = k.shape[0]
+    out = np.zeros((len(rows), q.shape[1]))
+    for n, i in enumerate(rows):
+        s = scale * (k @ q[i])
+        if causal:
+            s = np.where(np.arange(Nkv) > i, -np.inf, s)
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        dp = v @ dout[i]
+        ds = p * (dp - dout[i] @ (p @ v))
+        out[n] = scale * (ds @ k)
+    return out
+
+
+def attention_bwd_dkv_rows(q, k, v, dout, causal: bool, scale: float, b: int, hk: int, keys, block: int = 512):
+    """dK[b, hk, keys, :] and dV[b, hk, keys, :] of ``attention_bwd`` (summed over the q heads of kv
+    head hk), in fp64.  The weights P[i, keys] need every query row's full softmax; rows are taken
+    ``block`` at a time."""
+    keys = np.asarray(keys)
+    Hq, Hkv = q.shape[1], k.shape[1]
+    g = Hq // Hkv
+    kk, vv = _f64(k[b, hk]), _f64(v[b, hk])
+    Nq, Nkv, D = q.shape[2], kk.shape[0], kk.shape[1]
+    dk = np.zeros((len(keys), D))
+    dv = np.zeros((len(keys), D))
+    for h in range(hk * g, (hk + 1) * g):
+        qh, gh = _f64(q[b, h]), _f64(dout[b, h])
+        for i0 in range(0, Nq, block):
+            qb, gb = qh[i0:i0 + block], gh[i0:i0 + block]
+            s = scale * (qb @ kk.T)
+            if causal:
+                s = np.where(np.arange(Nkv)[None, :] > np.arange(i0, i0 + len(qb))[:, None], -np.inf, s)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            o = p @ vv
+            pk = p[:, keys]
+            dpk = gb @ vv[keys].T
+            dsk = pk * (dpk - (gb * o).sum(axis=1, keepdims=True))
+            dv += pk.T @ gb
+            dk += scale * (dsk.T @ qb)
+    return dk, dv
 
 
 def gather_pages(pages, block_table_row, length: int):

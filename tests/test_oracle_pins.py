@@ -557,3 +557,23 @@ def test_bwd_rows_of_ds_sum_to_zero():
     for causal in (False, True):
         _, dk, _ = oracle.attention_bwd(q, k, v, g, causal, 0.9)
         np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_sampled_rows_equal_full_backward(causal):
+    """The sampled-row gradients equal the pinned full backward on every row and key (GQA, unequal lengths,
+    blocks of query rows smaller than N_q)."""
+    r = _rng("bwdrows", causal)
+    B, Hq, Hkv, Nq, Nkv, D, scale = 2, 6, 2, 11, 13, 5, 0.6
+    q, k, v = r.normal(size=(B, Hq, Nq, D)), r.normal(size=(B, Hkv, Nkv, D)), r.normal(size=(B, Hkv, Nkv, D))
+    g = r.normal(size=(B, Hq, Nq, D))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, causal, scale)
+    for b in range(B):
+        for h in range(Hq):
+            np.testing.assert_allclose(oracle.attention_bwd_dq_rows(q, k, v, g, causal, scale, b, h, range(Nq)),
+                                       dq[b, h], rtol=0, atol=1e-12)
+        for hk in range(Hkv):
+            keys = [12, 0, 5, 6]
+            rk, rv = oracle.attention_bwd_dkv_rows(q, k, v, g, causal, scale, b, hk, keys, block=4)
+            np.testing.assert_allclose(rk, dk[b, hk, keys], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(rv, dv[b, hk, keys], rtol=0, atol=1e-12)
