@@ -50,6 +50,8 @@ CASES = [
     (1, 4, 1, 100, 300, 64, True, "bf16"),
     (1, 4, 4, 300, 100, 128, True, "f16"),
     (1, 16, 4, 1024, 1024, 128, True, "bf16"),
+    (1, 32, 1, 385, 385, 64, True, "f16"),       # MQA: every q head's dK, dV summed into one kv head
+    (2, 8, 8, 129, 640, 128, False, "bf16"),     # more keys than queries, one row past a tile
 ]
 
 
