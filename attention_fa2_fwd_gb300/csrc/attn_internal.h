@@ -164,10 +164,12 @@ struct BwdMaps {
   CUtensorMap q, dout, k, v;  // 4-D tiled maps, 64 x 128 boxes, 128-byte swizzle
 };
 // masked: a window, ALiBi slopes or key ranges are set (the MASKED build).
+// side: a second stream for the dK/dV kernel (null: everything on stream);
+// stream waits for it before returning work.
 cudaError_t launch_bwd(int D, bool causal, bool bf16, bool masked, const BwdMaps &m, const BwdParams &p, int B,
-                       int Hkv, cudaStream_t stream);
+                       int Hkv, cudaStream_t stream, cudaStream_t side);
 cudaError_t launch_bwd_masked(int D, bool causal, bool bf16, const BwdMaps &m, const BwdParams &p, int B, int Hkv,
-                              cudaStream_t stream);
+                              cudaStream_t stream, cudaStream_t side);
 
 // Rotary embedding of whole rows (rope_rows.cu): job j rotates the (B, H, N, D)
 // 16-bit tensor src into dst (the same place for an in-place rotation), the row

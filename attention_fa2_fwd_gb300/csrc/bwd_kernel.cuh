@@ -792,11 +792,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, bool CAUSAL, bool BF16, bool MASKED>
-cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv, cudaStream_t stream) {
+// The dQ and the dK/dV kernels depend only on the preprocess (D_i), not on each
+// other.  Each CTA of either holds all of an SM's TMEM, so they share SMs CTA by
+// CTA: with a second stream (side, if given) the dK/dV kernel runs beside the
+// dQ kernel, and each fills the other's last partial waves.  The caller's stream
+// waits for the side stream at the end.
+cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv, cudaStream_t stream,
+                           cudaStream_t side) {
   constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
   bwd_preprocess_kernel<D, BF16><<<dim3((p.Nq + kRowsPerBlock - 1) / kRowsPerBlock, p.Hq, B), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  const bool two = side != nullptr && side != stream;
+  cudaEvent_t ev = nullptr;
+  if (two) {
+    if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+    e = cudaEventRecord(ev, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ev, 0);
+    cudaEventDestroy(ev);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = bwd_dkdv_kernel<D, CAUSAL, BF16, MASKED>;
+    constexpr uint32_t smem = DkvCfg<D>::SMEM_BYTES;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
+        cudaSuccess)
+      return e;
+    kern<<<dim3(Hkv * B * ((p.Nkv + kT - 1) / kT)), kThreads, smem, two ? side : stream>>>(m.q, m.dout, m.k, m.v,
+                                                                                           p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   {
     auto kern = bwd_dq_kernel<D, CAUSAL, BF16, MASKED>;
     constexpr uint32_t smem = DqCfg<D>::SMEM_BYTES;
@@ -806,14 +831,11 @@ cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv,
     kern<<<dim3(p.Hq * B * ((p.Nq + kT - 1) / kT)), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  {
-    auto kern = bwd_dkdv_kernel<D, CAUSAL, BF16, MASKED>;
-    constexpr uint32_t smem = DkvCfg<D>::SMEM_BYTES;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
-        cudaSuccess)
-      return e;
-    kern<<<dim3(Hkv * B * ((p.Nkv + kT - 1) / kT)), kThreads, smem, stream>>>(m.q, m.dout, m.k, m.v, p);
-    e = cudaGetLastError();
+  if (two) {
+    if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+    e = cudaEventRecord(ev, side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev, 0);
+    cudaEventDestroy(ev);
   }
   return e;
 }
@@ -821,9 +843,9 @@ cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv,
 // Dispatch over D, causal and dtype for one value of MASKED.
 template <bool MASKED>
 cudaError_t launch_bwd_variant(int D, bool causal, bool bf16, const BwdMaps &m, const BwdParams &p, int B, int Hkv,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, cudaStream_t side) {
 #define ATTN_BWD_CASE(DD, CC, BB) \
-  if (D == DD && causal == CC && bf16 == BB) return launch_bwd_one<DD, CC, BB, MASKED>(m, p, B, Hkv, stream);
+  if (D == DD && causal == CC && bf16 == BB) return launch_bwd_one<DD, CC, BB, MASKED>(m, p, B, Hkv, stream, side);
   ATTN_BWD_CASE(128, true, true)
   ATTN_BWD_CASE(128, false, true)
   ATTN_BWD_CASE(128, true, false)

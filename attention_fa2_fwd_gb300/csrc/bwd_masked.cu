@@ -5,8 +5,8 @@
 namespace attn {
 
 cudaError_t launch_bwd_masked(int D, bool causal, bool bf16, const BwdMaps &m, const BwdParams &p, int B, int Hkv,
-                              cudaStream_t stream) {
-  return launch_bwd_variant<true>(D, causal, bf16, m, p, B, Hkv, stream);
+                              cudaStream_t stream, cudaStream_t side) {
+  return launch_bwd_variant<true>(D, causal, bf16, m, p, B, Hkv, stream, side);
 }
 
 }  // namespace attn
