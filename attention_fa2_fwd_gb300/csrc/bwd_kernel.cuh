@@ -116,7 +116,11 @@ __device__ __forceinline__ float dot8(const uint4 &a, const uint4 &b) {
 }
 
 // D_i = sum_d dO[i, d] * O[i, d] in fp32.  D / 8 lanes per row, one 16-byte
-// load of each tensor per lane, so a warp reads 32 / (D / 8) whole rows at once.
+// load of each tensor per lane and row, so a warp reads 32 / (D / 8) whole rows
+// at once; each warp takes kPreRowGroups such groups of consecutive rows and
+// issues all their loads before the first use (more bytes in flight per
+// thread, fewer blocks).
+constexpr int kPreRowGroups = 4;
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
   constexpr int kLanesPerRow = D / 8;
@@ -124,21 +128,29 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   if (load_volatile(p.err) != 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y, b = blockIdx.z;
-  const int row = (blockIdx.x * 8 + warp) * kRowsPerWarp + lane / kLanesPerRow;
+  const int row0 = (blockIdx.x * 8 + warp) * kRowsPerWarp * kPreRowGroups + lane / kLanesPerRow;
   const int part = lane % kLanesPerRow;
-  float acc = 0.f;
-  if (row < p.Nq) {
-    const int64_t oo = static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
-                       static_cast<int64_t>(row) * p.o_sn + part * 8;
-    const int64_t od = static_cast<int64_t>(b) * p.do_sb + static_cast<int64_t>(h) * p.do_sh +
-                       static_cast<int64_t>(row) * p.do_sn + part * 8;
-    const uint4 o = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.o) + oo);
-    const uint4 g = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.dout) + od);
-    acc = dot8<BF16>(o, g);
+  const int64_t ob = static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(h) * p.o_sh + part * 8;
+  const int64_t db = static_cast<int64_t>(b) * p.do_sb + static_cast<int64_t>(h) * p.do_sh + part * 8;
+  uint4 o[kPreRowGroups], g[kPreRowGroups];
+#pragma unroll
+  for (int it = 0; it < kPreRowGroups; ++it) {
+    const int row = row0 + it * kRowsPerWarp;
+    if (row < p.Nq) {
+      o[it] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.o) + ob +
+                                               static_cast<int64_t>(row) * p.o_sn);
+      g[it] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.dout) + db +
+                                               static_cast<int64_t>(row) * p.do_sn);
+    }
   }
 #pragma unroll
-  for (int off = kLanesPerRow / 2; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (part == 0 && row < p.Nq) p.dvec[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row] = acc;
+  for (int it = 0; it < kPreRowGroups; ++it) {
+    const int row = row0 + it * kRowsPerWarp;
+    float acc = row < p.Nq ? dot8<BF16>(o[it], g[it]) : 0.f;
+#pragma unroll
+    for (int off = kLanesPerRow / 2; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (part == 0 && row < p.Nq) p.dvec[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + row] = acc;
+  }
 }
 
 // ---------------------------------------------------------------- dQ
@@ -799,7 +811,7 @@ template <int D, bool CAUSAL, bool BF16, bool MASKED>
 // waits for the side stream at the end.
 cudaError_t launch_bwd_one(const BwdMaps &m, const BwdParams &p, int B, int Hkv, cudaStream_t stream,
                            cudaStream_t side) {
-  constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
+  constexpr int kRowsPerBlock = 8 * (32 / (D / 8)) * kPreRowGroups;
   bwd_preprocess_kernel<D, BF16><<<dim3((p.Nq + kRowsPerBlock - 1) / kRowsPerBlock, p.Hq, B), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
