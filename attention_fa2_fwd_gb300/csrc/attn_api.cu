@@ -31,6 +31,11 @@ struct DeviceState {
   int pair_clusters = 0;  // CTA-pair prefill clusters resident at once (0: pair kernel not used)
   unsigned *err = nullptr;
   unsigned *taken = nullptr;
+  // Library-owned stream on which the backward's dK/dV kernel runs beside its
+  // dQ kernel (event-ordered against the caller's stream).  Created with the
+  // rest of the per-device state, so that a backward captured into a CUDA graph
+  // after any earlier call on the device creates nothing during the capture.
+  cudaStream_t side = nullptr;
 };
 
 std::mutex g_mutex;
@@ -72,6 +77,7 @@ attn_status_t device_state(const DeviceState **out) {
         g_encode = reinterpret_cast<EncodeTiledFn>(fn);
       }
       s.pair_clusters = prefill_pair_max_clusters();
+      if (cudaStreamCreateWithFlags(&s.side, cudaStreamNonBlocking) != cudaSuccess) return ATTN_ERR_CUDA;
     }
     s.ready = true;
   }
@@ -502,34 +508,6 @@ attn_status_t attn_fwd_prefill_varlen_ex(const void *q, const void *k, const voi
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-}  // extern "C"
-
-namespace attn {
-namespace {
-// A library-owned stream per device on which the backward's dK/dV kernel runs
-// beside its dQ kernel (ordered by events against the caller's stream).
-std::mutex g_side_mutex;
-cudaStream_t g_side[kMaxDevices] = {};
-}  // namespace
-}  // namespace attn
-
-extern "C" {
-
-namespace {
-attn_status_t bwd_side_stream(cudaStream_t *side) {
-  using namespace attn;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_side_mutex);
-  if (g_side[dev] == nullptr && cudaStreamCreateWithFlags(&g_side[dev], cudaStreamNonBlocking) != cudaSuccess) {
-    g_side[dev] = nullptr;
-    return ATTN_ERR_CUDA;
-  }
-  *side = g_side[dev];
-  return ATTN_OK;
-}
-}  // namespace
-
 size_t attn_bwd_workspace_size(int B, int H_q, int N_q) {
   if (B < 1 || H_q < 1 || N_q < 1) return 0;
   return (static_cast<size_t>(B) * H_q * N_q * sizeof(float) + 15) & ~size_t(15);
@@ -678,9 +656,7 @@ attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, const voi
     e = launch_rope_rows(D, bf16, op.rope_interleaved != 0, rp, rotate_k ? 2 : 1, s);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
   }
-  cudaStream_t side = nullptr;
-  if ((st = bwd_side_stream(&side)) != ATTN_OK) return st;
-  e = launch_bwd(D, causal != 0, bf16, masked, m, p, B, H_kv, s, side);
+  e = launch_bwd(D, causal != 0, bf16, masked, m, p, B, H_kv, s, dev->side);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   if (rope) {
     // dQ = R^T dQ', dK = R^T dK' (dK' itself when the keys came rotated).

@@ -265,8 +265,10 @@ size_t attn_bwd_workspace_size(int B, int H_q, int N_q);
  * current device that starts after D_i and that `stream` waits for (event
  * dependencies), so the two independent kernels share the GPU.  All work of the
  * call is complete once the work enqueued on `stream` so far is; a CUDA graph
- * captured on `stream` includes it.  Concurrent calls from several host threads
- * share that stream (their dK/dV kernels run one after another).
+ * captured on `stream` includes it (the library stream is created by the first
+ * call of any kind on the device, which must precede the capture).  Concurrent
+ * calls from several host threads share that stream (their dK/dV kernels run
+ * one after another).
  */
 attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
                        const float *lse, void *dq, void *dk, void *dv, attn_dtype_t dtype, int B, int H_q, int H_kv,

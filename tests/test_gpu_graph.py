@@ -100,3 +100,45 @@ def test_paged_decode_step_replayed_from_a_cuda_graph():
     lens = (start + steps).numpy()
     o_ref, lse_ref = oracle.decode_paged(np64(q_all[steps - 1]), kp_h, vp_h, table.numpy(), lens, 1 / math.sqrt(D))
     assert_close(graphed["o"], o_ref, graphed["lse"], lse_ref, "graph replay vs oracle")
+
+
+def test_backward_replayed_from_a_cuda_graph():
+    """attn_bwd captured into a CUDA graph (after an earlier call on the device): its dK/dV kernel runs on the
+    library's second stream, joined to the captured stream by events, and every replay reproduces the eager
+    gradients bit for bit (the backward is deterministic); new inputs copied into the captured buffers give
+    their own gradients."""
+    import attention_fa2_fwd_gb300 as A
+    from attention_fa2_fwd_gb300 import inputs as I
+    B, Hq, Hkv, N, D = 1, 8, 2, 640, 128
+    q, k, v = (t.cuda() for t in I.prefill_inputs(B, Hq, Hkv, N, N, D, "bf16", seed=90))
+    dout = torch.randn_like(q)
+    o, lse = A.prefill(q, k, v, causal=True)  # the first call on the device happens before the capture
+    n = A.attn_bwd_workspace_size(B, Hq, N)
+    ws = torch.empty((n + 15) // 16 * 4, dtype=torch.float32, device="cuda")
+    eager = A.backward(q, k, v, o, lse, dout, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            captured = A.backward(q, k, v, o, lse, dout, causal=True, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    A.check_device_error()
+    for x, y in zip(captured, eager):
+        assert torch.equal(x, y)
+    # new inputs in the captured buffers
+    q2, k2, v2 = (t.cuda() for t in I.prefill_inputs(B, Hq, Hkv, N, N, D, "bf16", seed=91))
+    o2, lse2 = A.prefill(q2, k2, v2, causal=True)
+    g2 = torch.randn_like(q2)
+    ref = A.backward(q2, k2, v2, o2, lse2, g2, causal=True)
+    for dst, src in ((q, q2), (k, k2), (v, v2), (o, o2), (lse, lse2), (dout, g2)):
+        dst.copy_(src)
+    graph.replay()
+    torch.cuda.synchronize()
+    A.check_device_error()
+    for x, y in zip(captured, ref):
+        assert torch.equal(x, y)
