@@ -462,6 +462,35 @@ def measure_also(A, dev, stream, flush, peaks, reps=10):
                n=max(3, reps // 2))
     out.append(tf_line("gqa_causal_backward_n8192_d128 + RoPE (2.5x forward FLOPs)", 2.5 * fl, ms))
     del q, k, v, o, lse, dout, ws
+    # variable-length prefill: 16 packed causal sequences, lengths uniform in [N/8, N] (seeded)
+    lens = torch.randint(P["N"] // 8, P["N"] + 1, (16,), generator=torch.Generator().manual_seed(11)).tolist()
+    tq = sum(lens)
+    q, k, v = randn(tq, P["Hq"], P["D"]), randn(tq, P["Hkv"], P["D"]), randn(tq, P["Hkv"], P["D"])
+    cu = torch.tensor([0] + torch.tensor(lens).cumsum(0).tolist(), dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    ms = timed(lambda: A.prefill_varlen(q, k, v, cu, cu, max(lens), max(lens), causal=True, out=o,
+                                        return_lse=False))
+    pairs = sum(n * (n + 1) // 2 for n in lens)
+    out.append(tf_line(f"varlen_causal_prefill_16_seqs_{min(lens)}..{max(lens)}_tokens_hq32_hkv8_d128 "
+                       f"(FLOPs over the visible pairs)", 4.0 * P["Hq"] * P["D"] * pairs, ms))
+    del q, k, v, o
+    # paged decode: B=64 requests of 8192 cached tokens in 16-token pages of a shuffled pool
+    Dc = DECODE
+    ps = 16
+    max_pages = Dc["L"] // ps
+    kp, vp = randn(Dc["B"] * max_pages, Dc["Hkv"], ps, Dc["D"]), randn(Dc["B"] * max_pages, Dc["Hkv"], ps, Dc["D"])
+    table = torch.randperm(Dc["B"] * max_pages, generator=torch.Generator().manual_seed(7)).to(torch.int32)
+    table = table.view(Dc["B"], max_pages).to(dev)
+    lens_d = torch.full((Dc["B"],), Dc["L"], dtype=torch.int32, device=dev)
+    qd = randn(Dc["B"], Dc["Hq"], Dc["D"])
+    od = torch.empty_like(qd)
+    wsd = A.decode_workspace(Dc["B"], Dc["Hq"], Dc["Hkv"], Dc["D"], dev)
+    ms = timed(lambda: A.decode_paged(qd, kp, vp, table, lens_d, Dc["L"], out=od, return_lse=False, workspace=wsd))
+    kvb = decode_bytes(Dc["B"], Dc["Hkv"], Dc["L"], Dc["D"])
+    out.append({"workload": "paged_decode_b64_hq32_hkv8_l8192_d128_bf16, 16-token pages, shuffled pool",
+                "value": round(kvb / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms": round(ms, 4),
+                "frac": round(kvb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)})
+    del kp, vp, table, lens_d, qd, od, wsd
     # B=2 one-token decode step (cache write + decode) replayed from a CUDA graph
     Dc = dict(DECODE, B=2)
     kc, vc = randn(2, Dc["Hkv"], Dc["L"], Dc["D"]), randn(2, Dc["Hkv"], Dc["L"], Dc["D"])
